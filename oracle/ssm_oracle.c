@@ -1,0 +1,216 @@
+/*
+ * ssm_oracle.c -- fp64 CPU oracle for the selective-scan forward and the
+ * single-token state update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * What it computes (plain definition, no blocking, fusion or reordering):
+ *
+ *   for every batch row b and channel d, with h[n] = h0[b,d,n] (or 0):
+ *     for l = 0 .. L-1:
+ *       x     = delta[b,d,l] + bias[d]
+ *       dt    = softplus(x)  (or x when softplus is off)
+ *       for n:
+ *         Abar  = exp(dt * A[d,n])
+ *         coef  = (exp(dt*A) - 1) / A[d,n]      (coef = dt when A[d,n] == 0)
+ *         h[n]  = Abar * h[n] + coef * B[b,n,l] * u[b,d,l]
+ *       y     = sum_n C[b,n,l] * h[n] + D[d] * u[b,d,l]
+ *       y    *= silu(z[b,d,l])                  (when z is given)
+ *     h_last[b,d,:] = h
+ *
+ * Passages followed:
+ *  - zero-order-hold discretisation Abar = exp(dA), Bbar = (dA)^-1 (exp(dA) - I) dB:
+ *    velog review of "Mamba: Linear-Time Sequence Modeling with Selective
+ *    State Spaces", section 2 "Discretization"; the derivation and the
+ *    invertibility condition on A are in "mamba 学习" (fakeeyes2wo), section
+ *    "MAMBA" (integral of e^{A tau} = A^-1 (e^{A dt} - I)).  For diagonal A the
+ *    matrix expression is elementwise, giving coef above; its A -> 0 limit is dt.
+ *  - recurrence h_k = Abar h_{k-1} + Bbar x_k, y_k = C h_k (inclusive
+ *    convention): velog review, section 2 "Discretization", item 3.
+ *  - D skip y += D x: "mamba 学习", section "SSM 状态空间模型" (output equation)
+ *    and Mamba_Model_Report.md section 4.2 (y = y + D * x).
+ *  - gate y * silu(z), applied after the D skip: Mamba_Model_Report.md section 3
+ *    (MambaBlock.forward: z = silu(z); output = y * z).
+ *  - dt = softplus(raw + bias): "Mamba学习记录" (lengnian), section "怎么增加选择性"
+ *    (tau_delta = softplus) and velog review section 3.2 (broadcast, add the
+ *    parameter, softplus).
+ *  - h starts at zero: Mamba_Model_Report.md section 4.2 (selective_scan_seq
+ *    starts from torch.zeros) and "mamba 学习" (h_0 = 0).
+ *  - decode step: Mamba_Model_Report.md section 6 (ssm_step: h = deltaA * h + BX;
+ *    y = h @ C + D * x), with the same discretisation.
+ *
+ * Pinned by tests/test_oracle_pins.py against brute-force unrolled sums,
+ * the LTI convolution form, a geometric-series closed form, the A -> 0 limit,
+ * linearity in u, step/scan equivalence and split invariance.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(x) = log(1 + e^x), in a form that neither overflows nor loses
+ * the small-x tail. */
+static double oracle_softplus(double x)
+{
+    if (x > 0.0)
+        return x + log1p(exp(-x));
+    return log1p(exp(x));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^{-z}) */
+static double oracle_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* One recurrence step for channel (b, d) at one position.
+ * h has dstate entries; B_col/C_col are the dstate values of B and C at this
+ * position, read with stride `bc_stride` between consecutive n. */
+static double oracle_step(int64_t dstate, double* h, double u, double delta_raw,
+                          double bias, int delta_softplus, const double* A_row,
+                          const double* B_col, const double* C_col, int64_t bc_stride,
+                          double Dd, const double* z)
+{
+    double x = delta_raw + bias;
+    double dt = delta_softplus ? oracle_softplus(x) : x;
+    double acc = 0.0;
+    for (int64_t n = 0; n < dstate; ++n) {
+        double a = A_row[n];
+        double Abar = exp(dt * a);
+        double coef = (a == 0.0) ? dt : expm1(dt * a) / a;
+        h[n] = Abar * h[n] + coef * B_col[n * bc_stride] * u;
+        acc += C_col[n * bc_stride] * h[n];
+    }
+    double y = acc + Dd * u;
+    if (z)
+        y *= oracle_silu(*z);
+    return y;
+}
+
+/* Scan one (b, d) row over all L positions. */
+static void oracle_scan_row(int64_t b, int64_t d, int64_t dim, int64_t dstate, int64_t seqlen,
+                            const double* u, const double* delta, const double* delta_bias,
+                            int delta_softplus, const double* A, const double* B,
+                            const double* C, const double* D, const double* z,
+                            const double* h0, double* h_last, double* y, double* h)
+{
+    const int64_t row = b * dim + d;
+    for (int64_t n = 0; n < dstate; ++n)
+        h[n] = h0 ? h0[row * dstate + n] : 0.0;
+    const double bias = delta_bias ? delta_bias[d] : 0.0;
+    const double Dd = D ? D[d] : 0.0;
+    for (int64_t l = 0; l < seqlen; ++l) {
+        const int64_t i = row * seqlen + l;
+        const double* Bcol = B + b * dstate * seqlen + l;
+        const double* Ccol = C + b * dstate * seqlen + l;
+        y[i] = oracle_step(dstate, h, u[i], delta[i], bias, delta_softplus, A + d * dstate,
+                           Bcol, Ccol, seqlen, Dd, z ? z + i : NULL);
+    }
+    if (h_last)
+        for (int64_t n = 0; n < dstate; ++n)
+            h_last[row * dstate + n] = h[n];
+}
+
+/* Full scan.  Rows are independent; `nthreads` > 1 only spreads whole rows
+ * over threads and does not change any arithmetic.
+ * Returns 0 on success, -1 on bad sizes or allocation failure. */
+int oracle_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                    const double* u, const double* delta, const double* delta_bias,
+                    int delta_softplus, const double* A, const double* B, const double* C,
+                    const double* D, const double* z, const double* h0, double* h_last,
+                    double* y, int nthreads)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0 || seqlen < 0)
+        return -1;
+    const int64_t rows = batch * dim;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+    {
+        double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+        if (!h) {
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < rows; ++r)
+                oracle_scan_row(r / dim, r % dim, dim, dstate, seqlen, u, delta, delta_bias,
+                                delta_softplus, A, B, C, D, z, h0, h_last, y, h);
+            free(h);
+        }
+    }
+    (void)nthreads;
+    return failed ? -1 : 0;
+}
+
+/* Scan only the listed rows (row = b * dim + d).  y_rows is [nrows, seqlen],
+ * h_last_rows (optional) is [nrows, dstate], h0 (optional) is the full
+ * [batch, dim, dstate] tensor.  Used for sampled parity at full sizes. */
+int oracle_scan_rows(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                     const int64_t* rows, int64_t nrows,
+                     const double* u_rows, const double* delta_rows, const double* delta_bias,
+                     int delta_softplus, const double* A, const double* B, const double* C,
+                     const double* D, const double* z_rows, const double* h0,
+                     double* h_last_rows, double* y_rows)
+{
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || nrows < 0)
+        return -1;
+    double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+    if (!h)
+        return -1;
+    for (int64_t k = 0; k < nrows; ++k) {
+        const int64_t r = rows[k];
+        if (r < 0 || r >= batch * dim) {
+            free(h);
+            return -1;
+        }
+        const int64_t b = r / dim, d = r % dim;
+        for (int64_t n = 0; n < dstate; ++n)
+            h[n] = h0 ? h0[r * dstate + n] : 0.0;
+        const double bias = delta_bias ? delta_bias[d] : 0.0;
+        const double Dd = D ? D[d] : 0.0;
+        for (int64_t l = 0; l < seqlen; ++l) {
+            const int64_t i = k * seqlen + l;
+            y_rows[i] = oracle_step(dstate, h, u_rows[i], delta_rows[i], bias, delta_softplus,
+                                    A + d * dstate, B + b * dstate * seqlen + l,
+                                    C + b * dstate * seqlen + l, seqlen, Dd,
+                                    z_rows ? z_rows + i : NULL);
+        }
+        if (h_last_rows)
+            for (int64_t n = 0; n < dstate; ++n)
+                h_last_rows[k * dstate + n] = h[n];
+    }
+    free(h);
+    return 0;
+}
+
+/* Single-token state update, h updated in place.
+ * h [batch, dim, dstate]; u, delta, z, y [batch, dim]; B, C [batch, dstate]. */
+int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double* h,
+                        const double* u, const double* delta, const double* delta_bias,
+                        int delta_softplus, const double* A, const double* B, const double* C,
+                        const double* D, const double* z, double* y)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0)
+        return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t i = b * dim + d;
+            y[i] = oracle_step(dstate, h + i * dstate, u[i], delta[i],
+                               delta_bias ? delta_bias[d] : 0.0, delta_softplus,
+                               A + d * dstate, B + b * dstate, C + b * dstate, 1,
+                               D ? D[d] : 0.0, z ? z + i : NULL);
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,295 @@
+"""Pins for the fp64 oracle: checks against facts fixed by the pages and by
+mathematics, independent of the oracle's own loop.
+
+Each pin takes an ``oracle.Oracle`` and raises AssertionError on a mismatch, so
+the same pins can be run against deliberately broken copies of the oracle
+(tests/test_oracle_pins.py::test_pins_catch_planted_mistakes).
+
+Sources of each fact:
+  * continuous system h'(t) = A h(t) + B x(t), y = C h (+ D x), input held over
+    each step (zero-order hold) of length delta_k:
+    "mamba 学习" (fakeeyes2wo), sections "MAMBA" and "引入可变步长 Δ_k";
+    velog Mamba review, section 2 "Discretization".
+  * inclusive recurrence h_k = Abar h_{k-1} + Bbar x_k, y_k = C h_k:
+    velog Mamba review, section 2 "Discretization", item 3.
+  * unrolled sum h_k = Abar^k h_0 + sum_j Abar^{k-1-j} Bbar x_j and the
+    convolution kernel K_l = C Abar^l Bbar for constant parameters:
+    "mamba 学习", section "离散 SSM 的卷积形式与时不变性" (shifted to the
+    inclusive convention above).
+  * ZOH integral needs invertible A; its A -> 0 limit is delta * B:
+    "mamba 学习", section "MAMBA".
+  * linearity of the SSM in its input: velog Mamba review, section 2 "LTI".
+  * dt = softplus(raw + bias): velog Mamba review, section 3.2; the D skip:
+    "mamba 学习", section "SSM 状态空间模型"; gate y * silu(z):
+    Mamba_Model_Report.md, section 3 (MambaBlock.forward).
+  * single-token step equals the scan: Mamba_Model_Report.md, section 6.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.integrate import solve_ivp
+
+
+def _rng(seed):
+    return np.random.default_rng(1000 + seed)
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = np.abs(a - b)
+    lim = atol + rtol * np.abs(b)
+    if not np.all(err <= lim):
+        i = int(np.argmax(err - lim))
+        raise AssertionError(f"{what}: max excess at flat index {i}: got {a.flat[i]!r}, "
+                             f"expected {b.flat[i]!r}")
+
+
+# ---------------------------------------------------------------------------
+# 1. zero-order hold, checked by integrating the continuous system
+# ---------------------------------------------------------------------------
+def pin_zoh_matches_ode(orc):
+    """Integrate h' = A h + B_k x_k over [t_k, t_k + delta_k] with an ODE solver
+    (no closed form used) and compare y_k = C_k h(t_k + delta_k) + D x_k."""
+    rng = _rng(1)
+    n, L = 4, 7
+    A = np.array([[-1.0, -2.5, -0.003, 0.0]])          # includes A = 0 exactly
+    dts = rng.uniform(0.05, 0.9, size=L)
+    x = rng.standard_normal(L)
+    B = rng.standard_normal((n, L))
+    C = rng.standard_normal((n, L))
+    Dd = 0.7
+    h0 = rng.standard_normal(n) * 0.5
+    h = h0.copy()
+    y_ref = np.empty(L)
+    a = A[0]
+    for k in range(L):
+        bx = B[:, k] * x[k]
+        sol = solve_ivp(lambda t, hh: a * hh + bx, (0.0, dts[k]), h, method="DOP853",
+                        rtol=1e-13, atol=1e-15)
+        h = sol.y[:, -1]
+        y_ref[k] = C[:, k] @ h + Dd * x[k]
+    y = orc.scan_fwd(x[None, None, :], dts[None, None, :], A, B[None], C[None],
+                     D=np.array([Dd]), delta_softplus=False, h0=h0[None, None, :])
+    _close(y[0, 0], y_ref, rtol=1e-9, atol=1e-11, what="ZOH vs ODE")
+
+
+# ---------------------------------------------------------------------------
+# 2. brute-force unrolled sum (no loop-carried state)
+# ---------------------------------------------------------------------------
+def _unrolled(u, dt, A, B, C, D, h0):
+    """y_k = sum_n C[n,k] (prod_{i<=k} Abar_i h0 + sum_{j<=k} prod_{j<i<=k} Abar_i Bbar_j u_j) + D u_k"""
+    L = u.shape[0]
+    n = A.shape[0]
+    Abar = np.exp(dt[:, None] * A[None, :])                        # [L, n]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        coef = np.where(A[None, :] == 0.0, dt[:, None],
+                        np.expm1(dt[:, None] * A[None, :]) / A[None, :])
+    Bbar_u = coef * B.T * u[:, None]                                # [L, n]
+    y = np.empty(L)
+    for k in range(L):
+        hk = np.prod(Abar[: k + 1], axis=0) * h0
+        for j in range(k + 1):
+            hk = hk + np.prod(Abar[j + 1: k + 1], axis=0) * Bbar_u[j]
+        y[k] = C[:, k] @ hk + D * u[k]
+    return y
+
+
+def pin_unrolled_sum(orc):
+    rng = _rng(2)
+    b, d, n, L = 2, 3, 5, 37
+    u = rng.standard_normal((b, d, L))
+    raw = rng.standard_normal((b, d, L))
+    bias = rng.uniform(-3.0, 0.5, size=d)
+    A = -rng.uniform(0.2, 4.0, size=(d, n))
+    A[1, 2] = 0.0
+    B = rng.standard_normal((b, n, L))
+    C = rng.standard_normal((b, n, L))
+    D = rng.standard_normal(d)
+    h0 = rng.standard_normal((b, d, n))
+    y, hl = orc.scan_fwd(u, raw, A, B, C, D=D, delta_bias=bias, h0=h0, return_last_state=True)
+    for bi in range(b):
+        for di in range(d):
+            x = raw[bi, di] + bias[di]
+            dt = np.log1p(np.exp(-np.abs(x))) + np.maximum(x, 0.0)   # softplus, stable form
+            y_ref = _unrolled(u[bi, di], dt, A[di], B[bi], C[bi], D[di], h0[bi, di])
+            _close(y[bi, di], y_ref, rtol=1e-11, atol=1e-12, what=f"unrolled sum ({bi},{di})")
+
+
+# ---------------------------------------------------------------------------
+# 3. LTI special case: convolution with K_l = sum_n C_n Abar_n^l Bbar_n
+# ---------------------------------------------------------------------------
+def pin_lti_convolution(orc):
+    rng = _rng(3)
+    n, L = 6, 64
+    A = -np.arange(1, n + 1, dtype=np.float64)[None, :] * 0.7
+    dt = 0.13
+    Bc = rng.standard_normal(n)
+    Cc = rng.standard_normal(n)
+    Dd = -0.4
+    u = rng.standard_normal(L)
+    B = np.repeat(Bc[:, None], L, axis=1)[None]
+    C = np.repeat(Cc[:, None], L, axis=1)[None]
+    y = orc.scan_fwd(u[None, None], np.full((1, 1, L), dt), A, B, C, D=np.array([Dd]),
+                     delta_softplus=False)[0, 0]
+    Abar = np.exp(dt * A[0])
+    Bbar = np.expm1(dt * A[0]) / A[0] * Bc
+    K = np.array([np.sum(Cc * Abar ** l * Bbar) for l in range(L)])
+    y_ref = np.convolve(u, K)[:L] + Dd * u
+    _close(y, y_ref, rtol=1e-11, atol=1e-12, what="LTI convolution")
+
+
+# ---------------------------------------------------------------------------
+# 4. geometric series: N = 1, x = 1, constant parameters
+# ---------------------------------------------------------------------------
+def pin_geometric_series(orc):
+    L = 50
+    for a, dt, bval, cval in [(-1.0, 0.1, 1.0, 1.0), (-3.0, 0.02, 0.5, -2.0),
+                              (-0.25, 1.7, -1.5, 0.3)]:
+        A = np.array([[a]])
+        y = orc.scan_fwd(np.ones((1, 1, L)), np.full((1, 1, L), dt), A,
+                         np.full((1, 1, L), bval), np.full((1, 1, L), cval),
+                         delta_softplus=False)[0, 0]
+        Abar = math.exp(a * dt)
+        Bbar = (Abar - 1.0) / a * bval
+        k = np.arange(L)
+        h_ref = Bbar * (1.0 - Abar ** (k + 1)) / (1.0 - Abar)
+        _close(y, cval * h_ref, rtol=1e-11, atol=1e-13, what=f"geometric series a={a}")
+
+
+# ---------------------------------------------------------------------------
+# 5. A -> 0 limit of the ZOH input coefficient
+# ---------------------------------------------------------------------------
+def pin_zoh_small_A(orc):
+    dt, bval, uval = 0.37, 1.3, -0.8
+    # A == 0 exactly: Bbar = dt * B (the integral of e^{0 tau} over [0, dt])
+    y0 = orc.scan_fwd(np.full((1, 1, 1), uval), np.full((1, 1, 1), dt), np.zeros((1, 1)),
+                      np.full((1, 1, 1), bval), np.ones((1, 1, 1)), delta_softplus=False)
+    if y0[0, 0, 0] != dt * bval * uval:
+        raise AssertionError(f"A=0: got {y0[0, 0, 0]!r}, expected {dt * bval * uval!r}")
+    # tiny A: coef = dt * (1 + q/2 + q^2/6 + q^3/24), q = dt*A, truncation < q^4
+    for p in range(3, 13):
+        a = -(10.0 ** -p)
+        q = dt * a
+        ref = dt * (1 + q / 2 + q * q / 6 + q ** 3 / 24) * bval * uval
+        y = orc.scan_fwd(np.full((1, 1, 1), uval), np.full((1, 1, 1), dt), np.array([[a]]),
+                         np.full((1, 1, 1), bval), np.ones((1, 1, 1)), delta_softplus=False)
+        _close(y[0, 0, 0], ref, rtol=1e-13, what=f"A=-1e-{p}")
+
+
+# ---------------------------------------------------------------------------
+# 6. linearity in u (delta, B, C, z fixed; h0 = 0)
+# ---------------------------------------------------------------------------
+def pin_linearity(orc):
+    rng = _rng(6)
+    b, d, n, L = 1, 3, 4, 40
+    raw = rng.standard_normal((b, d, L))
+    A = -rng.uniform(0.5, 3.0, size=(d, n))
+    B = rng.standard_normal((b, n, L))
+    C = rng.standard_normal((b, n, L))
+    D = rng.standard_normal(d)
+    z = rng.standard_normal((b, d, L))
+    u1 = rng.standard_normal((b, d, L))
+    u2 = rng.standard_normal((b, d, L))
+    al, be = 1.7, -0.6
+    y1 = orc.scan_fwd(u1, raw, A, B, C, D=D, z=z)
+    y2 = orc.scan_fwd(u2, raw, A, B, C, D=D, z=z)
+    y12 = orc.scan_fwd(al * u1 + be * u2, raw, A, B, C, D=D, z=z)
+    _close(y12, al * y1 + be * y2, rtol=1e-11, atol=1e-12, what="linearity in u")
+
+
+# ---------------------------------------------------------------------------
+# 7. parameter plumbing: softplus(raw + bias), D skip, silu gate order
+# ---------------------------------------------------------------------------
+def pin_softplus_bias_gate(orc):
+    import torch
+    import torch.nn.functional as F
+
+    rng = _rng(7)
+    L = 64
+    raw = rng.uniform(-25.0, 25.0, size=L)
+    bias = 0.75
+    # A = 0, B = C = u = 1, h0 = 0, one step per row: y = dt = softplus(raw + bias)
+    y = orc.scan_fwd(np.ones((1, L, 1)), raw[None, :, None], np.zeros((L, 1)),
+                     np.ones((1, 1, 1)), np.ones((1, 1, 1)),
+                     delta_bias=np.full(L, bias))[0, :, 0]
+    ref = F.softplus(torch.tensor(raw + bias, dtype=torch.float64), beta=1.0,
+                     threshold=1e9).numpy()
+    _close(y, ref, rtol=1e-14, atol=1e-300, what="softplus(raw + bias)")
+    # B = 0 keeps h = 0, so y = D u silu(z): D skip enters before the gate
+    u = rng.standard_normal(L)
+    z = rng.uniform(-12.0, 12.0, size=L)
+    Dv = rng.standard_normal(L)
+    y = orc.scan_fwd(u[None, :, None], np.zeros((1, L, 1)), -np.ones((L, 1)),
+                     np.zeros((1, 1, 1)), np.ones((1, 1, 1)), D=Dv, z=z[None, :, None])[0, :, 0]
+    ref = Dv * u * F.silu(torch.tensor(z, dtype=torch.float64)).numpy()
+    _close(y, ref, rtol=1e-14, atol=1e-300, what="D skip then silu gate")
+
+
+# ---------------------------------------------------------------------------
+# 8. decode step == scan, and split invariance through h0 / h_last
+# ---------------------------------------------------------------------------
+def pin_step_equals_scan(orc):
+    rng = _rng(8)
+    b, d, n, L = 2, 3, 4, 12
+    u = rng.standard_normal((b, d, L))
+    raw = rng.standard_normal((b, d, L))
+    bias = rng.uniform(-4, 0, size=d)
+    A = -rng.uniform(0.5, 3.0, size=(d, n))
+    B = rng.standard_normal((b, n, L))
+    C = rng.standard_normal((b, n, L))
+    D = rng.standard_normal(d)
+    z = rng.standard_normal((b, d, L))
+    h0 = rng.standard_normal((b, d, n)) * 0.3
+    y, hl = orc.scan_fwd(u, raw, A, B, C, D=D, z=z, delta_bias=bias, h0=h0,
+                         return_last_state=True)
+    h = h0.copy()
+    for l in range(L):
+        yl, h = orc.state_update(h, u[:, :, l], raw[:, :, l], A, B[:, :, l], C[:, :, l], D=D,
+                                 z=z[:, :, l], delta_bias=bias)
+        _close(yl, y[:, :, l], rtol=1e-13, atol=1e-14, what=f"step {l} vs scan")
+    _close(h, hl, rtol=1e-13, atol=1e-14, what="final state: steps vs scan")
+
+
+def pin_split_invariance(orc):
+    rng = _rng(9)
+    b, d, n, L, m = 1, 2, 4, 30, 11
+    u = rng.standard_normal((b, d, L))
+    raw = rng.standard_normal((b, d, L))
+    A = -rng.uniform(0.5, 3.0, size=(d, n))
+    B = rng.standard_normal((b, n, L))
+    C = rng.standard_normal((b, n, L))
+    D = rng.standard_normal(d)
+    y, hl = orc.scan_fwd(u, raw, A, B, C, D=D, return_last_state=True)
+    ya, ha = orc.scan_fwd(u[..., :m], raw[..., :m], A, B[..., :m], C[..., :m], D=D,
+                          return_last_state=True)
+    yb, hb = orc.scan_fwd(u[..., m:], raw[..., m:], A, B[..., m:], C[..., m:], D=D, h0=ha,
+                          return_last_state=True)
+    _close(np.concatenate([ya, yb], axis=-1), y, rtol=1e-13, atol=1e-14, what="split y")
+    _close(hb, hl, rtol=1e-13, atol=1e-14, what="split h_last")
+
+
+def pin_rows_match_full(orc):
+    rng = _rng(10)
+    b, d, n, L = 2, 5, 4, 20
+    u = rng.standard_normal((b, d, L))
+    raw = rng.standard_normal((b, d, L))
+    A = -rng.uniform(0.5, 3.0, size=(d, n))
+    B = rng.standard_normal((b, n, L))
+    C = rng.standard_normal((b, n, L))
+    z = rng.standard_normal((b, d, L))
+    h0 = rng.standard_normal((b, d, n))
+    y, hl = orc.scan_fwd(u, raw, A, B, C, z=z, h0=h0, return_last_state=True)
+    rows = [0, 3, 7, 9]
+    uf, rf, zf = u.reshape(b * d, L), raw.reshape(b * d, L), z.reshape(b * d, L)
+    yr, hr = orc.scan_rows(rows, uf[rows], rf[rows], A, B, C, b, d, z_rows=zf[rows], h0=h0,
+                           return_last_state=True)
+    _close(yr, y.reshape(b * d, L)[rows], rtol=0, atol=0, what="scan_rows")
+    _close(hr, hl.reshape(b * d, n)[rows], rtol=0, atol=0, what="scan_rows h_last")
+
+
+ALL_PINS = [pin_zoh_matches_ode, pin_unrolled_sum, pin_lti_convolution, pin_geometric_series,
+            pin_zoh_small_A, pin_linearity, pin_softplus_bias_gate, pin_step_equals_scan,
+            pin_split_invariance, pin_rows_match_full]

@@ -1,0 +1,79 @@
+"""The oracle against its pins, and the pins against planted mistakes.
+
+Every pin in tests/pins.py is checked against the real oracle.  Then each of a
+list of plausible mistakes (a dropped term, a wrong sign, a wrong index, a
+swapped operand, a wrong convention) is planted in a temporary copy of the
+oracle source on the CPU, compiled, and the pins must reject it.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import pins
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(orc, pin):
+    pin(orc)
+
+
+# (name, text in ssm_oracle.c, replacement)
+MUTANTS = [
+    ("euler_instead_of_zoh",
+     "double coef = (a == 0.0) ? dt : expm1(dt * a) / a;", "double coef = dt;"),
+    ("sign_of_Abar", "double Abar = exp(dt * a);", "double Abar = exp(-dt * a);"),
+    ("exclusive_output_convention",
+     "h[n] = Abar * h[n] + coef * B_col[n * bc_stride] * u;\n"
+     "        acc += C_col[n * bc_stride] * h[n];",
+     "acc += C_col[n * bc_stride] * h[n];\n"
+     "        h[n] = Abar * h[n] + coef * B_col[n * bc_stride] * u;"),
+    ("dropped_D_skip", "double y = acc + Dd * u;", "double y = acc;"),
+    ("gate_before_D_skip",
+     "double y = acc + Dd * u;\n    if (z)\n        y *= oracle_silu(*z);",
+     "double y = acc;\n    if (z)\n        y *= oracle_silu(*z);\n    y += Dd * u;"),
+    ("bias_after_softplus",
+     "double x = delta_raw + bias;\n    double dt = delta_softplus ? oracle_softplus(x) : x;",
+     "double x = delta_raw;\n    double dt = (delta_softplus ? oracle_softplus(x) : x) + bias;"),
+    ("wrong_BC_stride", "Bcol, Ccol, seqlen, Dd,", "Bcol, Ccol, 1, Dd,"),
+    ("swapped_B_C", "Bcol, Ccol, seqlen, Dd,", "Ccol, Bcol, seqlen, Dd,"),
+    ("ignored_h0", "h[n] = h0 ? h0[row * dstate + n] : 0.0;", "h[n] = 0.0;"),
+    ("wrong_A_row", "A + d * dstate,\n                           Bcol",
+     "A + d,\n                           Bcol"),
+    ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("softplus_branch", "return x + log1p(exp(-x));", "return x + log1p(exp(x));"),
+    ("dropped_input_u", "coef * B_col[n * bc_stride] * u;\n        acc",
+     "coef * B_col[n * bc_stride];\n        acc"),
+    ("expm1_without_divide", "expm1(dt * a) / a;", "expm1(dt * a);"),
+    ("decode_stride", "A + d * dstate, B + b * dstate, C + b * dstate, 1,",
+     "A + d * dstate, B + b * dstate, C + b * dstate, dstate,"),
+]
+
+
+@pytest.mark.parametrize("name,find,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistakes(tmp_path, name, find, repl):
+    src = open(oracle.SOURCE).read()
+    assert src.count(find) == 1, f"mutation site for {name} not unique/present"
+    mutant = tmp_path / f"mutant_{name}.c"
+    mutant.write_text(src.replace(find, repl))
+    lib = oracle.compile_source(str(mutant), str(tmp_path / f"lib_{name}.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(orc)
+        except (AssertionError, FloatingPointError, ValueError) as e:  # noqa: PERF203
+            caught.append(pin.__name__)
+    assert caught, f"no pin rejects the planted mistake '{name}'"
+
+
+def test_golden_tiny_regression(orc):
+    """tests/golden/tiny_scan.txt was written by tests/golden/make_golden.py from
+    the oracle; this guards the oracle against silent drift."""
+    from tests.golden import make_golden
+    path = os.path.join(os.path.dirname(__file__), "golden", "tiny_scan.txt")
+    stored = np.loadtxt(path)
+    fresh = make_golden.tiny_scan_values(orc)
+    np.testing.assert_allclose(fresh, stored, rtol=1e-13, atol=1e-15)
