@@ -1,0 +1,496 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan forward on B300 (one JSON line on rank 0).
+
+Step = one ssm_scan_fwd over the Mamba-2.8B-like layer workload (bf16 io, fp32
+state, batch 8, dim 5120, dstate 16, seqlen 2048, silu gate): softplus, ZOH
+discretisation, recurrence, C contraction, D skip and gate fused in one kernel.
+Inputs (672 MB per step) are larger than the 126 MB L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs the same workload on its own GPU (independent
+problems: weak scaling, no data-path collective); the timing is the max over
+ranks and `value` counts the elements of all ranks.
+
+The decode state update (batch 256, dim 5120, dstate 16, 1024 steps) is measured
+after the main loop and reported under "decode".
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_115_b300 import workloads as W  # noqa: E402
+
+METRIC = "selective-scan elements/s (B·D·L) and achieved HBM GB/s vs B300 roofline"
+CFG = W.SCAN_CONFIGS["2p8b"]
+DEC = W.DECODE_CONFIGS["decode"]
+SM_COUNT = 148
+SM_MAX_MHZ = 2032.0
+EX2_PER_CLK_SM = 32          # measured on this machine's B300 (ex2.approx.ftz.f32 throughput)
+FALLBACK_HBM_GBS = 6400.0
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "sm_max_mhz": SM_MAX_MHZ}, "fallback"
+
+
+def scan_bytes(cfg) -> int:
+    """Algorithmic bytes of one scan: u, delta, z read and y written at io width,
+    B and C read, fp32 A, D and bias read."""
+    s = 2 if cfg.io == W.BF16 else 4
+    e = cfg.batch * cfg.dim * cfg.seqlen
+    n_io = 3 + (1 if cfg.gate else 0)
+    return (n_io * e + 2 * cfg.batch * cfg.dstate * cfg.seqlen) * s + \
+        4 * (cfg.dim * cfg.dstate + 2 * cfg.dim)
+
+
+def decode_bytes(cfg) -> int:
+    s = 2 if cfg.io == W.BF16 else 4
+    ch = cfg.batch * cfg.dim
+    return 2 * 4 * ch * cfg.dstate + (3 + (1 if cfg.gate else 0)) * s * ch + \
+        2 * s * cfg.batch * cfg.dstate + 4 * (cfg.dim * cfg.dstate + 2 * cfg.dim)
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_115_b300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != source_sha():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id=None, period_ms=50):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(period_ms)]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        self.lines = []
+        self.marks = []
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        deadline = time.time() + 5
+        while not self.lines and time.time() < deadline:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        t0, t1 = (self.marks + [0, 0])[:2] if len(self.marks) >= 2 else (0, time.time())
+        sm, mx, reasons = [], [], set()
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.06):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+def oracle_sample_rate(target_core_seconds: float, cores: int, steps: int = 1):
+    """Time the oracle on a row sample of the bench workload; returns
+    (elements/s, rows, seconds, sample description)."""
+    import oracle
+    rows_total = CFG.batch * CFG.dim
+    x = W.make_scan_inputs(CFG, seed=0, batch=1, dim=min(CFG.dim, 4096))
+    f = lambda a: W.to_f64(a, CFG.io)  # noqa: E731
+    u, dl, z, B, C = f(x["u"]), f(x["delta"]), f(x["z"]), f(x["B"]), f(x["C"])
+    # calibrate on 8 rows, one thread
+    t = time.perf_counter()
+    oracle.scan_fwd(u[:, :8], dl[:, :8], x["A"][:8], B, C, D=x["D"][:8], z=z[:, :8],
+                    delta_bias=x["delta_bias"][:8], nthreads=1)
+    per_row = (time.perf_counter() - t) / 8
+    rows = int(max(cores, min(u.shape[1], rows_total, target_core_seconds / per_row)))
+    rows = max(1, min(rows, u.shape[1]))
+    times = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        oracle.scan_fwd(u[:, :rows], dl[:, :rows], x["A"][:rows], B, C, D=x["D"][:rows],
+                        z=z[:, :rows], delta_bias=x["delta_bias"][:rows], nthreads=cores)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    elems = rows * CFG.seqlen * steps
+    desc = (f"{rows} of {rows_total} (b,d) rows of the bench workload (batch row 0), full "
+            f"seqlen {CFG.seqlen}, dstate {CFG.dstate}, bf16 inputs widened to fp64, fp64 "
+            f"sequential loops, OpenMP over rows")
+    return elems / total, rows, total, desc
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cores = os.cpu_count() or 1
+    steps, warm = args.steps, args.warmup
+    budget = 120.0  # seconds for the whole run
+    per_step_core_s = max(0.05, budget * cores / max(1, steps + warm))
+    # warm-up steps: tiny calibration runs
+    if warm:
+        oracle_sample_rate(min(per_step_core_s, 0.5), cores, steps=1)
+    rate, rows, secs, desc = oracle_sample_rate(per_step_core_s, cores, steps=steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "elements/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": 1e3 * secs / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": bench_config("oracle (fp64 CPU loops) on host cores"),
+        "cpu_baseline": {"value": rate, "unit": "elements/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": rate, "unit": "elements/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_config(impl_note: str):
+    return {"workload": "Mamba-2.8B-like selective scan: bf16 io, fp32 state, batch 8, dim 5120, "
+                        "dstate 16, seqlen 2048, silu(z) gate, dt bias = inverse softplus of "
+                        "log-uniform dt, A[d,n] = -(n+1), D ~ N(0,1)",
+            "batch": CFG.batch, "dim": CFG.dim, "dstate": CFG.dstate, "seqlen": CFG.seqlen,
+            "io": "bf16", "impl": impl_note,
+            "l2": "inputs larger than L2 (672 MB per step vs 126 MB L2); no flush",
+            "parallelism": "one independent problem per GPU (weak scaling)"}
+
+
+# ---------------------------------------------------------------------------
+# main (GPU) arm
+# ---------------------------------------------------------------------------
+def to_dev_io(a, dev):
+    import torch
+    if a is None:
+        return None
+    if CFG.io == W.BF16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(a).to(dev)
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from selective_state_space_115_b300 import binding as S
+    S.library()
+
+    x = W.make_scan_inputs(CFG, seed=rank)
+    u, dl, z = to_dev_io(x["u"], dev), to_dev_io(x["delta"], dev), to_dev_io(x["z"], dev)
+    B, C = to_dev_io(x["B"], dev), to_dev_io(x["C"], dev)
+    A = torch.from_numpy(x["A"]).to(dev)
+    Dv = torch.from_numpy(x["D"]).to(dev)
+    bias = torch.from_numpy(x["delta_bias"]).to(dev)
+    y = torch.empty_like(u)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        S.scan_fwd(u, dl, A, B, C, D=Dv, z=z, delta_bias=bias, algo="auto", out=y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert S.read_device_status() == 0, "device-side wait timed out during warm-up"
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001
+        gpu_id = None
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark()
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if sampler:
+        sampler.mark()
+    barrier(world)
+    dev_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    assert S.read_device_status() == 0, "device-side wait timed out in the timed region"
+    ms_step = max_over_ranks(dev_ms / args.steps, world, dev)
+
+    elems = CFG.elements
+    value = world * elems / (ms_step * 1e-3)
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    bytes_step = scan_bytes(CFG)
+    ex2_peak = EX2_PER_CLK_SM * SM_COUNT * SM_MAX_MHZ * 1e6 / 1e12   # Texp/s
+    achieved_exp = CFG.updates / (dev_ms / args.steps * 1e-3) / 1e12
+    traffic = profiled_traffic("scan_channel_2p8b")
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = max(3, min(20, args.steps))
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hu, hd, hz, hB, hC = pin(u), pin(dl), pin(z), pin(B), pin(C)
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hu, hd, hz, hB, hC))
+    d2h = hy.numel() * hy.element_size()
+
+    def e2e_step():
+        du, dd, dz = hu.to(dev, non_blocking=True), hd.to(dev, non_blocking=True), \
+            hz.to(dev, non_blocking=True)
+        dB, dC = hB.to(dev, non_blocking=True), hC.to(dev, non_blocking=True)
+        yy = S.scan_fwd(du, dd, A, dB, dC, D=Dv, z=dz, delta_bias=bias, algo="auto")
+        hy.copy_(yy, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, dev)
+    e2e_value = world * elems / e2e_s
+
+    # ---- decode state update (rank 0's measurement)
+    decode = run_decode(dev, S) if (rank == 0 and not args.no_decode) else None
+    barrier(world)
+
+    # ---- CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        rate, rows, secs, desc = oracle_sample_rate(20.0, cores)
+        cpu = {"value": rate, "unit": "elements/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": bench_config("libssm scan_channel kernel (TMA, "
+                                                        "lanes over channels)"),
+            "hbm": {"achieved_gbs": bytes_step / (ms_step * 1e-3) / 1e9, "peak_gbs": hbm_peak,
+                    "frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm_peak,
+                    "bytes_per_step": bytes_step, "peak_kind": peak_kind},
+            "roofline": {"bound": "alu", "achieved": achieved_exp, "peak": ex2_peak,
+                         "unit": "Texp/s", "frac": achieved_exp / ex2_peak, "traffic": traffic,
+                         "kernel": "scan_channel_kernel<bf16, N=16, G=4, gate>",
+                         "units_per_launch": CFG.updates,
+                         "peak_note": "148 SMs x 32 ex2/clk/SM (measured ex2.approx.f32 "
+                                      "throughput) x 2032 MHz max SM clock"},
+            "e2e": {"value": e2e_value, "unit": "elements/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "wall_s_timed": wall,
+        }
+        if decode:
+            line["decode"] = decode
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_decode(dev, S):
+    """1024 sequential single-token updates of the decode workload, h in place."""
+    import torch
+    cfg = DEC
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    static = W.make_decode_static(cfg, seed=0)
+    h = torch.from_numpy(static["h"]).to(dev)
+    A = torch.from_numpy(static["A"]).to(dev)
+    Dv = torch.from_numpy(static["D"]).to(dev)
+    bias = torch.from_numpy(static["delta_bias"]).to(dev)
+    steps = cfg.steps
+    bd = (steps, cfg.batch, cfg.dim)
+    bn = (steps, cfg.batch, cfg.dstate)
+    u = torch.randn(bd, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dl = torch.randn(bd, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    z = torch.randn(bd, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    B = torch.randn(bn, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    C = torch.randn(bn, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    y = torch.empty(bd, dtype=torch.bfloat16, device=dev)
+
+    def loop():
+        for t in range(steps):
+            S.state_update(h, u[t], dl[t], A, B[t], C[t], D=Dv, z=z[t], delta_bias=bias, out=y[t])
+
+    loop()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    loop()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_plain = e0.elapsed_time(e1) / steps
+    # the same loop captured once in a CUDA graph
+    ms_graph = None
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            loop()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            loop()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_graph = e0.elapsed_time(e1) / steps
+    except Exception as e:  # noqa: BLE001
+        ms_graph = f"graph capture failed: {e}"
+    peaks, kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    nb = decode_bytes(cfg)
+    best = ms_plain if not isinstance(ms_graph, float) else min(ms_plain, ms_graph)
+    return {"workload": "decode: batch 256, dim 5120, dstate 16, bf16 io, fp32 state, "
+                        "1024 sequential steps, h in place",
+            "ms_per_step_plain": ms_plain, "ms_per_step_graph": ms_graph,
+            "bytes_per_step": nb, "gpu_launches": 2 * steps,
+            "roofline": {"bound": "hbm", "achieved": nb / (best * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": nb / (best * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+                         "peak_kind": kind,
+                         "note": "h (84 MB) fits in L2, so DRAM bytes can be below the "
+                                 "algorithmic bytes"}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="libssm", choices=["libssm", "reference"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,174 @@
+/*
+ * ssm.h -- C ABI of libssm: the Mamba selective-scan forward and the
+ * single-token recurrent state update, as CUDA kernels for B300 (sm_103a).
+ *
+ * The method (citations are to the pages this library follows):
+ *
+ *   dt_l   = softplus(delta[b,d,l] + delta_bias[d])            (or no softplus)
+ *   Abar   = exp(dt_l * A[d,n])
+ *   Bbar   = (dt_l A)^-1 (exp(dt_l A) - 1) dt_l B[b,n,l]  = (Abar - 1) / A[d,n] * B[b,n,l]
+ *            (= dt_l * B[b,n,l] when A[d,n] == 0, the A -> 0 limit)
+ *   h_l[n] = Abar * h_{l-1}[n] + Bbar * u[b,d,l]                h_{-1} = h0 (or 0)
+ *   y_l    = sum_n C[b,n,l] * h_l[n] + D[d] * u[b,d,l]
+ *   y_l   *= silu(z[b,d,l])                                     (when z is given)
+ *
+ *  - zero-order-hold discretisation and the recurrence h_k = Abar h_{k-1} + Bbar x_k:
+ *    velog review of "Mamba: Linear-Time Sequence Modeling with Selective State
+ *    Spaces", section 2 "Discretization"; the ZOH integral and the need for an
+ *    invertible A: "mamba 学习" (fakeeyes2wo), section "MAMBA".
+ *  - input-dependent dt, B, C and A fixed per channel: velog review, sections
+ *    3.2 and 3.5; "Mamba学习记录" (lengnian), section "怎么增加选择性".
+ *  - D skip and silu(z) gate: Mamba_Model_Report.md, sections 3 and 4.2.
+ *  - single-token step: Mamba_Model_Report.md, section 6 (ssm_step).
+ *  - fusion rule (load the 3-D inputs once, keep the state on chip, write only
+ *    the 3-D output; never materialise the (B, L, D, N) tensor): velog review,
+ *    section 3.3 "Kernel Fusion".
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers, owned by the caller.  The library
+ *    allocates no device memory and keeps no per-call state.
+ *  - Tensors are contiguous, row-major, last index fastest:
+ *      u, delta, z, y : [batch, dim, seqlen]      (scan)  /  [batch, dim]  (update)
+ *      B, C           : [batch, dstate, seqlen]   (scan)  /  [batch, dstate] (update)
+ *      A              : [dim, dstate]     float32
+ *      D, delta_bias  : [dim]             float32
+ *      h0, h_last, h  : [batch, dim, dstate] float32
+ *  - u, delta, z, B, C and y have the io dtype (float32 or bfloat16); A, D,
+ *    delta_bias and every state tensor are float32.  Arithmetic is float32.
+ *    bfloat16 outputs are rounded to nearest even.
+ *  - dstate must be 4, 8 or 16 (SSM_ERR_UNSUPPORTED otherwise).  batch, dim and
+ *    seqlen may be any value >= 1; there is no alignment requirement beyond the
+ *    element size (aligned, L-multiple shapes take the TMA path).
+ *  - Arguments are validated on the host before anything is enqueued; a call
+ *    that returns an error has launched nothing.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and the call returns without synchronising.  A launch failure returns
+ *    SSM_ERR_CUDA (ssm_last_cuda_error() gives the CUDA message).
+ *  - Outputs must not alias inputs, except that ssm_state_update updates h in place.
+ */
+#ifndef SSM_B300_H
+#define SSM_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same ABI as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* ssm_stream_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,    /* bad size, NULL required pointer, misaligned pointer */
+    SSM_ERR_UNSUPPORTED = 2,    /* valid but not built: dstate not in {4, 8, 16}, unknown dtype/algo */
+    SSM_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+    SSM_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait gave up (see ssm_read_device_status) */
+} ssm_status;
+
+typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype;
+
+/* Kernel family of the scan.  AUTO picks by the number of independent
+ * (batch, dim) channels: many channels -> CHANNEL, few -> CHUNK. */
+typedef enum {
+    SSM_ALGO_AUTO = 0,
+    SSM_ALGO_CHANNEL = 1,  /* lanes over channels; each lane runs its channel's whole
+                              sequence with its state slice in registers; L streamed
+                              through shared memory in TMA chunks */
+    SSM_ALGO_CHUNK = 2     /* lanes over positions; warp-shuffle associative scan of
+                              (Abar, Bbar u) pairs inside each chunk, state carried
+                              across chunks */
+} ssm_algo;
+
+/*
+ * Size in bytes of the device workspace ssm_scan_fwd needs for these sizes
+ * (a 16-byte-aligned block holding the device status words; at least 256).
+ */
+SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+
+/*
+ * Selective-scan forward over a whole sequence (the pages' selective scan with
+ * ZOH discretisation, fused: softplus, discretisation, recurrence,
+ * C-contraction, D skip and gate in one kernel; u, delta, z, B, C read once,
+ * y written once).
+ *
+ *  io             dtype of u, delta, z, B, C, y
+ *  u, delta, y    [batch, dim, seqlen], required
+ *  delta_bias     [dim] float32 or NULL (0)
+ *  delta_softplus nonzero: dt = softplus(delta + bias); zero: dt = delta + bias
+ *  A              [dim, dstate] float32, required (A == 0 entries use the dt limit)
+ *  B, C           [batch, dstate, seqlen], required
+ *  D              [dim] float32 or NULL (no skip)
+ *  z              [batch, dim, seqlen] or NULL (no gate)
+ *  h0             [batch, dim, dstate] float32 or NULL (zero initial state)
+ *  h_last         [batch, dim, dstate] float32 or NULL (final state not written)
+ *  workspace      device buffer of at least ssm_scan_fwd_workspace_size() bytes,
+ *                 16-byte aligned, required.  Its status words are cleared on
+ *                 `stream` before the kernel runs; a device-side wait that hits
+ *                 its iteration limit records SSM_ERR_DEVICE_TIMEOUT there (the
+ *                 outputs are then incomplete).  Calls that share a workspace
+ *                 must not overlap on the GPU.
+ * Returns SSM_OK once the work is enqueued.
+ */
+SSM_API ssm_status ssm_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ssm_dtype io,
+                        const void* u, const void* delta, const float* delta_bias,
+                        int delta_softplus, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* h0, float* h_last, void* y,
+                        void* workspace, size_t workspace_bytes, ssm_stream_t stream);
+
+/* ssm_scan_fwd with an explicit kernel family (SSM_ALGO_AUTO behaves exactly
+ * like ssm_scan_fwd).  CHANNEL falls back to CHUNK when the TMA alignment rules
+ * do not hold (seqlen * element size not a multiple of 16, or a tensor base not
+ * 16-byte aligned). */
+SSM_API ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                             ssm_dtype io, const void* u, const void* delta,
+                             const float* delta_bias, int delta_softplus, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* h0, float* h_last, void* y, void* workspace,
+                             size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream);
+
+/*
+ * Single-token recurrent state update (decode): one step of the scan for every
+ * (batch, dim) channel, h read and written in place (Mamba_Model_Report.md,
+ * section 6, ssm_step, with the ZOH discretisation above).
+ *
+ *  h       [batch, dim, dstate] float32, in/out, required
+ *  u, delta, y  [batch, dim], required;  z [batch, dim] or NULL
+ *  B, C    [batch, dstate], required;  A [dim, dstate] float32, required
+ *  delta_bias, D  [dim] float32 or NULL
+ * No workspace: the kernel has no device-side waits.
+ */
+SSM_API ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, ssm_dtype io, float* h,
+                            const void* u, const void* delta, const float* delta_bias,
+                            int delta_softplus, const float* A, const void* B, const void* C,
+                            const float* D, const void* z, void* y, ssm_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads the status words of `workspace` (as filled
+ * by the last ssm_scan_fwd that used it).  Returns SSM_OK, SSM_ERR_DEVICE_TIMEOUT,
+ * or SSM_ERR_CUDA if the synchronisation or the copy failed.
+ */
+SSM_API ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t stream);
+
+/* Static description of a status code. */
+SSM_API const char* ssm_status_string(ssm_status status);
+
+/* Message of the last CUDA error seen by a call on this host thread ("" if none). */
+SSM_API const char* ssm_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+SSM_API int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_B300_H */

@@ -1,0 +1,235 @@
+"""ctypes binding over libssm's C ABI (include/ssm.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their data pointers and torch's current CUDA stream are passed to
+the C entry points, and every step of the computation runs in libssm's CUDA
+kernels.  A missing or unloadable library raises SsmError; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssm.so")
+
+SSM_OK = 0
+SSM_ERR_INVALID_ARG = 1
+SSM_ERR_UNSUPPORTED = 2
+SSM_ERR_CUDA = 3
+SSM_ERR_DEVICE_TIMEOUT = 4
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+ALGO_AUTO = 0
+ALGO_CHANNEL = 1
+ALGO_CHUNK = 2
+_ALGOS = {"auto": ALGO_AUTO, "channel": ALGO_CHANNEL, "chunk": ALGO_CHUNK,
+          ALGO_AUTO: ALGO_AUTO, ALGO_CHANNEL: ALGO_CHANNEL, ALGO_CHUNK: ALGO_CHUNK}
+
+# every symbol include/ssm.h declares
+EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_algo",
+            "ssm_state_update", "ssm_read_device_status", "ssm_status_string",
+            "ssm_last_cuda_error", "ssm_version")
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(what)
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+def library(path: Optional[str] = None):
+    """Load libssm.so (building it first if the sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if path is None:
+            from . import build as _build
+            if not _build.up_to_date():
+                try:
+                    _build.build()
+                except Exception as e:  # noqa: BLE001
+                    if not os.path.exists(p):
+                        raise SsmError(SSM_ERR_CUDA, f"libssm.so is not built and building it "
+                                                     f"failed: {e}") from e
+        if not os.path.exists(p):
+            raise SsmError(SSM_ERR_CUDA, f"libssm.so not found at {p}")
+        lib = ctypes.CDLL(p)
+        lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_fwd_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
+        scan_args = [_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
+                     _vp, _vp, _vp, _vp, ctypes.c_size_t]
+        lib.ssm_scan_fwd.restype = _int
+        lib.ssm_scan_fwd.argtypes = scan_args + [_vp]
+        lib.ssm_scan_fwd_algo.restype = _int
+        lib.ssm_scan_fwd_algo.argtypes = scan_args + [_int, _vp]
+        lib.ssm_state_update.restype = _int
+        lib.ssm_state_update.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int, _vp,
+                                         _vp, _vp, _vp, _vp, _vp, _vp]
+        lib.ssm_read_device_status.restype = _int
+        lib.ssm_read_device_status.argtypes = [_vp, _vp]
+        lib.ssm_status_string.restype = ctypes.c_char_p
+        lib.ssm_status_string.argtypes = [_int]
+        lib.ssm_last_cuda_error.restype = ctypes.c_char_p
+        lib.ssm_last_cuda_error.argtypes = []
+        lib.ssm_version.restype = _int
+        lib.ssm_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return library().ssm_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != SSM_OK:
+        lib = library()
+        msg = f"{what}: {status_string(status)}"
+        if status == SSM_ERR_CUDA:
+            msg += f" ({lib.ssm_last_cuda_error().decode()})"
+        raise SsmError(status, msg)
+
+
+def _io_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise SsmError(SSM_ERR_UNSUPPORTED, f"io dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: Optional[torch.Tensor], name: str, shape, dtype, device, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise SsmError(SSM_ERR_INVALID_ARG, f"{name} is required")
+    if t.device != device:
+        raise SsmError(SSM_ERR_INVALID_ARG, f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise SsmError(SSM_ERR_INVALID_ARG, f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise SsmError(SSM_ERR_INVALID_ARG, f"{name} has shape {tuple(t.shape)}, expected "
+                                            f"{tuple(shape)}")
+    if not t.is_contiguous():
+        raise SsmError(SSM_ERR_INVALID_ARG, f"{name} must be contiguous")
+
+
+_ws_cache = {}
+
+
+def scan_fwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
+    return int(library().ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen))
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    key = (device.index, nbytes)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True, h0=None,
+             return_last_state=False, algo="auto", out=None, workspace=None):
+    """Selective-scan forward on torch CUDA tensors.
+
+    u, delta, z, out: [batch, dim, seqlen] (float32 or bfloat16); B, C: [batch, dstate, seqlen]
+    (same dtype); A: [dim, dstate] float32; D, delta_bias: [dim] float32; h0: [batch, dim,
+    dstate] float32.  Returns y (and h_last [batch, dim, dstate] float32 when asked)."""
+    if not isinstance(u, torch.Tensor) or not u.is_cuda:
+        raise SsmError(SSM_ERR_INVALID_ARG, "u must be a CUDA tensor")
+    if u.dim() != 3:
+        raise SsmError(SSM_ERR_INVALID_ARG, "u must be [batch, dim, seqlen]")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    dev = u.device
+    io = _io_dtype(u)
+    _need(u, "u", (batch, dim, seqlen), u.dtype, dev)
+    _need(delta, "delta", (batch, dim, seqlen), u.dtype, dev)
+    _need(z, "z", (batch, dim, seqlen), u.dtype, dev, optional=True)
+    _need(B, "B", (batch, dstate, seqlen), u.dtype, dev)
+    _need(C, "C", (batch, dstate, seqlen), u.dtype, dev)
+    _need(A, "A", (dim, dstate), torch.float32, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    _need(h0, "h0", (batch, dim, dstate), torch.float32, dev, optional=True)
+    y = torch.empty_like(u) if out is None else out
+    _need(y, "out", (batch, dim, seqlen), u.dtype, dev)
+    h_last = (torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+              if return_last_state else None)
+    lib = library()
+    nbytes = int(lib.ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen))
+    ws = _workspace(dev, nbytes) if workspace is None else workspace
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_fwd_algo(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                   _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
+                                   _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(h_last), _ptr(y),
+                                   _ptr(ws), ws.numel(), _ALGOS[algo], ctypes.c_void_p(stream))
+    _check(st, "ssm_scan_fwd")
+    return (y, h_last) if return_last_state else y
+
+
+def read_device_status(workspace: Optional[torch.Tensor] = None, device=None) -> int:
+    """Synchronise the current stream and return the status recorded in a scan workspace."""
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        nbytes = int(library().ssm_scan_fwd_workspace_size(1, 1, 4, 1))
+        workspace = _workspace(dev, nbytes)
+    stream = torch.cuda.current_stream(workspace.device).cuda_stream
+    return int(library().ssm_read_device_status(_ptr(workspace), ctypes.c_void_p(stream)))
+
+
+def state_update(h, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 out=None):
+    """One decode step; h [batch, dim, dstate] float32 is updated in place.
+
+    u, delta, z, out: [batch, dim]; B, C: [batch, dstate]; A: [dim, dstate] float32.
+    Returns y [batch, dim]."""
+    if not isinstance(h, torch.Tensor) or not h.is_cuda:
+        raise SsmError(SSM_ERR_INVALID_ARG, "h must be a CUDA tensor")
+    batch, dim, dstate = h.shape
+    dev = h.device
+    io = _io_dtype(u)
+    _need(h, "h", (batch, dim, dstate), torch.float32, dev)
+    _need(u, "u", (batch, dim), u.dtype, dev)
+    _need(delta, "delta", (batch, dim), u.dtype, dev)
+    _need(z, "z", (batch, dim), u.dtype, dev, optional=True)
+    _need(B, "B", (batch, dstate), u.dtype, dev)
+    _need(C, "C", (batch, dstate), u.dtype, dev)
+    _need(A, "A", (dim, dstate), torch.float32, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    y = torch.empty_like(u) if out is None else out
+    _need(y, "out", (batch, dim), u.dtype, dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = library().ssm_state_update(batch, dim, dstate, io, _ptr(h), _ptr(u), _ptr(delta),
+                                        _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
+                                        _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
+                                        ctypes.c_void_p(stream))
+    _check(st, "ssm_state_update")
+    return y

@@ -1,0 +1,217 @@
+// scan_chunk.cuh -- selective-scan forward, "chunk" kernel family.
+//
+// For inputs with few (batch, dim) channels (long sequences, small layers),
+// one warp owns one channel and splits each chunk of 32*T positions over its
+// lanes (T consecutive positions per lane).  The recurrence h_l = Abar_l h_{l-1}
+// + Bbar_l u_l is associative in the pairs (Abar, Bbar u):
+//     (P1, H1) then (P2, H2)  =  (P1 P2, P2 H1 + H2)
+// (velog Mamba review, section 3.3 "Parallel Scan"), so per state n each lane
+//   1. forms its T pairs and folds them into one (P, H) (zero initial state),
+//   2. joins a 5-step warp-shuffle inclusive scan of (P, H) over the lanes,
+//   3. takes its carry-in h = P_prev * h_chunk + H_prev from the exclusive
+//      prefix and replays its T positions, accumulating y += C h,
+// and the state after the last lane is carried (in shared memory) to the next chunk.
+// The 4-D (position, state) tensor exists only as T pairs per lane per state.
+//
+// Loads are plain coalesced global loads (16-byte vectors when the row pitch
+// and the pointers allow, element loads with bounds checks otherwise), so this
+// kernel accepts every shape and alignment.
+#pragma once
+
+#include "scan_channel.cuh"
+#include "ssm_device.cuh"
+
+namespace ssm {
+
+template <typename IO, int N_, bool GATE_, bool VEC_>
+struct ChunkCfg {
+  static constexpr int N = N_;
+  static constexpr bool GATE = GATE_;
+  static constexpr bool VEC = VEC_;
+  static constexpr int WARPS = 4;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int ESZ = Io<IO>::kBytes;
+  static constexpr int T = 32 / ESZ;        // positions per lane: 16 bf16 / 8 fp32 (32 bytes)
+  static constexpr int TB = 16 / ESZ;       // positions per 16-byte vector
+  static constexpr int LCH = 32 * T;        // positions per chunk
+};
+
+// T io values starting at position l of a row (row_base points at position 0)
+template <typename IO, typename Cfg>
+__device__ __forceinline__ void load_run(const IO* row_base, int64_t l, int seqlen, float* out) {
+  constexpr int T = Cfg::T, TB = Cfg::TB;
+  if constexpr (Cfg::VEC) {
+#pragma unroll
+    for (int v = 0; v < T / TB; ++v) {
+      const int64_t lv = l + v * TB;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (lv < seqlen) w = __ldg(reinterpret_cast<const uint4*>(row_base + lv));
+      if constexpr (sizeof(IO) == 2) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          out[v * TB + 2 * k] = bf16lo(ws[k]);
+          out[v * TB + 2 * k + 1] = bf16hi(ws[k]);
+        }
+      } else {
+        out[v * TB + 0] = __uint_as_float(w.x);
+        out[v * TB + 1] = __uint_as_float(w.y);
+        out[v * TB + 2] = __uint_as_float(w.z);
+        out[v * TB + 3] = __uint_as_float(w.w);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < T; ++i) out[i] = (l + i < seqlen) ? Io<IO>::ldg(row_base + l + i) : 0.0f;
+  }
+}
+
+template <typename IO, typename Cfg>
+__device__ __forceinline__ void store_run(IO* row_base, int64_t l, int seqlen, const float* v) {
+  constexpr int T = Cfg::T, TB = Cfg::TB;
+  if constexpr (Cfg::VEC) {
+#pragma unroll
+    for (int q = 0; q < T / TB; ++q) {
+      const int64_t lv = l + q * TB;
+      if (lv < seqlen) {
+        uint4 w;
+        if constexpr (sizeof(IO) == 2) {
+          w = make_uint4(pack_bf16x2(v[q * TB + 0], v[q * TB + 1]),
+                         pack_bf16x2(v[q * TB + 2], v[q * TB + 3]),
+                         pack_bf16x2(v[q * TB + 4], v[q * TB + 5]),
+                         pack_bf16x2(v[q * TB + 6], v[q * TB + 7]));
+        } else {
+          w = make_uint4(__float_as_uint(v[q * TB + 0]), __float_as_uint(v[q * TB + 1]),
+                         __float_as_uint(v[q * TB + 2]), __float_as_uint(v[q * TB + 3]));
+        }
+        *reinterpret_cast<uint4*>(row_base + lv) = w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < T; ++i)
+      if (l + i < seqlen) Io<IO>::store(row_base + l + i, v[i]);
+  }
+}
+
+template <typename IO, typename Cfg, bool ACC>
+__device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d, int lane,
+                                              float* carry /* [N], this warp's, in shared memory */) {
+  constexpr int N = Cfg::N, T = Cfg::T, LCH = Cfg::LCH;
+  const unsigned FULL = 0xffffffffu;
+  const int64_t row = static_cast<int64_t>(b) * p.dim + d;
+  const IO* urow = static_cast<const IO*>(p.u) + row * p.seqlen;
+  const IO* drow = static_cast<const IO*>(p.delta) + row * p.seqlen;
+  const IO* zrow = Cfg::GATE ? static_cast<const IO*>(p.z) + row * p.seqlen : nullptr;
+  IO* yrow = static_cast<IO*>(p.y) + row * p.seqlen;
+  const IO* Bb = static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * N * p.seqlen;
+  const IO* Cb = static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * N * p.seqlen;
+  const float* Arow = p.A + static_cast<int64_t>(d) * N;
+
+  if (lane < N) carry[lane] = p.h0 ? __ldg(p.h0 + row * N + lane) : 0.0f;
+  __syncwarp();
+  const float Dd = p.D ? __ldg(p.D + d) : 0.0f;
+  const float bias2 = p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f;
+
+  const int nch = (p.seqlen + LCH - 1) / LCH;
+#pragma unroll 1
+  for (int k = 0; k < nch; ++k) {
+    const int64_t l = static_cast<int64_t>(k) * LCH + lane * T;  // this lane's first position
+    float s[T], u[T], y[T];
+    load_run<IO, Cfg>(urow, l, p.seqlen, u);
+    load_run<IO, Cfg>(drow, l, p.seqlen, s);
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+      const float x2 = fmaf(s[i], kLog2e, bias2);
+      const float sv =
+          p.softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
+      s[i] = (l + i < p.seqlen) ? sv : 0.0f;  // past the end: identity pair (1, 0)
+      y[i] = 0.0f;
+    }
+#pragma unroll 1
+    for (int n = 0; n < N; ++n) {
+      const float An = __ldg(Arow + n);
+      const float IAn = (An == 0.0f) ? 0.0f : 1.0f / An;
+      const float isZn = (An == 0.0f) ? 1.0f : 0.0f;
+      float Bv[T], Cv[T], a[T], bb[T];
+      load_run<IO, Cfg>(Bb + static_cast<int64_t>(n) * p.seqlen, l, p.seqlen, Bv);
+      load_run<IO, Cfg>(Cb + static_cast<int64_t>(n) * p.seqlen, l, p.seqlen, Cv);
+      float P = 1.0f, H = 0.0f;
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        const float q = s[i] * An;
+        const float ahw = ex2(q);
+        const float X = Bv[i] * u[i];
+        if constexpr (!ACC) {
+          const float nK = X * (-IAn);       // -B u / A
+          a[i] = ahw;
+          bb[i] = fmaf(-ahw, nK, nK);        // (Abar - 1) B u / A
+        } else {
+          const float em1 = exp2m1_accurate(q, ahw);
+          a[i] = (fabsf(q) < 0.36f) ? 1.0f + em1 : ahw;
+          const float coef = fmaf(isZn, s[i] * kLn2, em1 * IAn);
+          bb[i] = coef * X;
+        }
+        H = fmaf(a[i], H, bb[i]);
+        P *= a[i];
+      }
+      // inclusive warp scan of (P, H) over lanes (lane order = position order)
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float Pu = __shfl_up_sync(FULL, P, o);
+        const float Hu = __shfl_up_sync(FULL, H, o);
+        if (lane >= o) {
+          H = fmaf(P, Hu, H);
+          P *= Pu;
+        }
+      }
+      const float Pe = __shfl_up_sync(FULL, P, 1);
+      const float He = __shfl_up_sync(FULL, H, 1);
+      const float P31 = __shfl_sync(FULL, P, 31);
+      const float H31 = __shfl_sync(FULL, H, 31);
+      const float cin = carry[n];
+      float hs = (lane == 0) ? cin : fmaf(Pe, cin, He);
+      __syncwarp();
+      if (lane == 0) carry[n] = fmaf(P31, cin, H31);
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        hs = fmaf(a[i], hs, bb[i]);
+        y[i] = fmaf(Cv[i], hs, y[i]);
+      }
+    }
+    float z[T];
+    if constexpr (Cfg::GATE) load_run<IO, Cfg>(zrow, l, p.seqlen, z);
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+      float v = fmaf(Dd, u[i], y[i]);
+      if constexpr (Cfg::GATE) v *= (ACC ? silu_accurate(z[i]) : silu_fast(z[i]));
+      y[i] = v;
+    }
+    store_run<IO, Cfg>(yrow, l, p.seqlen, y);
+    __syncwarp();
+  }
+  if (p.h_last && lane < N) p.h_last[row * N + lane] = carry[lane];
+}
+
+template <typename IO, typename Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS) scan_chunk_kernel(const ScanParams p) {
+  __shared__ float carry_smem[Cfg::WARPS][Cfg::N];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* carry = carry_smem[warp];
+  const int64_t ch = static_cast<int64_t>(blockIdx.x) * Cfg::WARPS + warp;
+  if (ch >= static_cast<int64_t>(p.batch) * p.dim) return;  // whole warp leaves together
+  const int b = static_cast<int>(ch / p.dim), d = static_cast<int>(ch % p.dim);
+  bool small_a = false;
+  if constexpr (sizeof(IO) == 2) {
+    for (int n = lane; n < Cfg::N; n += 32)
+      small_a |= !(fabsf(__ldg(p.A + static_cast<int64_t>(d) * Cfg::N + n)) >= kFastPathMinAbsA);
+    small_a = __any_sync(0xffffffffu, small_a);
+    if (!small_a) {
+      chunk_channel<IO, Cfg, false>(p, b, d, lane, carry);
+      return;
+    }
+  }
+  chunk_channel<IO, Cfg, true>(p, b, d, lane, carry);
+}
+
+}  // namespace ssm

@@ -1,0 +1,389 @@
+// ssm_api.cu -- C ABI of libssm (declared in include/ssm.h).
+//
+// Host side: argument validation (nothing is enqueued when it fails), choice of
+// kernel family, TMA descriptor encoding, launches on the caller's stream.
+// The library allocates no device memory and keeps no per-call state.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "ssm.h"
+#include "scan_channel.cuh"
+#include "scan_chunk.cuh"
+#include "state_update.cuh"
+
+namespace {
+
+using ssm::ChanCfg;
+using ssm::ChanMaps;
+using ssm::ChunkCfg;
+using ssm::ScanParams;
+using ssm::UpdateParams;
+using ssm::UpdCfg;
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr size_t kWorkspaceBytes = 256;
+// channel kernel only when there are enough (batch, dim) channels to fill the GPU
+// with lanes-over-channels warps; below this the chunk kernel's lanes-over-positions
+// layout keeps every SM busy.
+constexpr int64_t kChannelKernelMinChannels = 8192;
+
+thread_local std::string g_last_cuda_error;
+
+ssm_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_cuda_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return SSM_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------------------
+// TMA descriptor encoding through the driver entry point
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// 3-D map over a [d2][d1][d0] tensor (d0 fastest), box {box0, box1, 1},
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint32_t box0, uint32_t box1) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const uint64_t esz = bf16 ? 2 : 4;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * esz, d0 * d1 * esz};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+struct ScanCall {
+  int64_t batch, dim, dstate, seqlen;
+  bool bf16;
+  const void *u, *delta, *B, *C, *z;
+  const float *bias, *A, *D, *h0;
+  float* h_last;
+  void* y;
+  int softplus;
+};
+
+ssm_status validate_common(int64_t batch, int64_t dim, int64_t dstate, ssm_dtype io) {
+  if (batch < 1 || dim < 1 || dstate < 1) return SSM_ERR_INVALID_ARG;
+  if (io != SSM_DTYPE_F32 && io != SSM_DTYPE_BF16) return SSM_ERR_UNSUPPORTED;
+  if (dstate != 4 && dstate != 8 && dstate != 16) return SSM_ERR_UNSUPPORTED;
+  if (dim > INT32_MAX || batch > INT32_MAX) return SSM_ERR_INVALID_ARG;
+  return SSM_OK;
+}
+
+ssm_status validate_scan(const ScanCall& c, const void* workspace, size_t workspace_bytes) {
+  ssm_status st = validate_common(c.batch, c.dim, c.dstate, c.bf16 ? SSM_DTYPE_BF16 : SSM_DTYPE_F32);
+  if (st != SSM_OK) return st;
+  if (c.seqlen < 1 || c.seqlen > INT32_MAX - 4096) return SSM_ERR_INVALID_ARG;
+  // element counts must fit comfortably in 63 bits
+  if (c.batch > (int64_t(1) << 62) / c.dim / c.seqlen) return SSM_ERR_INVALID_ARG;
+  if (!c.u || !c.delta || !c.A || !c.B || !c.C || !c.y || !workspace) return SSM_ERR_INVALID_ARG;
+  const size_t esz = c.bf16 ? 2 : 4;
+  const void* io_ptrs[6] = {c.u, c.delta, c.B, c.C, c.y, c.z};
+  for (const void* q : io_ptrs)
+    if (q && !aligned(q, esz)) return SSM_ERR_INVALID_ARG;
+  const float* f_ptrs[5] = {c.A, c.D, c.bias, c.h0, c.h_last};
+  for (const float* q : f_ptrs)
+    if (q && !aligned(q, 4)) return SSM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16) || workspace_bytes < kWorkspaceBytes) return SSM_ERR_INVALID_ARG;
+  // the chunk kernel's grid has one CTA per 4 channels
+  if ((c.batch * c.dim + 3) / 4 > INT32_MAX) return SSM_ERR_INVALID_ARG;
+  return SSM_OK;
+}
+
+bool tma_eligible(const ScanCall& c) {
+  const int64_t esz = c.bf16 ? 2 : 4;
+  if ((c.seqlen * esz) % 16 != 0) return false;
+  const void* ptrs[6] = {c.u, c.delta, c.B, c.C, c.y, c.z};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return false;
+  return encode_fn() != nullptr;
+}
+
+bool vec_eligible(const ScanCall& c) {
+  const int64_t esz = c.bf16 ? 2 : 4;
+  if ((c.seqlen * esz) % 16 != 0) return false;
+  const void* ptrs[6] = {c.u, c.delta, c.B, c.C, c.y, c.z};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return false;
+  return true;
+}
+
+ScanParams make_params(const ScanCall& c, void* workspace) {
+  ScanParams p;
+  p.batch = static_cast<int>(c.batch);
+  p.dim = static_cast<int>(c.dim);
+  p.seqlen = static_cast<int>(c.seqlen);
+  p.dtiles = 1;
+  p.softplus = c.softplus;
+  p.A = c.A;
+  p.D = c.D;
+  p.bias = c.bias;
+  p.h0 = c.h0;
+  p.h_last = c.h_last;
+  p.status = static_cast<ssm::DeviceStatus*>(workspace);
+  p.u = c.u;
+  p.delta = c.delta;
+  p.z = c.z;
+  p.B = c.B;
+  p.C = c.C;
+  p.y = c.y;
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+template <typename IO, int N, bool GATE>
+ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t stream) {
+  constexpr int G = N / 4;                  // 4 states per lane
+  constexpr int S = (G == 1) ? 2 : 4;       // ring depth (G == 1 tiles are 4x larger)
+  using Cfg = ChanCfg<IO, N, G, GATE, S>;
+  ChanMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const bool bf = c.bf16;
+  const uint64_t L = c.seqlen, Dm = c.dim, Bt = c.batch, Nn = N;
+  if (!make_map(&maps.u, c.u, bf, L, Dm, Bt, Cfg::LC, Cfg::DT) ||
+      !make_map(&maps.delta, c.delta, bf, L, Dm, Bt, Cfg::LC, Cfg::DT) ||
+      !make_map(&maps.y, c.y, bf, L, Dm, Bt, Cfg::LC, Cfg::DT) ||
+      !make_map(&maps.B, c.B, bf, L, Nn, Bt, Cfg::LC, N) ||
+      !make_map(&maps.C, c.C, bf, L, Nn, Bt, Cfg::LC, N) ||
+      (GATE && !make_map(&maps.z, c.z, bf, L, Dm, Bt, Cfg::LC, Cfg::DT))) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled failed";
+    return SSM_ERR_CUDA;
+  }
+  ScanParams p = make_params(c, workspace);
+  p.dtiles = static_cast<int>((c.dim + Cfg::DT - 1) / Cfg::DT);
+  auto kern = ssm::scan_channel_kernel<IO, Cfg>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::SMEM_ALLOC);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel)");
+  const unsigned grid = static_cast<unsigned>(c.batch * p.dtiles);
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_ALLOC, stream>>>(maps, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "scan_channel launch");
+  return SSM_OK;
+}
+
+template <typename IO, int N, bool GATE, bool VEC>
+ssm_status launch_chunk(const ScanCall& c, void* workspace, cudaStream_t stream) {
+  using Cfg = ChunkCfg<IO, N, GATE, VEC>;
+  ScanParams p = make_params(c, workspace);
+  const int64_t channels = c.batch * c.dim;
+  const unsigned grid = static_cast<unsigned>((channels + Cfg::WARPS - 1) / Cfg::WARPS);
+  ssm::scan_chunk_kernel<IO, Cfg><<<grid, Cfg::THREADS, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "scan_chunk launch");
+  return SSM_OK;
+}
+
+template <typename IO, int N>
+ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s) {
+  const bool gate = c.z != nullptr;
+  if (algo == SSM_ALGO_CHANNEL) {
+    return gate ? launch_channel<IO, N, true>(c, ws, s) : launch_channel<IO, N, false>(c, ws, s);
+  }
+  if (vec_eligible(c))
+    return gate ? launch_chunk<IO, N, true, true>(c, ws, s) : launch_chunk<IO, N, false, true>(c, ws, s);
+  return gate ? launch_chunk<IO, N, true, false>(c, ws, s) : launch_chunk<IO, N, false, false>(c, ws, s);
+}
+
+template <typename IO>
+ssm_status dispatch_scan(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s) {
+  switch (c.dstate) {
+    case 4: return dispatch_scan_n<IO, 4>(c, algo, ws, s);
+    case 8: return dispatch_scan_n<IO, 8>(c, algo, ws, s);
+    case 16: return dispatch_scan_n<IO, 16>(c, algo, ws, s);
+    default: return SSM_ERR_UNSUPPORTED;
+  }
+}
+
+template <typename IO, int N, bool GATE, bool VEC>
+ssm_status launch_update(const UpdateParams& p, cudaStream_t stream) {
+  using Cfg = UpdCfg<IO, N, GATE, VEC>;
+  const int64_t threads = p.channels * Cfg::G;
+  const int64_t grid = (threads + Cfg::THREADS - 1) / Cfg::THREADS;
+  if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;
+  ssm::state_update_kernel<IO, Cfg><<<static_cast<unsigned>(grid), Cfg::THREADS, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "state_update launch");
+  return SSM_OK;
+}
+
+template <typename IO, int N>
+ssm_status dispatch_update_n(const UpdateParams& p, bool vec, cudaStream_t s) {
+  const bool gate = p.z != nullptr;
+  if (vec)
+    return gate ? launch_update<IO, N, true, true>(p, s) : launch_update<IO, N, false, true>(p, s);
+  return gate ? launch_update<IO, N, true, false>(p, s) : launch_update<IO, N, false, false>(p, s);
+}
+
+template <typename IO>
+ssm_status dispatch_update(const UpdateParams& p, int64_t dstate, bool vec, cudaStream_t s) {
+  switch (dstate) {
+    case 4: return dispatch_update_n<IO, 4>(p, vec, s);
+    case 8: return dispatch_update_n<IO, 8>(p, vec, s);
+    case 16: return dispatch_update_n<IO, 16>(p, vec, s);
+    default: return SSM_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+  (void)batch;
+  (void)dim;
+  (void)dstate;
+  (void)seqlen;
+  return kWorkspaceBytes;
+}
+
+ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                             ssm_dtype io, const void* u, const void* delta,
+                             const float* delta_bias, int delta_softplus, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* h0, float* h_last, void* y, void* workspace,
+                             size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream) {
+  if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_CHANNEL && algo != SSM_ALGO_CHUNK)
+    return SSM_ERR_UNSUPPORTED;
+  ScanCall c;
+  c.batch = batch;
+  c.dim = dim;
+  c.dstate = dstate;
+  c.seqlen = seqlen;
+  c.bf16 = (io == SSM_DTYPE_BF16);
+  c.u = u;
+  c.delta = delta;
+  c.B = B;
+  c.C = C;
+  c.z = z;
+  c.bias = delta_bias;
+  c.A = A;
+  c.D = D;
+  c.h0 = h0;
+  c.h_last = h_last;
+  c.y = y;
+  c.softplus = delta_softplus ? 1 : 0;
+  if (io != SSM_DTYPE_F32 && io != SSM_DTYPE_BF16) return SSM_ERR_UNSUPPORTED;
+  ssm_status st = validate_scan(c, workspace, workspace_bytes);
+  if (st != SSM_OK) return st;
+
+  if (algo == SSM_ALGO_AUTO)
+    algo = (c.batch * c.dim >= kChannelKernelMinChannels) ? SSM_ALGO_CHANNEL : SSM_ALGO_CHUNK;
+  if (algo == SSM_ALGO_CHANNEL && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(ssm::DeviceStatus), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
+  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s)
+                : dispatch_scan<float>(c, algo, workspace, s);
+}
+
+ssm_status ssm_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ssm_dtype io,
+                        const void* u, const void* delta, const float* delta_bias,
+                        int delta_softplus, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* h0, float* h_last, void* y,
+                        void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+  return ssm_scan_fwd_algo(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A,
+                           B, C, D, z, h0, h_last, y, workspace, workspace_bytes, SSM_ALGO_AUTO,
+                           stream);
+}
+
+ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, ssm_dtype io, float* h,
+                            const void* u, const void* delta, const float* delta_bias,
+                            int delta_softplus, const float* A, const void* B, const void* C,
+                            const float* D, const void* z, void* y, ssm_stream_t stream) {
+  ssm_status st = validate_common(batch, dim, dstate, io);
+  if (st != SSM_OK) return st;
+  if (batch > (int64_t(1) << 40) / dim) return SSM_ERR_INVALID_ARG;
+  if (!h || !u || !delta || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+  const size_t esz = (io == SSM_DTYPE_BF16) ? 2 : 4;
+  const void* io_ptrs[6] = {u, delta, B, C, y, z};
+  for (const void* q : io_ptrs)
+    if (q && !aligned(q, esz)) return SSM_ERR_INVALID_ARG;
+  const float* f_ptrs[4] = {h, A, D, delta_bias};
+  for (const float* q : f_ptrs)
+    if (q && !aligned(q, 4)) return SSM_ERR_INVALID_ARG;
+  UpdateParams p;
+  p.channels = batch * dim;
+  p.dim = static_cast<int>(dim);
+  p.softplus = delta_softplus ? 1 : 0;
+  p.h = h;
+  p.A = A;
+  p.D = D;
+  p.bias = delta_bias;
+  p.u = u;
+  p.delta = delta;
+  p.z = z;
+  p.B = B;
+  p.C = C;
+  p.y = y;
+  // 16-byte vectors for h and A, 4-element vectors for B and C
+  const bool vec = aligned(h, 16) && aligned(A, 16) && aligned(B, 4 * esz) && aligned(C, 4 * esz);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return (io == SSM_DTYPE_BF16) ? dispatch_update<uint16_t>(p, dstate, vec, s)
+                                : dispatch_update<float>(p, dstate, vec, s);
+}
+
+ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t stream) {
+  if (!workspace || !aligned(workspace, 16)) return SSM_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  ssm::DeviceStatus st;
+  e = cudaMemcpy(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(workspace status)");
+  return (st.flags & ssm::kStatusTimeout) ? SSM_ERR_DEVICE_TIMEOUT : SSM_OK;
+}
+
+const char* ssm_status_string(ssm_status status) {
+  switch (status) {
+    case SSM_OK: return "SSM_OK: success";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG: invalid size, NULL or misaligned pointer";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: dstate, dtype or algorithm not supported";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA: a CUDA call or kernel launch failed";
+    case SSM_ERR_DEVICE_TIMEOUT: return "SSM_ERR_DEVICE_TIMEOUT: a device-side wait hit its limit";
+  }
+  return "unknown ssm_status";
+}
+
+const char* ssm_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+int ssm_version(void) { return kVersion; }
+
+}  // extern "C"

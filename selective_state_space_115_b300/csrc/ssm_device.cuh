@@ -1,0 +1,269 @@
+// ssm_device.cuh -- device helpers shared by the libssm kernels (sm_103a).
+//
+// Inline PTX for the special-function unit (ex2/lg2/rcp), packed f32x2
+// arithmetic, bf16 packing, mbarriers and TMA (cp.async.bulk.tensor).
+// Every spin-wait here is bounded: on timeout it records SSM device status
+// bits and returns false; it never traps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+// ---------------------------------------------------------------------------
+// device status words (first bytes of the caller's workspace)
+// ---------------------------------------------------------------------------
+struct DeviceStatus {
+  unsigned int flags;        // bit 0: an mbarrier wait timed out
+  unsigned int where;        // kernel-specific code of the first timeout
+  unsigned int pad[2];
+};
+constexpr unsigned int kStatusTimeout = 1u;
+
+// A wait gives up after this much wall time (read from %globaltimer): far
+// beyond any legitimate TMA completion, short enough that a broken pipeline
+// ends the kernel with an error status instead of a hang.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ void record_timeout(DeviceStatus* st, unsigned int where) {
+  if (st) {
+    if ((atomicOr(&st->flags, kStatusTimeout) & kStatusTimeout) == 0u) st->where = where;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// special-function unit (approximate, hardware) and constants
+// ---------------------------------------------------------------------------
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// packed f32x2 arithmetic (two lanes of fp32 per instruction)
+// ---------------------------------------------------------------------------
+struct f2 {
+  float x, y;
+};
+__device__ __forceinline__ f2 mk2(float a, float b) { return f2{a, b}; }
+
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+// round both to bf16 (nearest even); lo in bits 0..15
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float v) {
+  return static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
+}
+
+// io element traits: float or bf16 (stored as uint16_t)
+template <typename IO>
+struct Io;
+template <>
+struct Io<float> {
+  static constexpr int kBytes = 4;
+  __device__ __forceinline__ static float load(const float* p) { return *p; }
+  __device__ __forceinline__ static float ldg(const float* p) { return __ldg(p); }
+  __device__ __forceinline__ static void store(float* p, float v) { *p = v; }
+};
+template <>
+struct Io<uint16_t> {
+  static constexpr int kBytes = 2;
+  __device__ __forceinline__ static float load(const uint16_t* p) { return bf16_to_f32(*p); }
+  __device__ __forceinline__ static float ldg(const uint16_t* p) {
+    return bf16_to_f32(__ldg(reinterpret_cast<const unsigned short*>(p)));
+  }
+  __device__ __forceinline__ static void store(uint16_t* p, float v) { *p = f32_to_bf16(v); }
+};
+
+// ---------------------------------------------------------------------------
+// exact-ish pieces for the fp32 (accurate) path
+// ---------------------------------------------------------------------------
+// 2^q - 1 without cancellation: Taylor series of e^x - 1 (x = q ln 2) for
+// |q| < 0.36 (truncation below 5e-8 relative); hardware ex2 minus one beyond,
+// where |2^q - 1| >= 0.22 so the subtraction loses nothing.
+__device__ __forceinline__ float exp2m1_accurate(float q, float a /* = ex2(q) */) {
+  // coefficients ln2^k / k!, k = 1..6
+  const float c1 = 0.69314718055994531f, c2 = 0.24022650695910071f,
+              c3 = 0.05550410866482158f, c4 = 0.00961812910762848f,
+              c5 = 0.00133335581464284f, c6 = 0.00015403530393381f;
+  float p = fmaf(c6, q, c5);
+  p = fmaf(p, q, c4);
+  p = fmaf(p, q, c3);
+  p = fmaf(p, q, c2);
+  p = fmaf(p, q, c1);
+  p = p * q;
+  return (fabsf(q) < 0.36f) ? p : (a - 1.0f);
+}
+
+// softplus in log2 units: returns log2(1 + 2^x2) (= softplus(x) * log2 e for x2 = x log2 e)
+__device__ __forceinline__ float softplus_log2_fast(float x2) {
+  const float s = lg2(1.0f + ex2(x2));
+  return (x2 > 20.0f) ? x2 : s;
+}
+// accurate variant for the fp32 path (library log1pf / expf)
+__device__ __forceinline__ float softplus_log2_accurate(float x2) {
+  const float x = x2 * kLn2;
+  const float sp = (x > 15.0f) ? x : log1pf(expf(x));
+  return sp * kLog2e;
+}
+
+// z * sigmoid(z)
+__device__ __forceinline__ float silu_fast(float z) { return z * rcp(1.0f + ex2(-z * kLog2e)); }
+__device__ __forceinline__ float silu_accurate(float z) { return z / (1.0f + expf(-z)); }
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared::cta) with bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// true when the phase with `parity` completed; false once kWaitLimitNs passed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA: tiled bulk tensor copies (3-D), global <-> shared
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+// load box at (c0 fastest, c1, c2) into smem, completing on `bar`
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// store smem box to global at (c0, c1, c2); out-of-range elements are not written
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until at most N committed store groups still read shared memory
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 16-byte vector shared loads/stores
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ float4 lds128f(const void* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a tile written by
+// TMA with CU_TENSOR_MAP_SWIZZLE_128B and 128-byte rows (tile base 1024-byte
+// aligned): the chunk index is XOR-ed with the row index modulo 8.
+__device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t c) {
+  return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+}  // namespace ssm

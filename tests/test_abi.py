@@ -1,0 +1,119 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_115_b300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*SSM_API\s+[^(]*?\b(ssm_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(binding.EXPORTED), names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.ssm_version() == 10000
+
+
+def test_status_strings():
+    for st in range(5):
+        s = binding.status_string(st)
+        assert s.startswith("SSM_"), s
+    assert "unknown" in binding.status_string(99)
+
+
+def test_workspace_size():
+    lib = binding.library()
+    assert lib.ssm_scan_fwd_workspace_size(8, 5120, 16, 2048) >= 256
+    assert lib.ssm_scan_fwd_workspace_size(8, 5120, 16, 2048) % 16 == 0
+
+
+# fake device addresses: validation must fail before anything dereferences them
+P = 0x7F0000000000
+WS = 0x7F0000100000
+
+
+def scan(lib, batch=2, dim=8, dstate=16, seqlen=64, io=1, u=P, delta=P, bias=None, sp=1, A=P,
+         B=P, C=P, D=None, z=None, h0=None, hl=None, y=P, ws=WS, wsb=256, algo=None):
+    args = [batch, dim, dstate, seqlen, io, u, delta, bias, sp, A, B, C, D, z, h0, hl, y, ws, wsb]
+    args = [ctypes.c_void_p(a) if isinstance(a, int) and i >= 5 and i not in (8, 18) else a
+            for i, a in enumerate(args)]
+    if algo is None:
+        return lib.ssm_scan_fwd(*args, None)
+    return lib.ssm_scan_fwd_algo(*args, algo, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(batch=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(dim=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=-5), binding.SSM_ERR_INVALID_ARG),
+    (dict(dstate=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(dstate=32), binding.SSM_ERR_UNSUPPORTED),
+    (dict(dstate=12), binding.SSM_ERR_UNSUPPORTED),
+    (dict(io=7), binding.SSM_ERR_UNSUPPORTED),
+    (dict(u=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(delta=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(A=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(B=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(C=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(y=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(ws=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(wsb=16), binding.SSM_ERR_INVALID_ARG),
+    (dict(ws=WS + 8), binding.SSM_ERR_INVALID_ARG),         # workspace not 16-byte aligned
+    (dict(u=P + 1), binding.SSM_ERR_INVALID_ARG),           # bf16 pointer not 2-byte aligned
+    (dict(io=0, u=P + 2), binding.SSM_ERR_INVALID_ARG),     # fp32 pointer not 4-byte aligned
+    (dict(A=P + 2), binding.SSM_ERR_INVALID_ARG),
+    (dict(h0=P + 1), binding.SSM_ERR_INVALID_ARG),
+    (dict(batch=1 << 40, dim=1 << 20), binding.SSM_ERR_INVALID_ARG),
+    (dict(algo=9), binding.SSM_ERR_UNSUPPORTED),
+])
+def test_scan_validation(kw, expect):
+    lib = binding.library()
+    assert scan(lib, **kw) == expect
+
+
+def update(lib, batch=4, dim=8, dstate=16, io=1, h=P, u=P, delta=P, bias=None, sp=1, A=P, B=P,
+           C=P, D=None, z=None, y=P):
+    args = [batch, dim, dstate, io, h, u, delta, bias, sp, A, B, C, D, z, y]
+    args = [ctypes.c_void_p(a) if isinstance(a, int) and i >= 4 and i != 8 else a
+            for i, a in enumerate(args)]
+    return lib.ssm_state_update(*args, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(batch=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(dim=-1), binding.SSM_ERR_INVALID_ARG),
+    (dict(dstate=2), binding.SSM_ERR_UNSUPPORTED),
+    (dict(io=3), binding.SSM_ERR_UNSUPPORTED),
+    (dict(h=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(u=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(B=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(y=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(h=P + 2), binding.SSM_ERR_INVALID_ARG),
+    (dict(u=P + 1), binding.SSM_ERR_INVALID_ARG),
+])
+def test_update_validation(kw, expect):
+    lib = binding.library()
+    assert update(lib, **kw) == expect
+
+
+def test_read_status_rejects_null():
+    lib = binding.library()
+    assert lib.ssm_read_device_status(None, None) == binding.SSM_ERR_INVALID_ARG

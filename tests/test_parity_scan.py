@@ -1,0 +1,296 @@
+"""GPU parity of the selective-scan forward (through the C ABI) against the fp64 oracle.
+
+Tolerances (error metric in tests/helpers.py): 1e-4 for fp32 io, 2e-2 for bf16 io
+with fp32 state.  Every configuration runs both kernel families.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from selective_state_space_115_b300 import workloads as W
+from tests.helpers import TOL, from_torch, rel_err, sample_rows, torch_f32, torch_io
+
+pytestmark = pytest.mark.gpu
+ALGOS = ["channel", "chunk"]
+NTHREADS = os.cpu_count() or 1
+
+
+def S():
+    from selective_state_space_115_b300 import binding
+    return binding
+
+
+def gpu_scan(x, io, algo, softplus=True, return_last_state=False, out=None):
+    import torch
+    r = S().scan_fwd(torch_io(x["u"], io), torch_io(x["delta"], io), torch_f32(x["A"]),
+                     torch_io(x["B"], io), torch_io(x["C"], io), D=torch_f32(x.get("D")),
+                     z=torch_io(x.get("z"), io), delta_bias=torch_f32(x.get("delta_bias")),
+                     delta_softplus=softplus, h0=torch_f32(x.get("h0")),
+                     return_last_state=return_last_state, algo=algo, out=out)
+    torch.cuda.synchronize()
+    assert S().read_device_status() == 0
+    return r
+
+
+def f64(x, io):
+    return None if x is None else W.to_f64(x, io)
+
+
+def oracle_full(x, io, softplus=True, return_last_state=False):
+    return oracle.scan_fwd(f64(x["u"], io), f64(x["delta"], io), x["A"], f64(x["B"], io),
+                           f64(x["C"], io), D=x.get("D"), z=f64(x.get("z"), io),
+                           delta_bias=x.get("delta_bias"), delta_softplus=softplus,
+                           h0=x.get("h0"), return_last_state=return_last_state,
+                           nthreads=NTHREADS)
+
+
+def oracle_rows(x, io, rows, return_last_state=False):
+    b, d, L = x["u"].shape
+    take = lambda a: None if a is None else W.to_f64(a, io).reshape(b * d, L)[rows]  # noqa: E731
+    return oracle.scan_rows(rows, take(x["u"]), take(x["delta"]), x["A"], f64(x["B"], io),
+                            f64(x["C"], io), b, d, D=x.get("D"), z_rows=take(x.get("z")),
+                            delta_bias=x.get("delta_bias"), h0=x.get("h0"),
+                            return_last_state=return_last_state)
+
+
+# ---------------------------------------------------------------------------
+# the workloads at full size
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tiny(algo):
+    cfg = W.SCAN_CONFIGS["tiny"]
+    x = W.make_scan_inputs(cfg, seed=0)
+    y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
+    ref, hr = oracle_full(x, cfg.io, return_last_state=True)
+    assert rel_err(from_torch(y), ref) <= TOL[cfg.io]
+    assert rel_err(from_torch(hl), hr) <= TOL[cfg.io]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_130m_full(algo):
+    cfg = W.SCAN_CONFIGS["130m"]
+    x = W.make_scan_inputs(cfg, seed=0)
+    y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
+    ref, hr = oracle_full(x, cfg.io, return_last_state=True)
+    e = rel_err(from_torch(y), ref)
+    print(f"130m {algo}: max rel err {e:.3e}")
+    assert e <= TOL[cfg.io]
+    assert rel_err(from_torch(hl), hr) <= TOL[cfg.io]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_2p8b_sampled(algo):
+    cfg = W.SCAN_CONFIGS["2p8b"]
+    x = W.make_scan_inputs(cfg, seed=0)
+    y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
+    yg = from_torch(y).reshape(cfg.batch * cfg.dim, cfg.seqlen)
+    assert np.isfinite(yg).all()
+    rows = sample_rows(cfg.batch, cfg.dim, 48, seed=1)
+    ref, hr = oracle_rows(x, cfg.io, rows, return_last_state=True)
+    e = rel_err(yg[rows], ref)
+    print(f"2p8b {algo}: max rel err over {len(rows)} rows {e:.3e}")
+    assert e <= TOL[cfg.io]
+    assert rel_err(from_torch(hl).reshape(-1, cfg.dstate)[rows], hr) <= 1e-3
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_long_sampled(algo):
+    cfg = W.SCAN_CONFIGS["long"]
+    x = W.make_scan_inputs(cfg, seed=0)
+    y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
+    yg = from_torch(y).reshape(cfg.batch * cfg.dim, cfg.seqlen)
+    assert np.isfinite(yg).all()
+    rows = np.array([0, 1, 777, 1535], dtype=np.int64)
+    ref, hr = oracle_rows(x, cfg.io, rows, return_last_state=True)
+    e = rel_err(yg[rows], ref)
+    print(f"long {algo}: max rel err over {len(rows)} rows {e:.3e}")
+    assert e <= TOL[cfg.io]
+    assert rel_err(from_torch(hl).reshape(-1, cfg.dstate)[rows], hr) <= 1e-3
+
+
+# ---------------------------------------------------------------------------
+# odd shapes, optional arguments, both dtypes
+# ---------------------------------------------------------------------------
+SHAPES = [
+    # io, batch, dim, dstate, seqlen, gate, h0
+    (W.F32, 1, 1, 4, 1, False, False),
+    (W.BF16, 1, 3, 8, 3, True, True),
+    (W.F32, 2, 37, 16, 69, True, True),       # ragged dim tile and ragged L tail
+    (W.BF16, 3, 37, 16, 72, True, False),     # TMA-eligible L, ragged dim
+    (W.BF16, 2, 100, 8, 1000, False, True),
+    (W.F32, 1, 64, 4, 4096, True, False),
+    (W.BF16, 2, 33, 16, 517, True, True),     # L not a multiple of 8: no TMA
+    (W.F32, 1, 130, 16, 2, False, True),
+]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("io,batch,dim,dstate,seqlen,gate,h0", SHAPES)
+def test_shapes(algo, io, batch, dim, dstate, seqlen, gate, h0):
+    cfg = W.ScanConfig("t", batch, dim, dstate, seqlen, io, gate=gate, dt_bias=True,
+                       d_skip="normal", description="")
+    x = W.make_scan_inputs(cfg, seed=seqlen + dim, with_h0=h0)
+    y, hl = gpu_scan(x, io, algo, return_last_state=True)
+    ref, hr = oracle_full(x, io, return_last_state=True)
+    assert rel_err(from_torch(y), ref) <= TOL[io]
+    assert rel_err(from_torch(hl), hr) <= (1e-4 if io == W.F32 else 1e-3)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("io", [W.F32, W.BF16])
+def test_optional_arguments_absent(algo, io):
+    cfg = W.ScanConfig("t", 2, 40, 16, 256, io, gate=False, dt_bias=False, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=5)
+    x["D"] = None
+    x["delta_bias"] = None
+    # delta used as dt directly (no softplus): keep it positive
+    x32 = np.abs(W.to_f64(x["delta"], io)).astype(np.float32) * np.float32(0.05)
+    x["delta"] = W.encode(x32, io)
+    y = gpu_scan(x, io, algo, softplus=False)
+    ref = oracle_full(x, io, softplus=False)
+    assert rel_err(from_torch(y), ref) <= TOL[io]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("io", [W.F32, W.BF16])
+def test_zero_and_small_A(algo, io):
+    """A == 0 uses the dt limit; tiny |A| must stay accurate (bf16 switches to the
+    accurate path)."""
+    cfg = W.ScanConfig("t", 1, 48, 8, 512, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=11)
+    A = x["A"].copy()
+    A[0, :] = 0.0
+    A[5, 3] = -1e-7
+    A[9, :] = -np.float32(1e-3) * np.arange(1, 9, dtype=np.float32)
+    A[20, 1] = 0.0
+    x["A"] = A
+    y = gpu_scan(x, io, algo)
+    ref = oracle_full(x, io)
+    assert rel_err(from_torch(y), ref) <= TOL[io]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_large_and_tiny_dt(algo):
+    """softplus saturation (raw delta up to +60) and vanishing dt (raw down to -60)."""
+    io = W.F32
+    cfg = W.ScanConfig("t", 1, 32, 16, 256, io, gate=True, dt_bias=False, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=12)
+    rng = np.random.default_rng(3)
+    x["delta"] = rng.uniform(-60, 60, size=x["delta"].shape).astype(np.float32)
+    y = gpu_scan(x, io, algo)
+    ref = oracle_full(x, io)
+    assert rel_err(from_torch(y), ref) <= TOL[io]
+
+
+# ---------------------------------------------------------------------------
+# memory safety, fallbacks, properties
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("io", [W.F32, W.BF16])
+def test_guard_bands_untouched(algo, io):
+    """y lives inside a NaN-filled buffer: the bands around it must stay NaN and y
+    must be fully written (no NaN left)."""
+    import torch
+    cfg = W.ScanConfig("t", 2, 37, 16, 136, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=13)
+    n = cfg.batch * cfg.dim * cfg.seqlen
+    guard = 4096
+    dt = torch.float32 if io == W.F32 else torch.bfloat16
+    buf = torch.full((n + 2 * guard,), float("nan"), dtype=dt, device="cuda")
+    y = buf[guard:guard + n].view(cfg.batch, cfg.dim, cfg.seqlen)
+    gpu_scan(x, io, algo, out=y)
+    b = from_torch(buf)
+    assert np.isnan(b[:guard]).all() and np.isnan(b[guard + n:]).all()
+    assert np.isfinite(b[guard:guard + n]).all()
+    ref = oracle_full(x, io)
+    assert rel_err(from_torch(y), ref) <= TOL[io]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_unaligned_pointers_fall_back(algo):
+    """Tensors offset by one element from a 16-byte boundary take the element-load path."""
+    import torch
+    io = W.BF16
+    cfg = W.ScanConfig("t", 1, 24, 16, 128, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=14)
+
+    def shifted(a):
+        t = torch_io(a, io)
+        big = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+        v = big[1:].view(t.shape)
+        v.copy_(t)
+        return v
+
+    r = S().scan_fwd(shifted(x["u"]), shifted(x["delta"]), torch_f32(x["A"]), shifted(x["B"]),
+                     shifted(x["C"]), D=torch_f32(x["D"]), z=shifted(x["z"]),
+                     delta_bias=torch_f32(x["delta_bias"]), algo=algo)
+    torch.cuda.synchronize()
+    assert rel_err(from_torch(r), oracle_full(x, io)) <= TOL[io]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_split_invariance(algo):
+    """scan(0..L) == scan(0..m) then scan(m..L) from h_last (checkpoint / resume)."""
+    io = W.F32
+    cfg = W.ScanConfig("t", 2, 40, 16, 1024, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=15)
+    m = 384
+    part = lambda a, sl: None if a is None else np.ascontiguousarray(a[..., sl])  # noqa: E731
+    xa = {k: (part(v, slice(0, m)) if k in ("u", "delta", "z", "B", "C") else v)
+          for k, v in x.items()}
+    xb = {k: (part(v, slice(m, None)) if k in ("u", "delta", "z", "B", "C") else v)
+          for k, v in x.items()}
+    y, hl = gpu_scan(x, io, algo, return_last_state=True)
+    ya, ha = gpu_scan(xa, io, algo, return_last_state=True)
+    xb["h0"] = from_torch(ha).astype(np.float32)
+    yb, hb = gpu_scan(xb, io, algo, return_last_state=True)
+    yy = np.concatenate([from_torch(ya), from_torch(yb)], axis=-1)
+    assert rel_err(yy, from_torch(y)) <= 1e-5
+    assert rel_err(from_torch(hb), from_torch(hl)) <= 1e-5
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_linearity_in_u(algo):
+    io = W.F32
+    cfg = W.ScanConfig("t", 1, 64, 16, 512, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x1 = W.make_scan_inputs(cfg, seed=16)
+    x2 = dict(x1)
+    x2["u"] = np.random.default_rng(7).standard_normal(x1["u"].shape).astype(np.float32)
+    x12 = dict(x1)
+    x12["u"] = (np.float32(1.5) * x1["u"] - np.float32(0.5) * x2["u"]).astype(np.float32)
+    y1 = from_torch(gpu_scan(x1, io, algo))
+    y2 = from_torch(gpu_scan(x2, io, algo))
+    y12 = from_torch(gpu_scan(x12, io, algo))
+    assert rel_err(y12, 1.5 * y1 - 0.5 * y2) <= 1e-4
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_deterministic(algo):
+    cfg = W.ScanConfig("t", 2, 96, 16, 640, W.BF16, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=17)
+    a = from_torch(gpu_scan(x, cfg.io, algo))
+    b = from_torch(gpu_scan(x, cfg.io, algo))
+    assert np.array_equal(a, b)
+
+
+def test_auto_matches_explicit_choice():
+    cfg = W.SCAN_CONFIGS["2p8b"]
+    x = W.make_scan_inputs(cfg, seed=0, batch=2)  # 10240 channels: the channel kernel
+    a = from_torch(gpu_scan(x, cfg.io, "auto"))
+    b = from_torch(gpu_scan(x, cfg.io, "channel"))
+    assert np.array_equal(a, b)
+    cfg = W.SCAN_CONFIGS["130m"]
+    x = W.make_scan_inputs(cfg, seed=0, seqlen=256)  # 3072 channels: the chunk kernel
+    a = from_torch(gpu_scan(x, cfg.io, "auto"))
+    b = from_torch(gpu_scan(x, cfg.io, "chunk"))
+    assert np.array_equal(a, b)
