@@ -136,6 +136,36 @@ SSM_API ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate,
                              size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream);
 
 /*
+ * ssm_scan_fwd for callers that cannot allocate device memory, such as code
+ * running under an allocator it does not own (a custom arena, a memory pool that
+ * forbids new reservations) or inside a region where cudaMalloc is not allowed.
+ * The pages have no counterpart to this entry point; it exists only for such
+ * callers.  It allocates nothing: instead of a caller-provided workspace it uses
+ * a scratch array of 4096 bytes reserved statically in the library, which every
+ * GPU that loads the library keeps until the process exits.  The caller still
+ * passes all inputs and outputs, exactly as for ssm_scan_fwd (kernel chosen as
+ * by SSM_ALGO_AUTO).
+ *  - The first call on a device looks up that device's scratch address
+ *    (cudaGetSymbolAddress) with the caller's current device, which must be the
+ *    device of the tensors and of `stream`; make that first call before any
+ *    stream capture.
+ *  - Sizes whose scratch requirement (ssm_scan_fwd_workspace_size) exceeds the
+ *    reserved 4096 bytes are rejected with SSM_ERR_UNSUPPORTED and a message in
+ *    ssm_last_cuda_error(); nothing is enqueued then.
+ *  - Every call shares the one array per device and it keeps the last call's
+ *    contents; its status words are cleared on `stream` before each kernel.
+ *    Calls that overlap on the GPU (different streams, no ordering) race on it.
+ *  - Device-side wait timeouts are recorded in that shared array and are not
+ *    reported back by this entry point.
+ */
+SSM_API ssm_status ssm_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                        ssm_dtype io, const void* u, const void* delta,
+                                        const float* delta_bias, int delta_softplus,
+                                        const float* A, const void* B, const void* C,
+                                        const float* D, const void* z, const float* h0,
+                                        float* h_last, void* y, ssm_stream_t stream);
+
+/*
  * Single-token recurrent state update (decode): one step of the scan for every
  * (batch, dim) channel, h read and written in place (Mamba_Model_Report.md,
  * section 6, ssm_step, with the ZOH discretisation above).
@@ -161,7 +191,8 @@ SSM_API ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t st
 /* Static description of a status code. */
 SSM_API const char* ssm_status_string(ssm_status status);
 
-/* Message of the last CUDA error seen by a call on this host thread ("" if none). */
+/* Detail of the last CUDA error (or rejected no-alloc request) seen by a call on
+ * this host thread ("" if none). */
 SSM_API const char* ssm_last_cuda_error(void);
 
 /* Library version: major * 10000 + minor * 100 + patch. */

@@ -34,8 +34,8 @@ _ALGOS = {"auto": ALGO_AUTO, "channel": ALGO_CHANNEL, "chunk": ALGO_CHUNK,
 
 # every symbol include/ssm.h declares
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_algo",
-            "ssm_state_update", "ssm_read_device_status", "ssm_status_string",
-            "ssm_last_cuda_error", "ssm_version")
+            "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
+            "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
 
 class SsmError(RuntimeError):
@@ -79,6 +79,8 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_fwd.argtypes = scan_args + [_vp]
         lib.ssm_scan_fwd_algo.restype = _int
         lib.ssm_scan_fwd_algo.argtypes = scan_args + [_int, _vp]
+        lib.ssm_scan_fwd_noalloc.restype = _int
+        lib.ssm_scan_fwd_noalloc.argtypes = scan_args[:17] + [_vp]
         lib.ssm_state_update.restype = _int
         lib.ssm_state_update.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int, _vp,
                                          _vp, _vp, _vp, _vp, _vp, _vp]

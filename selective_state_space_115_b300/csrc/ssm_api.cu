@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "ssm.h"
@@ -258,6 +259,44 @@ ssm_status dispatch_update(const UpdateParams& p, int64_t dstate, bool vec, cuda
   }
 }
 
+// ---------------------------------------------------------------------------
+// statically reserved scratch for ssm_scan_fwd_noalloc
+// ---------------------------------------------------------------------------
+// Device scratch of fixed size that every GPU loading this library holds until
+// the process exits.  Host code must not pass the symbol itself to a kernel (on
+// the host it only names a stand-in object); the device address is looked up
+// once per device with cudaGetSymbolAddress.
+constexpr size_t kNoAllocScratchBytes = 4096;
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of the static scratch on the current device (set-up on first use).
+ssm_status noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices) {
+    g_last_cuda_error = "ssm_scan_fwd_noalloc: device ordinal beyond the supported range";
+    return SSM_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SSM_OK;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -321,6 +360,26 @@ ssm_status ssm_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seql
                         void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
   return ssm_scan_fwd_algo(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A,
                            B, C, D, z, h0, h_last, y, workspace, workspace_bytes, SSM_ALGO_AUTO,
+                           stream);
+}
+
+ssm_status ssm_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                ssm_dtype io, const void* u, const void* delta,
+                                const float* delta_bias, int delta_softplus, const float* A,
+                                const void* B, const void* C, const float* D, const void* z,
+                                const float* h0, float* h_last, void* y, ssm_stream_t stream) {
+  const size_t need = ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen);
+  if (need > kNoAllocScratchBytes) {
+    g_last_cuda_error = "ssm_scan_fwd_noalloc: these sizes need " + std::to_string(need) +
+                        " bytes of scratch, more than the " +
+                        std::to_string(kNoAllocScratchBytes) + " bytes reserved statically";
+    return SSM_ERR_UNSUPPORTED;
+  }
+  void* scratch = nullptr;
+  const ssm_status st = noalloc_scratch(&scratch);
+  if (st != SSM_OK) return st;
+  return ssm_scan_fwd_algo(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A,
+                           B, C, D, z, h0, h_last, y, scratch, kNoAllocScratchBytes, SSM_ALGO_AUTO,
                            stream);
 }
 
