@@ -18,6 +18,7 @@ after the main loop and reported under "decode".
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import glob
 import hashlib
 import json
@@ -384,7 +385,7 @@ def run_gpu(args):
                     "bytes_per_step": bytes_step, "peak_kind": peak_kind},
             "roofline": {"bound": "alu", "achieved": achieved_exp, "peak": ex2_peak,
                          "unit": "Texp/s", "frac": achieved_exp / ex2_peak, "traffic": traffic,
-                         "kernel": "scan_channel_kernel<bf16, N=16, G=4, gate>",
+                         "kernel": "scan_channel_kernel<bf16, N=16, gate> (one lane per channel)",
                          "units_per_launch": CFG.updates,
                          "peak_note": "148 SMs x 32 ex2/clk/SM (measured ex2.approx.f32 "
                                       "throughput) x 2032 MHz max SM clock"},
@@ -484,7 +485,12 @@ def main():
     ap.add_argument("--impl", default="libssm", choices=["libssm", "reference"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch of the scan workload (smaller cases for ncu)")
     args = ap.parse_args()
+    if args.batch:
+        global CFG
+        CFG = dataclasses.replace(CFG, batch=args.batch)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -62,22 +62,30 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a [d2][d1][d0] tensor (d0 fastest), box {box0, box1, 1},
-// 128-byte swizzle, zero fill outside the tensor.
+// 3-D map over a [d2][d1][d0] tensor (d0 fastest), box {box0, box1, 1}, zero fill
+// outside the tensor.  The box row (box0 elements) must be exactly one swizzle
+// span (32, 64 or 128 bytes): the kernels index their tiles with that span's
+// XOR pattern and size them for rows of exactly that width.
 bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
               uint32_t box0, uint32_t box1) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const uint64_t esz = bf16 ? 2 : 4;
+  CUtensorMapSwizzle swz;
+  switch (box0 * esz) {
+    case 32: swz = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    case 64: swz = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 128: swz = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    default: return false;
+  }
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {d0 * esz, d0 * d1 * esz};
   const cuuint32_t box[3] = {box0, box1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r =
       enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -167,9 +175,9 @@ ScanParams make_params(const ScanCall& c, void* workspace) {
 // ---------------------------------------------------------------------------
 template <typename IO, int N, bool GATE>
 ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t stream) {
-  constexpr int G = N / 4;                  // 4 states per lane
-  constexpr int S = (G == 1) ? 2 : 4;       // ring depth (G == 1 tiles are 4x larger)
-  using Cfg = ChanCfg<IO, N, G, GATE, S>;
+  // 32-byte chunk rows (16 bf16 / 8 fp32 positions), 4-stage ring: ~69 KB of
+  // shared memory per 128-channel CTA, three CTAs per SM.
+  using Cfg = ChanCfg<IO, N, GATE, 4, 32>;
   ChanMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const bool bf = c.bf16;

@@ -259,11 +259,4 @@ __device__ __forceinline__ float4 lds128f(const void* p) {
   return *reinterpret_cast<const float4*>(p);
 }
 
-// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a tile written by
-// TMA with CU_TENSOR_MAP_SWIZZLE_128B and 128-byte rows (tile base 1024-byte
-// aligned): the chunk index is XOR-ed with the row index modulo 8.
-__device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t c) {
-  return r * 128u + ((c ^ (r & 7u)) << 4);
-}
-
 }  // namespace ssm
