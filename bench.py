@@ -293,7 +293,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        S.scan_fwd(u, dl, A, B, C, D=Dv, z=z, delta_bias=bias, algo="auto", out=y)
+        S.scan_fwd(u, dl, A, B, C, D=Dv, z=z, delta_bias=bias, algo=args.algo, out=y)
 
     for _ in range(args.warmup):
         step()
@@ -348,7 +348,7 @@ def run_gpu(args):
         du, dd, dz = hu.to(dev, non_blocking=True), hd.to(dev, non_blocking=True), \
             hz.to(dev, non_blocking=True)
         dB, dC = hB.to(dev, non_blocking=True), hC.to(dev, non_blocking=True)
-        yy = S.scan_fwd(du, dd, A, dB, dC, D=Dv, z=dz, delta_bias=bias, algo="auto")
+        yy = S.scan_fwd(du, dd, A, dB, dC, D=Dv, z=dz, delta_bias=bias, algo=args.algo)
         hy.copy_(yy, non_blocking=True)
 
     e2e_step()
@@ -485,6 +485,9 @@ def main():
     ap.add_argument("--impl", default="libssm", choices=["libssm", "reference"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--algo", default="auto",
+                    choices=["auto", "channel", "chunk", "channel_l1", "channel_l2", "channel_l4"],
+                    help="scan kernel family (default: the library's own choice)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch of the scan workload (smaller cases for ncu)")
     args = ap.parse_args()

@@ -80,12 +80,17 @@ typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype;
  * (batch, dim) channels: many channels -> CHANNEL, few -> CHUNK. */
 typedef enum {
     SSM_ALGO_AUTO = 0,
-    SSM_ALGO_CHANNEL = 1,  /* lanes over channels; each lane runs its channel's whole
-                              sequence with its state slice in registers; L streamed
-                              through shared memory in TMA chunks */
-    SSM_ALGO_CHUNK = 2     /* lanes over positions; warp-shuffle associative scan of
-                              (Abar, Bbar u) pairs inside each chunk, state carried
-                              across chunks */
+    SSM_ALGO_CHANNEL = 1,     /* lanes over channels; 1, 2 or 4 adjacent lanes run a
+                                 channel's whole sequence, each with a slice of its
+                                 states in registers; L streamed through shared memory
+                                 in TMA chunks.  The lanes-per-channel split is chosen
+                                 from the sizes (finer split = more, shorter warps) */
+    SSM_ALGO_CHUNK = 2,       /* lanes over positions; warp-shuffle associative scan of
+                                 (Abar, Bbar u) pairs inside each chunk, state carried
+                                 across chunks */
+    SSM_ALGO_CHANNEL_L1 = 3,  /* CHANNEL with a fixed split: 1 lane per channel */
+    SSM_ALGO_CHANNEL_L2 = 4,  /* 2 lanes per channel (dstate 8 or 16) */
+    SSM_ALGO_CHANNEL_L4 = 5   /* 4 lanes per channel (dstate 16) */
 } ssm_algo;
 
 /*
@@ -125,9 +130,11 @@ SSM_API ssm_status ssm_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int6
                         void* workspace, size_t workspace_bytes, ssm_stream_t stream);
 
 /* ssm_scan_fwd with an explicit kernel family (SSM_ALGO_AUTO behaves exactly
- * like ssm_scan_fwd).  CHANNEL falls back to CHUNK when the TMA alignment rules
- * do not hold (seqlen * element size not a multiple of 16, or a tensor base not
- * 16-byte aligned). */
+ * like ssm_scan_fwd).  The CHANNEL variants fall back to CHUNK when the TMA
+ * alignment rules do not hold (seqlen * element size not a multiple of 16, or a
+ * tensor base not 16-byte aligned); a fixed lanes-per-channel split that would
+ * leave a lane fewer than 4 states (L2 with dstate 4, L4 with dstate 4 or 8)
+ * returns SSM_ERR_UNSUPPORTED. */
 SSM_API ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                              ssm_dtype io, const void* u, const void* delta,
                              const float* delta_bias, int delta_softplus, const float* A,

@@ -29,8 +29,13 @@ DTYPE_BF16 = 1
 ALGO_AUTO = 0
 ALGO_CHANNEL = 1
 ALGO_CHUNK = 2
+ALGO_CHANNEL_L1 = 3
+ALGO_CHANNEL_L2 = 4
+ALGO_CHANNEL_L4 = 5
 _ALGOS = {"auto": ALGO_AUTO, "channel": ALGO_CHANNEL, "chunk": ALGO_CHUNK,
-          ALGO_AUTO: ALGO_AUTO, ALGO_CHANNEL: ALGO_CHANNEL, ALGO_CHUNK: ALGO_CHUNK}
+          "channel_l1": ALGO_CHANNEL_L1, "channel_l2": ALGO_CHANNEL_L2,
+          "channel_l4": ALGO_CHANNEL_L4}
+_ALGOS.update({v: v for v in list(_ALGOS.values())})
 
 # every symbol include/ssm.h declares
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_algo",

@@ -1,24 +1,29 @@
 // scan_channel.cuh -- selective-scan forward, "channel" kernel family.
 //
-// Mapping (B300, sm_103a): one lane owns one (batch, dim) channel and all of its
-// N states, in registers, for the whole sequence.  The recurrence along L is
-// then a plain sequential loop per lane: no cross-lane scan, no exchange, and
-// N/2 independent packed (f32x2) state chains per position to hide latency.
-// The (B, L, D, N) tensor never leaves registers (velog Mamba review, section
-// 3.3 "Kernel Fusion": load the 3-D inputs to SRAM, discretise and recur there,
-// write only the 3-D output).
+// Mapping (B300, sm_103a): LPC lanes (1, 2 or 4, adjacent in the warp) own one
+// (batch, dim) channel; each of them holds NS = N / LPC of its states in
+// registers for the whole sequence.  The recurrence along L is a plain
+// sequential loop per lane -- no cross-lane scan -- with NS/2 independent packed
+// (f32x2) state chains per position to hide latency.  The (B, L, D, N) tensor
+// never leaves registers (velog Mamba review, section 3.3 "Kernel Fusion": load
+// the 3-D inputs to SRAM, discretise and recur there, write only the 3-D output).
 //
-// One CTA = 4 warps = 128 channels of one batch row.  L streams in chunks of
-// RB bytes per row (16 or 32 bf16 positions, 8..32 fp32 positions):
-//   * u, delta, z tiles [128 x chunk] and the B, C tiles [N x chunk] are loaded
+// Splitting a channel over 2 or 4 lanes gives 2x / 4x more, shorter warps: more
+// latency hiding per SM sub-partition and finer load balance over the 148 SMs.
+// The per-position work (softplus, D skip, gate, rounding, store) is split over
+// the LPC lanes too -- each takes TB/LPC positions of every 16-byte block -- and
+// two short xor-shuffle exchanges join them: an all-gather of the step sizes
+// before the recurrence and a reduce-scatter of the partial contractions after.
+//
+// One CTA = 4 warps = 128 / LPC channels of one batch row.  L streams in chunks
+// of RB bytes per row:
+//   * u, delta, z tiles [DT x chunk] and the B, C tiles [N x chunk] are loaded
 //     by TMA (cp.async.bulk.tensor.3d, swizzle matching the row width, zero fill
 //     past the tensor) into an S-stage ring; completion on mbarriers whose waits
 //     are bounded in time and record a status bit on timeout;
 //   * once per chunk the CTA re-lays B, C out as fp32 [position][state], so a
 //     lane reads four states of one position with one 16-byte broadcast load;
-//   * each lane reads 16-byte blocks of its row (8 bf16 / 4 fp32 positions),
-//     runs the recurrence, adds D u, applies silu(z), rounds, and writes its y
-//     block into a swizzled output tile that one thread stores by TMA.
+//   * y goes through a swizzled output tile that one thread stores by TMA.
 //
 // Discretisation (velog review, section 2 "Discretization"; "mamba 学习",
 // section "MAMBA"): Abar = 2^(s A) with s = dt log2(e) (softplus evaluated in
@@ -58,33 +63,46 @@ struct ScanParams {
 // 2^-22 |B u / A|.
 constexpr float kFastPathMinAbsA = 0.125f;
 
-template <typename IO, int N_, bool GATE_, int S_, int RB_>
+template <typename IO, int N_, bool GATE_, int LPC_, int S_, int RB_>
 struct ChanCfg {
   static constexpr int N = N_;
   static constexpr bool GATE = GATE_;
+  static constexpr int LPC = LPC_;          // lanes per channel
+  static constexpr int NS = N / LPC;        // states per lane
   static constexpr int S = S_;              // pipeline stages
   static constexpr int RB = RB_;            // bytes of one row of a chunk (32, 64 or 128)
   static_assert(RB == 32 || RB == 64 || RB == 128, "row width must be a TMA swizzle span");
-  static_assert(N % 4 == 0, "dstate must be a multiple of 4");
+  static_assert(LPC == 1 || LPC == 2 || LPC == 4, "1, 2 or 4 lanes per channel");
+  static_assert(NS % 4 == 0, "each lane holds a multiple of 4 states");
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
-  static constexpr int DT = THREADS;        // channels per CTA (one per lane)
+  static constexpr int DT = THREADS / LPC;  // channels per CTA
   static constexpr int ESZ = Io<IO>::kBytes;
   static constexpr int TB = 16 / ESZ;       // positions per 16-byte block
+  static constexpr int PB = TB / LPC;       // positions of a block finalised by one lane
+  static_assert(PB >= 1, "a lane finalises at least one position per block");
+  static constexpr int PBYTES = 16 / LPC;   // bytes of those positions
   static constexpr int LC = RB / ESZ;       // positions per chunk
   static constexpr int NBLK = RB / 16;      // 16-byte blocks per row
   static constexpr int NARR = GATE ? 3 : 2; // u, delta (, z)
-  static constexpr int pad1k(int x) { return (x + 1023) / 1024 * 1024; }
-  static constexpr int TILE = pad1k(DT * RB);      // one [DT x LC] swizzled tile
-  static constexpr int BCT = pad1k(N * RB);        // one [N x LC] swizzled tile
+  // tile bases aligned to the swizzle pattern's period (8 rows of RB bytes)
+  static constexpr int ALIGN = 8 * RB;
+  static constexpr int pad(int x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+  static constexpr int TILE = pad(DT * RB);        // one [DT x LC] swizzled tile
+  static constexpr int BCT = pad(N * RB);          // one [N x LC] swizzled tile
   static constexpr int STAGE = NARR * TILE + 2 * BCT;
   static constexpr int OFF_STAGES = 0;
   static constexpr int OFF_Y = OFF_STAGES + S * STAGE;          // 2 output tiles
   static constexpr int BCF = LC * N * 4;                        // fp32 [LC][N]
   static constexpr int OFF_BCF = OFF_Y + 2 * TILE;              // [2 buf][B, C]
-  static constexpr int OFF_BAR = OFF_BCF + 2 * 2 * BCF;
+  // per-warp exchange buffers (LPC > 1): step sizes [32 lanes][PB] and partial
+  // contractions [LPC parts][32 lanes][PB]
+  static constexpr int XCH_S = 32 * PB;                         // floats
+  static constexpr int XCH_WARP = (LPC > 1) ? 4 * (XCH_S + 32 * TB) : 0;
+  static constexpr int OFF_XCH = OFF_BCF + 2 * 2 * BCF;
+  static constexpr int OFF_BAR = OFF_XCH + WARPS * XCH_WARP;
   static constexpr int SMEM = OFF_BAR + S * 8;
-  static constexpr int SMEM_ALLOC = SMEM + 1024;                // for base alignment
+  static constexpr int SMEM_ALLOC = SMEM + ALIGN;               // for base alignment
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
   static constexpr uint32_t TX_BYTES = NARR * DT * RB + 2 * N * RB;
 };
@@ -94,76 +112,196 @@ struct ChanMaps {
 };
 
 // Byte offset of 16-byte granule c of row r in a tile of RB-byte rows written by
-// TMA with the swizzle of span RB (tile base 1024-byte aligned): the granule
+// TMA with the swizzle of span RB (tile base aligned to 8 * RB): the granule
 // index is XOR-ed with address bits 7 and up.
 template <int RB>
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
   return r * RB + ((c ^ (((r * RB) >> 7) & (RB / 16 - 1))) << 4);
 }
 
-template <typename IO, int TB>
-__device__ __forceinline__ void unpack16(const uint4 w, float* out) {
+// widen K io values packed in 32-bit words
+template <typename IO, int K>
+__device__ __forceinline__ void unpack_words(const uint32_t* w, float* out) {
   if constexpr (sizeof(IO) == 2) {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      out[2 * k] = bf16lo(ws[k]);
-      out[2 * k + 1] = bf16hi(ws[k]);
+    for (int k = 0; k < K / 2; ++k) {
+      out[2 * k] = bf16lo(w[k]);
+      out[2 * k + 1] = bf16hi(w[k]);
     }
   } else {
-    out[0] = __uint_as_float(w.x);
-    out[1] = __uint_as_float(w.y);
-    out[2] = __uint_as_float(w.z);
-    out[3] = __uint_as_float(w.w);
+#pragma unroll
+    for (int k = 0; k < K; ++k) out[k] = __uint_as_float(w[k]);
   }
 }
 
-template <typename IO, int TB>
-__device__ __forceinline__ uint4 pack16(const float* v) {
-  if constexpr (sizeof(IO) == 2) {
-    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+// load K consecutive io values (K * size bytes, naturally aligned) from shared memory
+template <typename IO, int K>
+__device__ __forceinline__ void lds_vals(const uint8_t* p, float* out) {
+  constexpr int BYTES = K * sizeof(IO);
+  if constexpr (BYTES == 16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    unpack_words<IO, K>(w, out);
+  } else if constexpr (BYTES == 8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const uint32_t w[2] = {v.x, v.y};
+    unpack_words<IO, K>(w, out);
+  } else if constexpr (BYTES == 4) {
+    const uint32_t w[1] = {*reinterpret_cast<const uint32_t*>(p)};
+    unpack_words<IO, K>(w, out);
   } else {
-    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                      __float_as_uint(v[3]));
+    static_assert(BYTES == 16 || BYTES == 8 || BYTES == 4, "unsupported vector width");
+  }
+}
+
+// round K values to io and store them (K * size bytes) to shared memory
+template <typename IO, int K>
+__device__ __forceinline__ void sts_vals(uint8_t* p, const float* v) {
+  constexpr int BYTES = K * sizeof(IO);
+  uint32_t w[(BYTES + 3) / 4];
+  if constexpr (sizeof(IO) == 2) {
+#pragma unroll
+    for (int k = 0; k < K / 2; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < K; ++k) w[k] = __float_as_uint(v[k]);
+  }
+  if constexpr (BYTES == 16) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if constexpr (BYTES == 8) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+  } else if constexpr (BYTES == 4) {
+    *reinterpret_cast<uint32_t*>(p) = w[0];
+  } else {
+    static_assert(BYTES == 16 || BYTES == 8 || BYTES == 4, "unsupported vector width");
+  }
+}
+
+// K consecutive floats to / from shared memory (K * 4 bytes, naturally aligned)
+template <int K>
+__device__ __forceinline__ void st_floats(float* p, const float* v) {
+  if constexpr (K == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  } else if constexpr (K == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  } else {
+    static_assert(K == 1, "1, 2 or 4 floats");
+    *p = v[0];
+  }
+}
+template <int K>
+__device__ __forceinline__ void ld_floats(const float* p, float* v) {
+  if constexpr (K % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < K; k += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(p + k);
+      v[k] = q.x; v[k + 1] = q.y; v[k + 2] = q.z; v[k + 3] = q.w;
+    }
+  } else if constexpr (K == 2) {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    v[0] = q.x; v[1] = q.y;
+  } else {
+    static_assert(K == 1, "1, 2 or a multiple of 4 floats");
+    v[0] = *p;
+  }
+}
+
+// All-gather over the LPC lanes of a channel through this warp's exchange
+// buffer: lane `part` holds the PB step sizes of positions [part*PB, part*PB+PB);
+// afterwards every lane of the channel holds all TB = LPC*PB in position order.
+template <int LPC, int PB>
+__device__ __forceinline__ void allgather(const float* mine, float* all, float* xs, int lane) {
+  if constexpr (LPC == 1) {
+#pragma unroll
+    for (int k = 0; k < PB; ++k) all[k] = mine[k];
+  } else {
+    st_floats<PB>(xs + lane * PB, mine);
+    __syncwarp();
+    ld_floats<LPC * PB>(xs + (lane & ~(LPC - 1)) * PB, all);
+  }
+}
+
+// Reduce-scatter over the LPC lanes of a channel: every lane holds partial sums
+// for TB positions; afterwards lane `part` holds the full sums of positions
+// [part*PB, part*PB + PB).  Each lane writes its partials split by position part
+// (row p of the buffer holds every lane's partials for part p), then sums the LPC
+// contiguous entries of its channel in row `part`.  The two halves of that read
+// are taken in an order that alternates with the part, so that one 16-byte load
+// of the warp covers every bank group.
+template <int LPC, int TB>
+__device__ __forceinline__ void reduce_scatter(const float* v, float* out, float* xp, int lane,
+                                               int part) {
+  constexpr int PB = TB / LPC;
+  if constexpr (LPC == 1) {
+#pragma unroll
+    for (int k = 0; k < TB; ++k) out[k] = v[k];
+  } else {
+#pragma unroll
+    for (int q = 0; q < LPC; ++q) st_floats<PB>(xp + (q * 32 + lane) * PB, v + q * PB);
+    __syncwarp();
+    const float* row = xp + (part * 32 + (lane & ~(LPC - 1))) * PB;  // TB floats
+    float r[TB];
+    if constexpr (TB == 8) {
+      const int h = (part & 1) * 4;
+      ld_floats<4>(row + h, r);
+      ld_floats<4>(row + (4 - h), r + 4);
+    } else {
+      ld_floats<TB>(row, r);
+    }
+#pragma unroll
+    for (int k = 0; k < PB; ++k) {
+      float acc = r[k];
+#pragma unroll
+      for (int q = 1; q < LPC; ++q) acc += r[q * PB + k];
+      out[k] = acc;
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// one chunk of positions for one lane (its channel's row `row` of the tiles)
+// one chunk of positions for one lane (its channel's row `row` of the tiles,
+// its states part*NS .. part*NS + NS - 1)
 // ---------------------------------------------------------------------------
 template <typename Cfg, typename IO, bool ACC, bool TAIL>
 __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile, const float* bcfB,
-                                           const float* bcfC, int row, int l0, int seqlen,
-                                           const float* Areg, const float* nIA, float Dd,
-                                           float bias2, int softplus, float* h) {
-  constexpr int N = Cfg::N, TB = Cfg::TB, RB = Cfg::RB;
+                                           const float* bcfC, float* xch, int row, int part,
+                                           int lane, int l0, int seqlen, const float* Areg,
+                                           const float* nIA, float Dd, float bias2, int softplus,
+                                           float* h) {
+  constexpr int N = Cfg::N, NS = Cfg::NS, LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB,
+                RB = Cfg::RB;
   const uint8_t* tu = stage;
   const uint8_t* td = stage + Cfg::TILE;
   const uint8_t* tz = stage + 2 * Cfg::TILE;
+  const int pofs = part * Cfg::PBYTES;
 
 #pragma unroll 1
   for (int blk = 0; blk < Cfg::NBLK; ++blk) {
     const uint32_t off = swz<RB>(row, blk);
     float uj[TB], sj[TB];
-    unpack16<IO, TB>(lds128(tu + off), uj);
-    unpack16<IO, TB>(lds128(td + off), sj);
+    lds_vals<IO, TB>(tu + off, uj);
+    // step sizes of this lane's positions, then shared with the channel's lanes
+    {
+      float dm[PB], sm[PB];
+      lds_vals<IO, PB>(td + off + pofs, dm);
 #pragma unroll
-    for (int j = 0; j < TB; ++j) {
-      const float x2 = fmaf(sj[j], kLog2e, bias2);
-      float s = softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
-      if constexpr (TAIL) s = (l0 + blk * TB + j < seqlen) ? s : 0.0f;  // past the end: Abar = 1
-      sj[j] = s;
+      for (int k = 0; k < PB; ++k) {
+        const float x2 = fmaf(dm[k], kLog2e, bias2);
+        float s = softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
+        if constexpr (TAIL) s = (l0 + blk * TB + part * PB + k < seqlen) ? s : 0.0f;  // Abar = 1
+        sm[k] = s;
+      }
+      allgather<LPC, PB>(sm, sj, xch, lane);
     }
-    float yo[TB];
+    float acc[TB];
 #pragma unroll
     for (int j = 0; j < TB; ++j) {
       const int lc = blk * TB + j;  // position within the chunk
-      const float* Bp = bcfB + lc * N;
-      const float* Cp = bcfC + lc * N;
-      f2 acc = mk2(0.0f, 0.0f);
+      const float* Bp = bcfB + lc * N + part * NS;
+      const float* Cp = bcfC + lc * N + part * NS;
+      f2 a2 = mk2(0.0f, 0.0f);
 #pragma unroll
-      for (int m = 0; m < N; m += 4) {
+      for (int m = 0; m < NS; m += 4) {
         const float4 Bv = lds128f(Bp + m);
         const float4 Cv = lds128f(Cp + m);
         const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
@@ -193,18 +331,30 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
               h[i + e] = fmaf(a, h[i + e], coef * (bv[pp + e] * uj[j]));
             }
           }
-          acc = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), acc);
+          a2 = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), a2);
         }
       }
-      yo[j] = fmaf(Dd, uj[j], acc.x + acc.y);
+      acc[j] = a2.x + a2.y;
     }
-    if constexpr (Cfg::GATE) {
-      float zj[TB];
-      unpack16<IO, TB>(lds128(tz + off), zj);
+    // full contraction of this lane's positions, then D skip, gate, rounding
+    float ym[PB];
+    reduce_scatter<LPC, TB>(acc, ym, xch + Cfg::XCH_S, lane, part);
+    float um[PB];
+    if constexpr (LPC == 1) {
 #pragma unroll
-      for (int j = 0; j < TB; ++j) yo[j] *= (ACC ? silu_accurate(zj[j]) : silu_fast(zj[j]));
+      for (int k = 0; k < PB; ++k) um[k] = uj[k];
+    } else {
+      lds_vals<IO, PB>(tu + off + pofs, um);
     }
-    *reinterpret_cast<uint4*>(ytile + off) = pack16<IO, TB>(yo);
+#pragma unroll
+    for (int k = 0; k < PB; ++k) ym[k] = fmaf(Dd, um[k], ym[k]);
+    if constexpr (Cfg::GATE) {
+      float zm[PB];
+      lds_vals<IO, PB>(tz + off + pofs, zm);
+#pragma unroll
+      for (int k = 0; k < PB; ++k) ym[k] *= (ACC ? silu_accurate(zm[k]) : silu_fast(zm[k]));
+    }
+    sts_vals<IO, PB>(ytile + off + pofs, ym);
   }
 }
 
@@ -214,30 +364,35 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 template <typename IO, typename Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS)
     scan_channel_kernel(const __grid_constant__ ChanMaps maps, const ScanParams p) {
-  constexpr int N = Cfg::N, S = Cfg::S, LC = Cfg::LC;
+  constexpr int N = Cfg::N, NS = Cfg::NS, S = Cfg::S, LC = Cfg::LC;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + Cfg::ALIGN - 1) &
+      ~static_cast<uintptr_t>(Cfg::ALIGN - 1));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
 
   const int tid = threadIdx.x;
   const int b = blockIdx.x / p.dtiles;
   const int d0 = (blockIdx.x % p.dtiles) * Cfg::DT;
-  const int row = tid;
+  const int row = tid / Cfg::LPC;
+  const int part = tid % Cfg::LPC;
+  const int lane = tid & 31;
+  float* xch = reinterpret_cast<float*>(smem + Cfg::OFF_XCH + (tid >> 5) * Cfg::XCH_WARP);
   const int d = d0 + row;
   const bool valid = d < p.dim;
   const int nchunks = (p.seqlen + LC - 1) / LC;
 
-  // per-lane parameters and state
-  float Areg[N], nIA[N], h[N];
+  // per-lane parameters and state: states part*NS .. part*NS + NS - 1
+  float Areg[NS], nIA[NS], h[NS];
   bool small_a = false;
+  const int64_t state0 = (static_cast<int64_t>(b) * p.dim + d) * N + part * NS;
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const float a = valid ? __ldg(p.A + static_cast<int64_t>(d) * N + i) : -1.0f;
+  for (int i = 0; i < NS; ++i) {
+    const float a = valid ? __ldg(p.A + static_cast<int64_t>(d) * N + part * NS + i) : -1.0f;
     Areg[i] = a;
     nIA[i] = (a == 0.0f) ? 0.0f : -1.0f / a;
     small_a |= !(fabsf(a) >= kFastPathMinAbsA);
-    h[i] = (valid && p.h0) ? __ldg(p.h0 + (static_cast<int64_t>(b) * p.dim + d) * N + i) : 0.0f;
+    h[i] = (valid && p.h0) ? __ldg(p.h0 + state0 + i) : 0.0f;
   }
   const float Dd = (valid && p.D) ? __ldg(p.D + d) : 0.0f;
   const float bias2 = (valid && p.bias) ? __ldg(p.bias + d) * kLog2e : 0.0f;
@@ -279,7 +434,7 @@ __global__ void __launch_bounds__(Cfg::THREADS)
     const bool arrived = mbar_wait_bounded(&full[s], (k / S) & 1);
     if (!arrived) record_timeout(p.status, 1u);
     // B, C of this chunk: swizzled [N][LC] io -> fp32 [LC][N]
-    {
+    if (arrived) {
       float* bf = reinterpret_cast<float*>(smem + Cfg::OFF_BCF + (k & 1) * 2 * Cfg::BCF);
       const uint8_t* raw = st + Cfg::NARR * Cfg::TILE;
 #pragma unroll 1
@@ -288,7 +443,7 @@ __global__ void __launch_bounds__(Cfg::THREADS)
         const int rem = piece % (N * Cfg::NBLK);
         const int n = rem % N, kb = rem / N;
         float v[Cfg::TB];
-        unpack16<IO, Cfg::TB>(lds128(raw + arr * Cfg::BCT + swz<Cfg::RB>(n, kb)), v);
+        lds_vals<IO, Cfg::TB>(raw + arr * Cfg::BCT + swz<Cfg::RB>(n, kb), v);
         float* dst = bf + arr * (Cfg::BCF / 4) + (kb * Cfg::TB) * N + n;
 #pragma unroll
         for (int e = 0; e < Cfg::TB; ++e) dst[e * N] = v[e];
@@ -316,18 +471,18 @@ __global__ void __launch_bounds__(Cfg::THREADS)
     if constexpr (sizeof(IO) == 2) {
       if (!accurate) {
         if (!tail)
-          chan_chunk<Cfg, IO, false, false>(st, ytile, bcfB, bcfC, row, k * LC, p.seqlen, Areg,
-                                            nIA, Dd, bias2, p.softplus, h);
+          chan_chunk<Cfg, IO, false, false>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen,
+                                            Areg, nIA, Dd, bias2, p.softplus, h);
         else
-          chan_chunk<Cfg, IO, false, true>(st, ytile, bcfB, bcfC, row, k * LC, p.seqlen, Areg,
-                                           nIA, Dd, bias2, p.softplus, h);
+          chan_chunk<Cfg, IO, false, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen,
+                                           Areg, nIA, Dd, bias2, p.softplus, h);
       } else {
-        chan_chunk<Cfg, IO, true, true>(st, ytile, bcfB, bcfC, row, k * LC, p.seqlen, Areg, nIA,
-                                        Dd, bias2, p.softplus, h);
+        chan_chunk<Cfg, IO, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen,
+                                        Areg, nIA, Dd, bias2, p.softplus, h);
       }
     } else {
-      chan_chunk<Cfg, IO, true, true>(st, ytile, bcfB, bcfC, row, k * LC, p.seqlen, Areg, nIA,
-                                      Dd, bias2, p.softplus, h);
+      chan_chunk<Cfg, IO, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen, Areg,
+                                      nIA, Dd, bias2, p.softplus, h);
     }
     fence_proxy_async_smem();  // y tile writes -> visible to the TMA store
   }
@@ -347,8 +502,7 @@ __global__ void __launch_bounds__(Cfg::THREADS)
   }
   if (ok && valid && p.h_last) {
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-      p.h_last[(static_cast<int64_t>(b) * p.dim + d) * N + i] = h[i];
+    for (int i = 0; i < NS; ++i) p.h_last[state0 + i] = h[i];
   }
 }
 

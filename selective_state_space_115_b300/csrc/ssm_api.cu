@@ -173,11 +173,19 @@ ScanParams make_params(const ScanCall& c, void* workspace) {
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-template <typename IO, int N, bool GATE>
+// Channel-kernel shapes: 32-byte chunk rows (16 bf16 / 8 fp32 positions) and a
+// 4-stage ring.  Per 4-warp CTA (bf16, dstate 16, gate): ~66 KB of shared memory
+// and ~107 registers a thread at 1 lane per channel (3 CTAs per SM), ~37 KB and
+// ~80 at 2 (6 per SM), ~22 KB and ~56 at 4 (9 per SM).
+template <int LPC>
+struct ChanShape {
+  static constexpr int S = 4, RB = 32;
+};
+
+template <typename IO, int N, bool GATE, int LPC>
 ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t stream) {
-  // 32-byte chunk rows (16 bf16 / 8 fp32 positions), 4-stage ring: ~69 KB of
-  // shared memory per 128-channel CTA, three CTAs per SM.
-  using Cfg = ChanCfg<IO, N, GATE, 4, 32>;
+  using Shape = ChanShape<LPC>;
+  using Cfg = ChanCfg<IO, N, GATE, LPC, Shape::S, Shape::RB>;
   ChanMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const bool bf = c.bf16;
@@ -193,6 +201,7 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
   }
   ScanParams p = make_params(c, workspace);
   p.dtiles = static_cast<int>((c.dim + Cfg::DT - 1) / Cfg::DT);
+  if (c.batch * p.dtiles > INT32_MAX) return SSM_ERR_INVALID_ARG;
   auto kern = ssm::scan_channel_kernel<IO, Cfg>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::SMEM_ALLOC);
@@ -202,6 +211,52 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "scan_channel launch");
   return SSM_OK;
+}
+
+// SM count of the current device (cached per device ordinal).
+int sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Lanes per channel for the channel kernel.  Every SM sub-partition runs one warp
+// of each resident CTA, so the busiest sub-partition processes kmax = ceil(CTAs /
+// SMs) warps.  Its time is the larger of kmax x the issue cost of one warp (which
+// falls with the states a lane holds, NS = dstate / LPC, but less than in
+// proportion because the per-position work and the lane exchange do not shrink)
+// and the latency of a single warp when there are too few warps to overlap.  The
+// relative costs below were measured on B300 with the 2.8B-like layer (bf16,
+// dstate 16, L 2048): one warp of NS = 16 / 8 / 4 states costs 1 / 0.58 / 0.37
+// when sub-partitions are full, and a lone warp takes 1.78 / 1.6 / 1.2.
+int choose_lpc(int64_t batch, int64_t dim, int64_t dstate) {
+  const int64_t sms = sm_count();
+  int best = 1;
+  double best_cost = 0.0;
+  for (int lpc = 1; lpc <= 4; lpc *= 2) {
+    const int64_t ns = dstate / lpc;
+    if (ns < 4) break;
+    const double w = (ns >= 16) ? 1.0 : (ns >= 8) ? 0.58 : 0.37;
+    const double lone = (ns >= 16) ? 1.78 : (ns >= 8) ? 1.6 : 1.2;
+    const int64_t dt = 128 / lpc;
+    const int64_t ctas = batch * ((dim + dt - 1) / dt);
+    const double kmax = double((ctas + sms - 1) / sms);
+    const double cost = (kmax * w > lone) ? kmax * w : lone;
+    if (lpc == 1 || cost < best_cost) {
+      best = lpc;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 template <typename IO, int N, bool GATE, bool VEC>
@@ -216,12 +271,29 @@ ssm_status launch_chunk(const ScanCall& c, void* workspace, cudaStream_t stream)
   return SSM_OK;
 }
 
+template <typename IO, int N, int LPC>
+ssm_status launch_channel_lpc(const ScanCall& c, void* ws, cudaStream_t s) {
+  if constexpr (N / LPC >= 4) {
+    return c.z ? launch_channel<IO, N, true, LPC>(c, ws, s)
+               : launch_channel<IO, N, false, LPC>(c, ws, s);
+  } else {
+    return SSM_ERR_UNSUPPORTED;
+  }
+}
+
 template <typename IO, int N>
 ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s) {
   const bool gate = c.z != nullptr;
   if (algo == SSM_ALGO_CHANNEL) {
-    return gate ? launch_channel<IO, N, true>(c, ws, s) : launch_channel<IO, N, false>(c, ws, s);
+    switch (choose_lpc(c.batch, c.dim, N)) {
+      case 4: return launch_channel_lpc<IO, N, 4>(c, ws, s);
+      case 2: return launch_channel_lpc<IO, N, 2>(c, ws, s);
+      default: return launch_channel_lpc<IO, N, 1>(c, ws, s);
+    }
   }
+  if (algo == SSM_ALGO_CHANNEL_L1) return launch_channel_lpc<IO, N, 1>(c, ws, s);
+  if (algo == SSM_ALGO_CHANNEL_L2) return launch_channel_lpc<IO, N, 2>(c, ws, s);
+  if (algo == SSM_ALGO_CHANNEL_L4) return launch_channel_lpc<IO, N, 4>(c, ws, s);
   if (vec_eligible(c))
     return gate ? launch_chunk<IO, N, true, true>(c, ws, s) : launch_chunk<IO, N, false, true>(c, ws, s);
   return gate ? launch_chunk<IO, N, true, false>(c, ws, s) : launch_chunk<IO, N, false, false>(c, ws, s);
@@ -326,7 +398,12 @@ ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t
                              const void* B, const void* C, const float* D, const void* z,
                              const float* h0, float* h_last, void* y, void* workspace,
                              size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream) {
-  if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_CHANNEL && algo != SSM_ALGO_CHUNK)
+  if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_CHANNEL && algo != SSM_ALGO_CHUNK &&
+      algo != SSM_ALGO_CHANNEL_L1 && algo != SSM_ALGO_CHANNEL_L2 && algo != SSM_ALGO_CHANNEL_L4)
+    return SSM_ERR_UNSUPPORTED;
+  const bool fixed_split = algo == SSM_ALGO_CHANNEL_L1 || algo == SSM_ALGO_CHANNEL_L2 ||
+                           algo == SSM_ALGO_CHANNEL_L4;
+  if ((algo == SSM_ALGO_CHANNEL_L2 && dstate < 8) || (algo == SSM_ALGO_CHANNEL_L4 && dstate < 16))
     return SSM_ERR_UNSUPPORTED;
   ScanCall c;
   c.batch = batch;
@@ -352,7 +429,7 @@ ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t
 
   if (algo == SSM_ALGO_AUTO)
     algo = (c.batch * c.dim >= kChannelKernelMinChannels) ? SSM_ALGO_CHANNEL : SSM_ALGO_CHUNK;
-  if (algo == SSM_ALGO_CHANNEL && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;
+  if ((algo == SSM_ALGO_CHANNEL || fixed_split) && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(ssm::DeviceStatus), s);

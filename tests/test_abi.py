@@ -83,6 +83,13 @@ def scan(lib, batch=2, dim=8, dstate=16, seqlen=64, io=1, u=P, delta=P, bias=Non
     (dict(h0=P + 1), binding.SSM_ERR_INVALID_ARG),
     (dict(batch=1 << 40, dim=1 << 20), binding.SSM_ERR_INVALID_ARG),
     (dict(algo=9), binding.SSM_ERR_UNSUPPORTED),
+    (dict(algo=-1), binding.SSM_ERR_UNSUPPORTED),
+    # a fixed lanes-per-channel split must leave every lane at least 4 states
+    (dict(algo=binding.ALGO_CHANNEL_L2, dstate=4), binding.SSM_ERR_UNSUPPORTED),
+    (dict(algo=binding.ALGO_CHANNEL_L4, dstate=8), binding.SSM_ERR_UNSUPPORTED),
+    (dict(algo=binding.ALGO_CHANNEL_L4, dstate=4), binding.SSM_ERR_UNSUPPORTED),
+    # validation still runs first for the fixed splits
+    (dict(algo=binding.ALGO_CHANNEL_L4, u=None), binding.SSM_ERR_INVALID_ARG),
 ])
 def test_scan_validation(kw, expect):
     lib = binding.library()

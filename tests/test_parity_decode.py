@@ -113,7 +113,7 @@ def test_decode_unaligned_state_falls_back():
 
 
 @pytest.mark.parametrize("io", [W.F32, W.BF16])
-@pytest.mark.parametrize("algo", ["channel", "chunk"])
+@pytest.mark.parametrize("algo", ["channel", "channel_l1", "channel_l2", "chunk"])
 def test_steps_equal_scan(io, algo):
     """L decode steps reproduce one scan over L (both on the GPU)."""
     import torch

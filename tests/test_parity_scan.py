@@ -1,7 +1,9 @@
 """GPU parity of the selective-scan forward (through the C ABI) against the fp64 oracle.
 
 Tolerances (error metric in tests/helpers.py): 1e-4 for fp32 io, 2e-2 for bf16 io
-with fp32 state.  Every configuration runs both kernel families.
+with fp32 state.  Every configuration runs both kernel families, the channel
+kernel at each of its lanes-per-channel splits (1, 2, 4 lanes; a split that would
+leave a lane fewer than 4 states is skipped).
 """
 import os
 
@@ -13,8 +15,18 @@ from selective_state_space_115_b300 import workloads as W
 from tests.helpers import TOL, from_torch, rel_err, sample_rows, torch_f32, torch_io
 
 pytestmark = pytest.mark.gpu
-ALGOS = ["channel", "chunk"]
+ALGOS = ["channel_l1", "channel_l2", "channel_l4", "chunk"]
+MIN_DSTATE = {"channel_l2": 8, "channel_l4": 16}
 NTHREADS = os.cpu_count() or 1
+_ORACLE_CACHE = {}
+_INPUT_CACHE = {}
+
+
+def workload_inputs(name):
+    """Seeded inputs of a named workload, drawn once per test session."""
+    if name not in _INPUT_CACHE:
+        _INPUT_CACHE[name] = W.make_scan_inputs(W.SCAN_CONFIGS[name], seed=0)
+    return _INPUT_CACHE[name]
 
 
 def S():
@@ -24,6 +36,8 @@ def S():
 
 def gpu_scan(x, io, algo, softplus=True, return_last_state=False, out=None):
     import torch
+    if x["A"].shape[1] < MIN_DSTATE.get(algo, 0):
+        pytest.skip(f"{algo} needs dstate >= {MIN_DSTATE[algo]}")
     r = S().scan_fwd(torch_io(x["u"], io), torch_io(x["delta"], io), torch_f32(x["A"]),
                      torch_io(x["B"], io), torch_io(x["C"], io), D=torch_f32(x.get("D")),
                      z=torch_io(x.get("z"), io), delta_bias=torch_f32(x.get("delta_bias")),
@@ -38,7 +52,13 @@ def f64(x, io):
     return None if x is None else W.to_f64(x, io)
 
 
-def oracle_full(x, io, softplus=True, return_last_state=False):
+def oracle_full(x, io, softplus=True, return_last_state=False, cache_key=None):
+    """The fp64 oracle on all rows (memoised per `cache_key` when given)."""
+    if cache_key is not None:
+        key = (cache_key, softplus, return_last_state)
+        if key not in _ORACLE_CACHE:
+            _ORACLE_CACHE[key] = oracle_full(x, io, softplus, return_last_state)
+        return _ORACLE_CACHE[key]
     return oracle.scan_fwd(f64(x["u"], io), f64(x["delta"], io), x["A"], f64(x["B"], io),
                            f64(x["C"], io), D=x.get("D"), z=f64(x.get("z"), io),
                            delta_bias=x.get("delta_bias"), delta_softplus=softplus,
@@ -71,9 +91,9 @@ def test_tiny(algo):
 @pytest.mark.parametrize("algo", ALGOS)
 def test_130m_full(algo):
     cfg = W.SCAN_CONFIGS["130m"]
-    x = W.make_scan_inputs(cfg, seed=0)
+    x = workload_inputs("130m")
     y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
-    ref, hr = oracle_full(x, cfg.io, return_last_state=True)
+    ref, hr = oracle_full(x, cfg.io, return_last_state=True, cache_key="130m")
     e = rel_err(from_torch(y), ref)
     print(f"130m {algo}: max rel err {e:.3e}")
     assert e <= TOL[cfg.io]
@@ -83,7 +103,7 @@ def test_130m_full(algo):
 @pytest.mark.parametrize("algo", ALGOS)
 def test_2p8b_sampled(algo):
     cfg = W.SCAN_CONFIGS["2p8b"]
-    x = W.make_scan_inputs(cfg, seed=0)
+    x = workload_inputs("2p8b")
     y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
     yg = from_torch(y).reshape(cfg.batch * cfg.dim, cfg.seqlen)
     assert np.isfinite(yg).all()
@@ -98,7 +118,7 @@ def test_2p8b_sampled(algo):
 @pytest.mark.parametrize("algo", ALGOS)
 def test_long_sampled(algo):
     cfg = W.SCAN_CONFIGS["long"]
-    x = W.make_scan_inputs(cfg, seed=0)
+    x = workload_inputs("long")
     y, hl = gpu_scan(x, cfg.io, algo, return_last_state=True)
     yg = from_torch(y).reshape(cfg.batch * cfg.dim, cfg.seqlen)
     assert np.isfinite(yg).all()
