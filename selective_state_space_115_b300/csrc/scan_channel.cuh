@@ -325,7 +325,7 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
               const float q = sj[j] * A0;
               const float ahw = ex2(q);
               const float em1 = exp2m1_accurate(q, ahw);
-              const float a = (fabsf(q) < 0.36f) ? 1.0f + em1 : ahw;
+              const float a = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
               // (Abar - 1) / A, or dt at A == 0
               const float coef = (A0 == 0.0f) ? sj[j] * kLn2 : em1 * -nIA[i + e];
               h[i + e] = fmaf(a, h[i + e], coef * (bv[pp + e] * uj[j]));

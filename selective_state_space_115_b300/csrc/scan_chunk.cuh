@@ -148,7 +148,7 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
           bb[i] = fmaf(-ahw, nK, nK);        // (Abar - 1) B u / A
         } else {
           const float em1 = exp2m1_accurate(q, ahw);
-          a[i] = (fabsf(q) < 0.36f) ? 1.0f + em1 : ahw;
+          a[i] = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
           const float coef = fmaf(isZn, s[i] * kLn2, em1 * IAn);
           bb[i] = coef * X;
         }

@@ -312,8 +312,7 @@ ssm_status dispatch_scan(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_
 template <typename IO, int N, bool GATE, bool VEC>
 ssm_status launch_update(const UpdateParams& p, cudaStream_t stream) {
   using Cfg = UpdCfg<IO, N, GATE, VEC>;
-  const int64_t threads = p.channels * Cfg::G;
-  const int64_t grid = (threads + Cfg::THREADS - 1) / Cfg::THREADS;
+  const int64_t grid = (p.channels + Cfg::THREADS - 1) / Cfg::THREADS;  // one lane per channel
   if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;
   ssm::state_update_kernel<IO, Cfg><<<static_cast<unsigned>(grid), Cfg::THREADS, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();

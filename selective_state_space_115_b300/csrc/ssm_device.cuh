@@ -132,21 +132,20 @@ struct Io<uint16_t> {
 // ---------------------------------------------------------------------------
 // exact-ish pieces for the fp32 (accurate) path
 // ---------------------------------------------------------------------------
-// 2^q - 1 without cancellation: Taylor series of e^x - 1 (x = q ln 2) for
-// |q| < 0.36 (truncation below 5e-8 relative); hardware ex2 minus one beyond,
-// where |2^q - 1| >= 0.22 so the subtraction loses nothing.
+// 2^q - 1 without cancellation: Taylor series of e^x - 1 (x = q ln 2) to degree
+// 4 for |q| < 1/8 (truncation below 4e-8 relative); hardware ex2 minus one
+// beyond, where |2^q - 1| >= 0.083 keeps the subtraction's relative error below
+// 3e-6.
+constexpr float kExpm1SeriesMaxQ = 0.125f;
 __device__ __forceinline__ float exp2m1_accurate(float q, float a /* = ex2(q) */) {
-  // coefficients ln2^k / k!, k = 1..6
+  // coefficients ln2^k / k!, k = 1..4
   const float c1 = 0.69314718055994531f, c2 = 0.24022650695910071f,
-              c3 = 0.05550410866482158f, c4 = 0.00961812910762848f,
-              c5 = 0.00133335581464284f, c6 = 0.00015403530393381f;
-  float p = fmaf(c6, q, c5);
-  p = fmaf(p, q, c4);
-  p = fmaf(p, q, c3);
+              c3 = 0.05550410866482158f, c4 = 0.00961812910762848f;
+  float p = fmaf(c4, q, c3);
   p = fmaf(p, q, c2);
   p = fmaf(p, q, c1);
   p = p * q;
-  return (fabsf(q) < 0.36f) ? p : (a - 1.0f);
+  return (fabsf(q) < kExpm1SeriesMaxQ) ? p : (a - 1.0f);
 }
 
 // softplus in log2 units: returns log2(1 + 2^x2) (= softplus(x) * log2 e for x2 = x log2 e)
@@ -249,6 +248,28 @@ __device__ __forceinline__ void tma_store_wait_read() {
 template <int N>
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Ampere-style asynchronous 16-byte copy global -> shared (L2 only), and its
+// group commit / wait (a hardware wait, not a spin loop)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(__cvta_generic_to_global(gmem_src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// bulk (TMA, untiled) copy shared -> global of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), tracked by the bulk async-group of this thread
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   __cvta_generic_to_global(gmem_dst)),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
 }
 
 // 16-byte vector shared loads/stores

@@ -4,11 +4,13 @@
 // (Mamba_Model_Report.md, section 6: ssm_step h = deltaA * h + BX,
 // y = h C + D x; here with the zero-order-hold input term of the velog review,
 // section 2 "Discretization").  The step moves the fp32 state twice (read and
-// write, 2 * 4 * N bytes per channel) against a few bytes of token inputs, so
-// it is bound by HBM: four lanes share a channel's 16 states as one 16-byte
-// vector each, a warp reads 512 contiguous bytes of h, and the contraction is
-// summed with two xor-shuffles.  The arithmetic uses the accurate ZOH form
-// (expm1 series near zero) since it costs nothing at this arithmetic intensity.
+// write, 2 * 4 * N bytes per channel) against a few bytes of token inputs, so it
+// is bound by memory.  One lane owns one channel and all N of its states and
+// evaluates the per-channel scalars (softplus, D skip, gate) once; each warp
+// moves its 32 channels' states (32 * 4 * N contiguous bytes) between global and
+// shared memory with coalesced asynchronous copies in and one bulk (TMA) copy
+// out.  The arithmetic uses the accurate ZOH form (expm1 series near zero),
+// which costs little at this arithmetic intensity.
 #pragma once
 
 #include "ssm_device.cuh"
@@ -34,92 +36,147 @@ struct UpdateParams {
 template <typename IO, int N_, bool GATE_, bool VEC_>
 struct UpdCfg {
   static constexpr int N = N_;
-  static constexpr int NS = 4;            // states per lane
-  static constexpr int G = N / NS;        // lanes per channel
   static constexpr bool GATE = GATE_;
-  static constexpr bool VEC = VEC_;
+  static constexpr bool VEC = VEC_;  // h, A 16-byte aligned; B, C rows 4-element aligned
   static constexpr int THREADS = 256;
 };
 
-template <typename IO, typename Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS) state_update_kernel(const UpdateParams p) {
-  constexpr int N = Cfg::N, NS = Cfg::NS, G = Cfg::G;
-  const int64_t gt = static_cast<int64_t>(blockIdx.x) * Cfg::THREADS + threadIdx.x;
-  const int64_t ch = gt / G;
-  const int g = static_cast<int>(gt % G);
-  const bool valid = ch < p.channels;
-  const int64_t chc = valid ? ch : 0;  // clamped for address arithmetic only
-  const int64_t b = chc / p.dim;
-  const int d = static_cast<int>(chc % p.dim);
-
-  float hv[NS], Av[NS], Bv[NS], Cv[NS];
-  float* hp = p.h + chc * N + g * NS;
-  const float* Ap = p.A + static_cast<int64_t>(d) * N + g * NS;
-  const IO* Bp = static_cast<const IO*>(p.B) + b * N + g * NS;
-  const IO* Cp = static_cast<const IO*>(p.C) + b * N + g * NS;
-  float uv = 0.f, dv = 0.f, zv = 0.f;
-  if (valid) {
-    if constexpr (Cfg::VEC) {
-      const float4 h4 = *reinterpret_cast<const float4*>(hp);
-      const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ap));
-      hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
-      Av[0] = a4.x; Av[1] = a4.y; Av[2] = a4.z; Av[3] = a4.w;
-      if constexpr (sizeof(IO) == 2) {
-        const uint2 bw = __ldg(reinterpret_cast<const uint2*>(Bp));
-        const uint2 cw = __ldg(reinterpret_cast<const uint2*>(Cp));
-        Bv[0] = bf16lo(bw.x); Bv[1] = bf16hi(bw.x); Bv[2] = bf16lo(bw.y); Bv[3] = bf16hi(bw.y);
-        Cv[0] = bf16lo(cw.x); Cv[1] = bf16hi(cw.x); Cv[2] = bf16lo(cw.y); Cv[3] = bf16hi(cw.y);
-      } else {
-        const float4 bw = __ldg(reinterpret_cast<const float4*>(Bp));
-        const float4 cw = __ldg(reinterpret_cast<const float4*>(Cp));
-        Bv[0] = bw.x; Bv[1] = bw.y; Bv[2] = bw.z; Bv[3] = bw.w;
-        Cv[0] = cw.x; Cv[1] = cw.y; Cv[2] = cw.z; Cv[3] = cw.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < NS; ++i) {
-        hv[i] = hp[i];
-        Av[i] = __ldg(Ap + i);
-        Bv[i] = Io<IO>::ldg(Bp + i);
-        Cv[i] = Io<IO>::ldg(Cp + i);
-      }
-    }
-    uv = Io<IO>::ldg(static_cast<const IO*>(p.u) + chc);
-    dv = Io<IO>::ldg(static_cast<const IO*>(p.delta) + chc);
-    if constexpr (Cfg::GATE) zv = Io<IO>::ldg(static_cast<const IO*>(p.z) + chc);
+// 4 io values of a B or C row into fp32 registers
+template <typename IO, bool VEC>
+__device__ __forceinline__ void load4(const IO* p, float* out) {
+  if constexpr (VEC && sizeof(IO) == 2) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+    out[0] = bf16lo(w.x);
+    out[1] = bf16hi(w.x);
+    out[2] = bf16lo(w.y);
+    out[3] = bf16hi(w.y);
+  } else if constexpr (VEC) {
+    const float4 w = __ldg(reinterpret_cast<const float4*>(p));
+    out[0] = w.x;
+    out[1] = w.y;
+    out[2] = w.z;
+    out[3] = w.w;
   } else {
 #pragma unroll
-    for (int i = 0; i < NS; ++i) { hv[i] = 0.f; Av[i] = -1.f; Bv[i] = 0.f; Cv[i] = 0.f; }
+    for (int k = 0; k < 4; ++k) out[k] = Io<IO>::ldg(p + k);
   }
-  const float x2 = fmaf(dv, kLog2e, p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f);
-  const float s = p.softplus ? softplus_log2_accurate(x2) : x2;  // dt * log2(e)
-  float acc = 0.f;
+}
+
+// One channel's step for the lane that owns it.  `hs` points at the channel's N
+// states (in shared memory when staged, else in global memory); granule k of the
+// lane's registers holds states 4*((k + rot) % G) .. +3, so lanes that start
+// at different granules spread their 16-byte accesses over all bank groups.
+template <typename IO, typename Cfg>
+__device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t ch, float* hs,
+                                               int rot) {
+  constexpr int N = Cfg::N, G = N / 4;
+  const int64_t b = ch / p.dim;
+  const int d = static_cast<int>(ch % p.dim);
+  const float* __restrict__ Ap = p.A + static_cast<int64_t>(d) * N;
+  const IO* __restrict__ Bp = static_cast<const IO*>(p.B) + b * N;
+  const IO* __restrict__ Cp = static_cast<const IO*>(p.C) + b * N;
+
+  float hv[N], Av[N];
 #pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    const float a0 = Av[i];
-    const float q = s * a0;
-    const float ahw = ex2(q);
-    const float em1 = exp2m1_accurate(q, ahw);
-    const float abar = (fabsf(q) < 0.36f) ? 1.0f + em1 : ahw;
-    const float coef = (a0 == 0.0f) ? s * kLn2 : em1 / a0;
-    hv[i] = fmaf(abar, hv[i], coef * (Bv[i] * uv));
-    acc = fmaf(Cv[i], hv[i], acc);
-  }
-#pragma unroll
-  for (int o = G / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (valid) {
+  for (int k = 0; k < G; ++k) {
+    const int g = ((k + rot) & (G - 1)) * 4;
     if constexpr (Cfg::VEC) {
-      *reinterpret_cast<float4*>(hp) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+      const float4 h4 = *reinterpret_cast<const float4*>(hs + g);
+      const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ap + g));
+      hv[4 * k] = h4.x; hv[4 * k + 1] = h4.y; hv[4 * k + 2] = h4.z; hv[4 * k + 3] = h4.w;
+      Av[4 * k] = a4.x; Av[4 * k + 1] = a4.y; Av[4 * k + 2] = a4.z; Av[4 * k + 3] = a4.w;
     } else {
 #pragma unroll
-      for (int i = 0; i < NS; ++i) hp[i] = hv[i];
-    }
-    if (g == 0) {
-      float yv = fmaf(p.D ? __ldg(p.D + d) : 0.0f, uv, acc);
-      if constexpr (Cfg::GATE) yv *= silu_accurate(zv);
-      Io<IO>::store(static_cast<IO*>(p.y) + chc, yv);
+      for (int i = 0; i < 4; ++i) {
+        hv[4 * k + i] = hs[g + i];
+        Av[4 * k + i] = __ldg(Ap + g + i);
+      }
     }
   }
+  const float uv = Io<IO>::ldg(static_cast<const IO*>(p.u) + ch);
+  const float dv = Io<IO>::ldg(static_cast<const IO*>(p.delta) + ch);
+  const float zv = Cfg::GATE ? Io<IO>::ldg(static_cast<const IO*>(p.z) + ch) : 0.0f;
+  const float x2 = fmaf(dv, kLog2e, p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f);
+  const float s = p.softplus ? softplus_log2_accurate(x2) : x2;  // dt * log2(e)
+
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int g = ((k + rot) & (G - 1)) * 4;
+    float Bv[4], Cv[4];
+    load4<IO, Cfg::VEC>(Bp + g, Bv);
+    load4<IO, Cfg::VEC>(Cp + g, Cv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a0 = Av[4 * k + i];
+      const float q = s * a0;
+      const float ahw = ex2(q);
+      const float em1 = exp2m1_accurate(q, ahw);
+      const float abar = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
+      // (Abar - 1) / A, or dt at A == 0; 1/A from the hardware reciprocal (a few
+      // ulp, far below the series' truncation)
+      const float coef = (a0 == 0.0f) ? s * kLn2 : em1 * rcp(a0);
+      const float hn = fmaf(abar, hv[4 * k + i], coef * (Bv[i] * uv));
+      hv[4 * k + i] = hn;
+      if (i & 1)
+        acc1 = fmaf(Cv[i], hn, acc1);
+      else
+        acc0 = fmaf(Cv[i], hn, acc0);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int g = ((k + rot) & (G - 1)) * 4;
+    if constexpr (Cfg::VEC) {
+      *reinterpret_cast<float4*>(hs + g) =
+          make_float4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hs[g + i] = hv[4 * k + i];
+    }
+  }
+  float yv = fmaf(p.D ? __ldg(p.D + d) : 0.0f, uv, acc0 + acc1);
+  // the gate only scales y, which a bf16 output rounds to 2^-9 anyway: hardware
+  // ex2 / rcp suffice there; fp32 outputs take the library expf and division
+  if constexpr (Cfg::GATE) yv *= (sizeof(IO) == 2) ? silu_fast(zv) : silu_accurate(zv);
+  Io<IO>::store(static_cast<IO*>(p.y) + ch, yv);
+}
+
+// Aligned path (VEC): each warp stages its 32 channels' states (32 * 4 * N
+// contiguous bytes) through shared memory: coalesced 16-byte asynchronous copies
+// in, one lane per channel for the arithmetic, one bulk (TMA) store out.  A warp
+// whose 32 channels run past the end, and the unaligned path, read and write h
+// directly.
+template <typename IO, typename Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 4) state_update_kernel(const UpdateParams p) {
+  constexpr int N = Cfg::N, G = N / 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t ch0 = static_cast<int64_t>(blockIdx.x) * Cfg::THREADS + warp * 32;
+  const int64_t ch = ch0 + lane;
+  if constexpr (Cfg::VEC) {
+    __shared__ __align__(16) float stage[Cfg::THREADS / 32][32 * N];
+    float* ws = stage[warp];
+    if (ch0 + 32 <= p.channels) {
+      const float* src = p.h + ch0 * N;
+#pragma unroll
+      for (int k = 0; k < G; ++k) cp_async16(ws + (k * 32 + lane) * 4, src + (k * 32 + lane) * 4);
+      cp_async_commit();
+      cp_async_wait_all();
+      __syncwarp();
+      // start granule per lane: 8 consecutive lanes cover all 8 bank groups
+      const int rot = (lane >> (G == 4 ? 1 : G == 2 ? 2 : 3)) & (G - 1);
+      update_channel<IO, Cfg>(p, ch, ws + lane * N, rot);
+      fence_proxy_async_smem();  // the lanes' stores -> visible to the bulk copy
+      __syncwarp();
+      if (lane == 0) {
+        bulk_store(p.h + ch0 * N, ws, 32 * N * 4);
+        tma_store_commit();
+        tma_store_wait_read<0>();  // the copy has read the staging buffer
+      }
+      return;
+    }
+  }
+  if (ch < p.channels) update_channel<IO, Cfg>(p, ch, p.h + ch * N, 0);
 }
 
 }  // namespace ssm
