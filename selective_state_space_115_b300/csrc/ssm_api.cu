@@ -310,13 +310,21 @@ ssm_status dispatch_scan(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_
 }
 
 template <typename IO, int N, bool GATE, bool VEC>
-ssm_status launch_update(const UpdateParams& p, cudaStream_t stream) {
+ssm_status launch_update(const UpdateParams& p0, cudaStream_t stream) {
   using Cfg = UpdCfg<IO, N, GATE, VEC>;
-  const int64_t grid = (p.channels + Cfg::THREADS - 1) / Cfg::THREADS;  // one lane per channel
-  if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;
-  ssm::state_update_kernel<IO, Cfg><<<static_cast<unsigned>(grid), Cfg::THREADS, 0, stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "state_update launch");
+  // one lane per channel: x over blocks of a batch row, y over up to 65535 batch rows
+  // per launch
+  constexpr int64_t kRowsPerLaunch = 65535;
+  UpdateParams p = p0;
+  for (int64_t b0 = 0; b0 < p0.batch; b0 += kRowsPerLaunch) {
+    p.b0 = b0;
+    const int64_t rows = (p0.batch - b0 < kRowsPerLaunch) ? p0.batch - b0 : kRowsPerLaunch;
+    const dim3 grid(static_cast<unsigned>((p.dim + Cfg::THREADS - 1) / Cfg::THREADS),
+                    static_cast<unsigned>(rows));
+    ssm::state_update_kernel<IO, Cfg><<<grid, Cfg::THREADS, 0, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "state_update launch");
+  }
   return SSM_OK;
 }
 
@@ -483,7 +491,8 @@ ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, ssm_dtyp
   for (const float* q : f_ptrs)
     if (q && !aligned(q, 4)) return SSM_ERR_INVALID_ARG;
   UpdateParams p;
-  p.channels = batch * dim;
+  p.batch = batch;
+  p.b0 = 0;
   p.dim = static_cast<int>(dim);
   p.softplus = delta_softplus ? 1 : 0;
   p.h = h;

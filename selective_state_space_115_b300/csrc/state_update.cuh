@@ -18,7 +18,8 @@
 namespace ssm {
 
 struct UpdateParams {
-  int64_t channels;  // batch * dim
+  int64_t batch;
+  int64_t b0;        // first batch row of this launch
   int dim;
   int softplus;
   float* h;          // [batch, dim, N]
@@ -67,11 +68,10 @@ __device__ __forceinline__ void load4(const IO* p, float* out) {
 // lane's registers holds states 4*((k + rot) % G) .. +3, so lanes that start
 // at different granules spread their 16-byte accesses over all bank groups.
 template <typename IO, typename Cfg>
-__device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t ch, float* hs,
+__device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b, int d, float* hs,
                                                int rot) {
   constexpr int N = Cfg::N, G = N / 4;
-  const int64_t b = ch / p.dim;
-  const int d = static_cast<int>(ch % p.dim);
+  const int64_t ch = b * p.dim + d;
   const float* __restrict__ Ap = p.A + static_cast<int64_t>(d) * N;
   const IO* __restrict__ Bp = static_cast<const IO*>(p.B) + b * N;
   const IO* __restrict__ Cp = static_cast<const IO*>(p.C) + b * N;
@@ -145,38 +145,40 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t ch
 // Aligned path (VEC): each warp stages its 32 channels' states (32 * 4 * N
 // contiguous bytes) through shared memory: coalesced 16-byte asynchronous copies
 // in, one lane per channel for the arithmetic, one bulk (TMA) store out.  A warp
-// whose 32 channels run past the end, and the unaligned path, read and write h
-// directly.
+// whose 32 channels run past the end of the row, and the unaligned path, read and
+// write h directly.
 template <typename IO, typename Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 4) state_update_kernel(const UpdateParams p) {
   constexpr int N = Cfg::N, G = N / 4;
+  // grid: x over channel blocks of one batch row, y over batch rows b0 + y
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t ch0 = static_cast<int64_t>(blockIdx.x) * Cfg::THREADS + warp * 32;
-  const int64_t ch = ch0 + lane;
+  const int64_t b = p.b0 + blockIdx.y;
+  const int d0 = blockIdx.x * Cfg::THREADS + warp * 32;
+  const int d = d0 + lane;
   if constexpr (Cfg::VEC) {
     __shared__ __align__(16) float stage[Cfg::THREADS / 32][32 * N];
     float* ws = stage[warp];
-    if (ch0 + 32 <= p.channels) {
-      const float* src = p.h + ch0 * N;
+    if (d0 + 32 <= p.dim) {
+      float* hrow = p.h + (b * p.dim + d0) * N;
 #pragma unroll
-      for (int k = 0; k < G; ++k) cp_async16(ws + (k * 32 + lane) * 4, src + (k * 32 + lane) * 4);
+      for (int k = 0; k < G; ++k) cp_async16(ws + (k * 32 + lane) * 4, hrow + (k * 32 + lane) * 4);
       cp_async_commit();
       cp_async_wait_all();
       __syncwarp();
       // start granule per lane: 8 consecutive lanes cover all 8 bank groups
       const int rot = (lane >> (G == 4 ? 1 : G == 2 ? 2 : 3)) & (G - 1);
-      update_channel<IO, Cfg>(p, ch, ws + lane * N, rot);
+      update_channel<IO, Cfg>(p, b, d, ws + lane * N, rot);
       fence_proxy_async_smem();  // the lanes' stores -> visible to the bulk copy
       __syncwarp();
       if (lane == 0) {
-        bulk_store(p.h + ch0 * N, ws, 32 * N * 4);
+        bulk_store(hrow, ws, 32 * N * 4);
         tma_store_commit();
         tma_store_wait_read<0>();  // the copy has read the staging buffer
       }
       return;
     }
   }
-  if (ch < p.channels) update_channel<IO, Cfg>(p, ch, p.h + ch * N, 0);
+  if (d < p.dim) update_channel<IO, Cfg>(p, b, d, p.h + (b * p.dim + d) * N, 0);
 }
 
 }  // namespace ssm
