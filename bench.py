@@ -19,7 +19,6 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
-import glob
 import hashlib
 import json
 import os
@@ -71,10 +70,18 @@ def decode_bytes(cfg) -> int:
         2 * s * cfg.batch * cfg.dstate + 4 * (cfg.dim * cfg.dstate + 2 * cfg.dim)
 
 
-def source_sha() -> str:
+# device sources each profiled kernel is compiled from
+KERNEL_SOURCES = {
+    "scan_channel_2p8b": ("scan_channel.cuh", "ssm_device.cuh"),
+    "state_update_decode": ("state_update.cuh", "ssm_device.cuh"),
+}
+
+
+def source_sha(kernel: str) -> str:
+    """Short hash of the device sources of a profiled kernel."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_115_b300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "selective_state_space_115_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -92,7 +99,7 @@ def profiled_traffic(kernel: str):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256") != source_sha():
+    if vals.get("source_sha256") != source_sha(kernel):
         return None
     try:
         return float(vals["traffic_bytes_per_launch"])
@@ -385,7 +392,8 @@ def run_gpu(args):
                     "bytes_per_step": bytes_step, "peak_kind": peak_kind},
             "roofline": {"bound": "alu", "achieved": achieved_exp, "peak": ex2_peak,
                          "unit": "Texp/s", "frac": achieved_exp / ex2_peak, "traffic": traffic,
-                         "kernel": "scan_channel_kernel<bf16, N=16, gate> (one lane per channel)",
+                         "kernel": "scan_channel_kernel<bf16, N=16, gate> (lanes-per-channel "
+                                   "split chosen by the library: 2 at this size)",
                          "units_per_launch": CFG.updates,
                          "peak_note": "148 SMs x 32 ex2/clk/SM (measured ex2.approx.f32 "
                                       "throughput) x 2032 MHz max SM clock"},
