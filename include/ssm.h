@@ -90,12 +90,22 @@ typedef enum {
                                  across chunks */
     SSM_ALGO_CHANNEL_L1 = 3,  /* CHANNEL with a fixed split: 1 lane per channel */
     SSM_ALGO_CHANNEL_L2 = 4,  /* 2 lanes per channel (dstate 8 or 16) */
-    SSM_ALGO_CHANNEL_L4 = 5   /* 4 lanes per channel (dstate 16) */
+    SSM_ALGO_CHANNEL_L4 = 5,  /* 4 lanes per channel (dstate 16) */
+    SSM_ALGO_SEGMENTED = 6    /* long sequences over few channels: the sequence is split
+                                 into segments run by separate CTAs (one lane per
+                                 channel) in two passes -- each segment's end state from
+                                 a zero state, then every segment again from the state
+                                 rebuilt from the earlier segments.  Needs the workspace
+                                 that ssm_scan_fwd_workspace_size() reports; sequences
+                                 too short to split run as CHANNEL_L1 */
 } ssm_algo;
 
 /*
- * Size in bytes of the device workspace ssm_scan_fwd needs for these sizes
- * (a 16-byte-aligned block holding the device status words; at least 256).
+ * Size in bytes of the device workspace ssm_scan_fwd needs for these sizes on
+ * the current device: 256 bytes of device status words, plus, when the sequence
+ * is long and the channels few (the segmented plan), each segment's fp32 end
+ * state and step-size sum.  A smaller workspace (at least 256 bytes) is accepted
+ * by SSM_ALGO_AUTO, which then runs a plan that fits it.
  */
 SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
 
@@ -156,9 +166,9 @@ SSM_API ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate,
  *    (cudaGetSymbolAddress) with the caller's current device, which must be the
  *    device of the tensors and of `stream`; make that first call before any
  *    stream capture.
- *  - Sizes whose scratch requirement (ssm_scan_fwd_workspace_size) exceeds the
- *    reserved 4096 bytes are rejected with SSM_ERR_UNSUPPORTED and a message in
- *    ssm_last_cuda_error(); nothing is enqueued then.
+ *  - The kernel is chosen as by SSM_ALGO_AUTO among the plans whose scratch fits
+ *    the reserved 4096 bytes (the segmented long-sequence plan does not, so long
+ *    sequences over few channels take the lanes-over-positions kernel here).
  *  - Every call shares the one array per device and it keeps the last call's
  *    contents; its status words are cleared on `stream` before each kernel.
  *    Calls that overlap on the GPU (different streams, no ordering) race on it.

@@ -32,9 +32,10 @@ ALGO_CHUNK = 2
 ALGO_CHANNEL_L1 = 3
 ALGO_CHANNEL_L2 = 4
 ALGO_CHANNEL_L4 = 5
+ALGO_SEGMENTED = 6
 _ALGOS = {"auto": ALGO_AUTO, "channel": ALGO_CHANNEL, "chunk": ALGO_CHUNK,
           "channel_l1": ALGO_CHANNEL_L1, "channel_l2": ALGO_CHANNEL_L2,
-          "channel_l4": ALGO_CHANNEL_L4}
+          "channel_l4": ALGO_CHANNEL_L4, "segmented": ALGO_SEGMENTED}
 _ALGOS.update({v: v for v in list(_ALGOS.values())})
 
 # every symbol include/ssm.h declares
@@ -151,10 +152,13 @@ def scan_fwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> i
 
 
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    key = (device.index, nbytes)
+    """The scan workspace of a device: one buffer per device, grown to the largest
+    size asked for so far, so that its status words are the ones the last scan on
+    that device wrote (zero-filled when allocated)."""
+    key = device.index
     ws = _ws_cache.get(key)
-    if ws is None:
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _ws_cache[key] = ws
     return ws
 
@@ -204,8 +208,7 @@ def read_device_status(workspace: Optional[torch.Tensor] = None, device=None) ->
     """Synchronise the current stream and return the status recorded in a scan workspace."""
     if workspace is None:
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-        nbytes = int(library().ssm_scan_fwd_workspace_size(1, 1, 4, 1))
-        workspace = _workspace(dev, nbytes)
+        workspace = _workspace(dev, 256)
     stream = torch.cuda.current_stream(workspace.device).cuda_stream
     return int(library().ssm_read_device_status(_ptr(workspace), ctypes.c_void_p(stream)))
 

@@ -56,7 +56,22 @@ struct ScanParams {
   const void* B;
   const void* C;
   void* y;
+  // L split across CTAs (segmented two-pass scan); nseg = 1, seg_len = seqlen otherwise
+  int nseg;                 // segments of the sequence
+  int seg_len;              // positions per segment (a multiple of the chunk)
+  float* seg_state;         // [nseg][batch * dim][N]: end state of each segment from h = 0
+  float* seg_sum;           // [nseg][batch * dim]: sum of dt * log2(e) over each segment
 };
+
+// Kernel modes of the channel kernel:
+//   kModeFull    one pass over the whole sequence (nseg = 1)
+//   kModeStates  pass 1 of the segmented scan: each CTA runs its segment from a zero
+//                state, reads u, delta, B only, and writes the segment's end state and
+//                step-size sum (no output)
+//   kModeCarry   pass 2: each CTA rebuilds the state entering its segment from h0 and
+//                the earlier segments' (end state, step-size sum), then runs the
+//                segment with outputs
+constexpr int kModeFull = 0, kModeStates = 1, kModeCarry = 2;
 
 // |A| below this (or A == 0) sends a bf16 CTA to the accurate path: the fast
 // path forms (Abar - 1) w as Abar (h + w) - w, whose absolute error grows like
@@ -262,12 +277,13 @@ __device__ __forceinline__ void reduce_scatter(const float* v, float* out, float
 // one chunk of positions for one lane (its channel's row `row` of the tiles,
 // its states part*NS .. part*NS + NS - 1)
 // ---------------------------------------------------------------------------
-template <typename Cfg, typename IO, bool ACC, bool TAIL>
+template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL>
 __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile, const float* bcfB,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
                                            const float* nIA, float Dd, float bias2, int softplus,
-                                           float* h) {
+                                           float* h, float& ssum) {
+  constexpr bool OUT = MODE != kModeStates;  // this pass writes y
   constexpr int N = Cfg::N, NS = Cfg::NS, LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB,
                 RB = Cfg::RB;
   const uint8_t* tu = stage;
@@ -293,6 +309,10 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
       }
       allgather<LPC, PB>(sm, sj, xch, lane);
     }
+    if constexpr (!OUT) {
+#pragma unroll
+      for (int j = 0; j < TB; ++j) ssum += sj[j];
+    }
     float acc[TB];
 #pragma unroll
     for (int j = 0; j < TB; ++j) {
@@ -303,7 +323,7 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 #pragma unroll
       for (int m = 0; m < NS; m += 4) {
         const float4 Bv = lds128f(Bp + m);
-        const float4 Cv = lds128f(Cp + m);
+        const float4 Cv = OUT ? lds128f(Cp + m) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
         const float cv[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
 #pragma unroll
@@ -331,11 +351,12 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
               h[i + e] = fmaf(a, h[i + e], coef * (bv[pp + e] * uj[j]));
             }
           }
-          a2 = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), a2);
+          if constexpr (OUT) a2 = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), a2);
         }
       }
       acc[j] = a2.x + a2.y;
     }
+    if constexpr (!OUT) continue;
     // full contraction of this lane's positions, then D skip, gate, rounding
     float ym[PB];
     reduce_scatter<LPC, TB>(acc, ym, xch + Cfg::XCH_S, lane, part);
@@ -361,10 +382,13 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <typename IO, typename Cfg>
+template <typename IO, typename Cfg, int MODE>
 __global__ void __launch_bounds__(Cfg::THREADS)
     scan_channel_kernel(const __grid_constant__ ChanMaps maps, const ScanParams p) {
   constexpr int N = Cfg::N, NS = Cfg::NS, S = Cfg::S, LC = Cfg::LC;
+  constexpr bool OUT = MODE != kModeStates;
+  // bytes one chunk brings in: pass 1 needs u, delta and B only
+  constexpr uint32_t TX = OUT ? Cfg::TX_BYTES : 2 * Cfg::DT * Cfg::RB + N * Cfg::RB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + Cfg::ALIGN - 1) &
@@ -372,15 +396,20 @@ __global__ void __launch_bounds__(Cfg::THREADS)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
 
   const int tid = threadIdx.x;
-  const int b = blockIdx.x / p.dtiles;
+  // block index = (segment * batch + b) * dtiles + channel tile
+  const int rest = blockIdx.x / p.dtiles;
+  const int b = rest % p.batch;
+  const int seg = rest / p.batch;
   const int d0 = (blockIdx.x % p.dtiles) * Cfg::DT;
+  const int l_begin = seg * p.seg_len;
+  const int l_end = (p.seqlen - l_begin < p.seg_len) ? p.seqlen : l_begin + p.seg_len;
   const int row = tid / Cfg::LPC;
   const int part = tid % Cfg::LPC;
   const int lane = tid & 31;
   float* xch = reinterpret_cast<float*>(smem + Cfg::OFF_XCH + (tid >> 5) * Cfg::XCH_WARP);
   const int d = d0 + row;
   const bool valid = d < p.dim;
-  const int nchunks = (p.seqlen + LC - 1) / LC;
+  const int nchunks = (l_end - l_begin + LC - 1) / LC;
 
   // per-lane parameters and state: states part*NS .. part*NS + NS - 1
   float Areg[NS], nIA[NS], h[NS];
@@ -392,8 +421,25 @@ __global__ void __launch_bounds__(Cfg::THREADS)
     Areg[i] = a;
     nIA[i] = (a == 0.0f) ? 0.0f : -1.0f / a;
     small_a |= !(fabsf(a) >= kFastPathMinAbsA);
-    h[i] = (valid && p.h0) ? __ldg(p.h0 + state0 + i) : 0.0f;
+    h[i] = (MODE != kModeStates && valid && p.h0) ? __ldg(p.h0 + state0 + i) : 0.0f;
   }
+  if constexpr (MODE == kModeCarry) {
+    // state entering this segment: fold in each earlier segment j as
+    // h <- 2^(A * sum_j) h + E_j (the recurrence is linear in h; 2^(A sum_j) is the
+    // product of the segment's Abar factors)
+    const int64_t chan = static_cast<int64_t>(b) * p.dim + d;
+    const int64_t per_seg = static_cast<int64_t>(p.batch) * p.dim;
+    if (valid) {
+#pragma unroll 1
+      for (int j = 0; j < seg; ++j) {
+        const float sum = __ldg(p.seg_sum + j * per_seg + chan);
+        const float* E = p.seg_state + (j * per_seg + chan) * N + part * NS;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) h[i] = fmaf(ex2(Areg[i] * sum), h[i], __ldg(E + i));
+      }
+    }
+  }
+  float ssum = 0.0f;  // pass 1: sum of the segment's step sizes (log2 units)
   const float Dd = (valid && p.D) ? __ldg(p.D + d) : 0.0f;
   const float bias2 = (valid && p.bias) ? __ldg(p.bias + d) * kLog2e : 0.0f;
   const bool accurate = (sizeof(IO) == 4) ? true : (__syncthreads_or(small_a) != 0);
@@ -413,13 +459,13 @@ __global__ void __launch_bounds__(Cfg::THREADS)
   auto issue_loads = [&](int k) {
     uint8_t* st = smem + Cfg::OFF_STAGES + (k % S) * Cfg::STAGE;
     uint64_t* bar = &full[k % S];
-    mbar_arrive_expect_tx(bar, Cfg::TX_BYTES);
-    const int l = k * LC;
+    mbar_arrive_expect_tx(bar, TX);
+    const int l = l_begin + k * LC;
     tma_load_3d(st, &maps.u, bar, l, d0, b);
     tma_load_3d(st + Cfg::TILE, &maps.delta, bar, l, d0, b);
-    if (Cfg::GATE) tma_load_3d(st + 2 * Cfg::TILE, &maps.z, bar, l, d0, b);
+    if (Cfg::GATE && OUT) tma_load_3d(st + 2 * Cfg::TILE, &maps.z, bar, l, d0, b);
     tma_load_3d(st + Cfg::NARR * Cfg::TILE, &maps.B, bar, l, 0, b);
-    tma_load_3d(st + Cfg::NARR * Cfg::TILE + Cfg::BCT, &maps.C, bar, l, 0, b);
+    if (OUT) tma_load_3d(st + Cfg::NARR * Cfg::TILE + Cfg::BCT, &maps.C, bar, l, 0, b);
   };
 
   int issued = (S < nchunks) ? S : nchunks;  // chunks whose loads were issued (thread 0)
@@ -438,7 +484,7 @@ __global__ void __launch_bounds__(Cfg::THREADS)
       float* bf = reinterpret_cast<float*>(smem + Cfg::OFF_BCF + (k & 1) * 2 * Cfg::BCF);
       const uint8_t* raw = st + Cfg::NARR * Cfg::TILE;
 #pragma unroll 1
-      for (int piece = tid; piece < 2 * N * Cfg::NBLK; piece += Cfg::THREADS) {
+      for (int piece = tid; piece < (OUT ? 2 : 1) * N * Cfg::NBLK; piece += Cfg::THREADS) {
         const int arr = piece / (N * Cfg::NBLK);
         const int rem = piece % (N * Cfg::NBLK);
         const int n = rem % N, kb = rem / N;
@@ -449,14 +495,17 @@ __global__ void __launch_bounds__(Cfg::THREADS)
         for (int e = 0; e < Cfg::TB; ++e) dst[e * N] = v[e];
       }
     }
-    if (tid == 0 && k >= 2) tma_store_wait_read<0>();  // store of chunk k-2 has read its tile
+    if (OUT && tid == 0 && k >= 2) tma_store_wait_read<0>();  // chunk k-2's store read its tile
     if (__syncthreads_or(!arrived)) {
       ok = false;
       break;
     }
     if (tid == 0 && k >= 1) {
-      tma_store_3d(&maps.y, smem + Cfg::OFF_Y + ((k - 1) & 1) * Cfg::TILE, (k - 1) * LC, d0, b);
-      tma_store_commit();
+      if (OUT) {
+        tma_store_3d(&maps.y, smem + Cfg::OFF_Y + ((k - 1) & 1) * Cfg::TILE,
+                     l_begin + (k - 1) * LC, d0, b);
+        tma_store_commit();
+      }
       if (k - 1 + S < nchunks) {
         fence_proxy_async_smem();
         issue_loads(k - 1 + S);  // stage of chunk k-1 is free: every thread passed the barrier
@@ -467,30 +516,33 @@ __global__ void __launch_bounds__(Cfg::THREADS)
         reinterpret_cast<const float*>(smem + Cfg::OFF_BCF + (k & 1) * 2 * Cfg::BCF);
     const float* bcfC = bcfB + Cfg::BCF / 4;
     uint8_t* ytile = smem + Cfg::OFF_Y + (k & 1) * Cfg::TILE;
-    const bool tail = (k + 1) * LC > p.seqlen;
+    const int l0 = l_begin + k * LC;
+    const bool tail = l0 + LC > p.seqlen;
     if constexpr (sizeof(IO) == 2) {
       if (!accurate) {
         if (!tail)
-          chan_chunk<Cfg, IO, false, false>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen,
-                                            Areg, nIA, Dd, bias2, p.softplus, h);
+          chan_chunk<Cfg, IO, MODE, false, false>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
+                                                  p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h,
+                                                  ssum);
         else
-          chan_chunk<Cfg, IO, false, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen,
-                                           Areg, nIA, Dd, bias2, p.softplus, h);
+          chan_chunk<Cfg, IO, MODE, false, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
+                                                 p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h,
+                                                 ssum);
       } else {
-        chan_chunk<Cfg, IO, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen,
-                                        Areg, nIA, Dd, bias2, p.softplus, h);
+        chan_chunk<Cfg, IO, MODE, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
+                                              p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h, ssum);
       }
     } else {
-      chan_chunk<Cfg, IO, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, k * LC, p.seqlen, Areg,
-                                      nIA, Dd, bias2, p.softplus, h);
+      chan_chunk<Cfg, IO, MODE, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
+                                            p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h, ssum);
     }
     fence_proxy_async_smem();  // y tile writes -> visible to the TMA store
   }
   __syncthreads();
   if (tid == 0) {
-    if (ok && nchunks > 0) {
+    if (OUT && ok && nchunks > 0) {
       tma_store_3d(&maps.y, smem + Cfg::OFF_Y + ((nchunks - 1) & 1) * Cfg::TILE,
-                   (nchunks - 1) * LC, d0, b);
+                   l_begin + (nchunks - 1) * LC, d0, b);
       tma_store_commit();
     }
     tma_store_wait_all<0>();
@@ -500,9 +552,18 @@ __global__ void __launch_bounds__(Cfg::THREADS)
       for (int kk = k; kk < issued; ++kk) (void)mbar_wait_bounded(&full[kk % S], (kk / S) & 1);
     }
   }
-  if (ok && valid && p.h_last) {
+  if (ok && valid) {
+    if constexpr (MODE == kModeStates) {
+      const int64_t chan = static_cast<int64_t>(b) * p.dim + d;
+      const int64_t per_seg = static_cast<int64_t>(p.batch) * p.dim;
+      float* E = p.seg_state + (seg * per_seg + chan) * N + part * NS;
 #pragma unroll
-    for (int i = 0; i < NS; ++i) p.h_last[state0 + i] = h[i];
+      for (int i = 0; i < NS; ++i) E[i] = h[i];
+      if (part == 0) p.seg_sum[seg * per_seg + chan] = ssum;
+    } else if (p.h_last && seg == p.nseg - 1) {
+#pragma unroll
+      for (int i = 0; i < NS; ++i) p.h_last[state0 + i] = h[i];
+    }
   }
 }
 

@@ -148,6 +148,22 @@ bool vec_eligible(const ScanCall& c) {
   return true;
 }
 
+// SM count of the current device (cached per device ordinal).
+int sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 ScanParams make_params(const ScanCall& c, void* workspace) {
   ScanParams p;
   p.batch = static_cast<int>(c.batch);
@@ -167,7 +183,54 @@ ScanParams make_params(const ScanCall& c, void* workspace) {
   p.B = c.B;
   p.C = c.C;
   p.y = c.y;
+  p.nseg = 1;
+  p.seg_len = static_cast<int>(c.seqlen);
+  p.seg_state = nullptr;
+  p.seg_sum = nullptr;
   return p;
+}
+
+// ---------------------------------------------------------------------------
+// segmented (two-pass) plan for long sequences over few channels
+// ---------------------------------------------------------------------------
+// Workspace layout: [0, 256) device status words; then the segments' end states
+// [nseg][batch * dim][N] fp32; then their step-size sums [nseg][batch * dim] fp32.
+constexpr size_t kStatusBytes = 256;
+constexpr int64_t kSegMinLen = 256;        // positions: shorter segments cost more than they gain
+constexpr int64_t kSegMinSeqlen = 8192;    // AUTO splits sequences at least this long
+constexpr int kSegCtasPerSm = 3;            // one-lane-per-channel CTAs an SM holds at once
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct SegPlan {
+  int nseg = 1;     // 1: not segmented
+  int seg_len = 0;
+};
+
+// Segments for the one-lane-per-channel channel kernel: enough that the CTAs fill
+// every SM (kSegCtasPerSm per SM), each at least kSegMinLen positions long, a
+// multiple of the chunk (lc positions).  `force` asks for at least two segments.
+SegPlan seg_plan(int64_t batch, int64_t dim, int64_t seqlen, int lc, bool force) {
+  SegPlan pl;
+  const int64_t ctas = batch * ((dim + 127) / 128);
+  int64_t nseg = static_cast<int64_t>(sm_count()) * kSegCtasPerSm / ctas;
+  if (nseg > seqlen / kSegMinLen) nseg = seqlen / kSegMinLen;
+  if (force && nseg < 2) nseg = 2;
+  if (nseg > (seqlen + lc - 1) / lc) nseg = (seqlen + lc - 1) / lc;
+  if (nseg < 2) return pl;
+  int64_t len = (seqlen + nseg - 1) / nseg;
+  len = (len + lc - 1) / lc * lc;
+  pl.nseg = static_cast<int>((seqlen + len - 1) / len);
+  pl.seg_len = static_cast<int>(len);
+  if (pl.nseg < 2) pl.nseg = 1;
+  return pl;
+}
+
+size_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, const SegPlan& pl) {
+  if (pl.nseg < 2) return kStatusBytes;
+  const size_t chans = static_cast<size_t>(batch) * static_cast<size_t>(dim);
+  return kStatusBytes + round_up(static_cast<size_t>(pl.nseg) * chans * dstate * 4, 256) +
+         round_up(static_cast<size_t>(pl.nseg) * chans * 4, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -183,7 +246,8 @@ struct ChanShape {
 };
 
 template <typename IO, int N, bool GATE, int LPC>
-ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t stream) {
+ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t stream,
+                          const SegPlan& seg = SegPlan()) {
   using Shape = ChanShape<LPC>;
   using Cfg = ChanCfg<IO, N, GATE, LPC, Shape::S, Shape::RB>;
   ChanMaps maps;
@@ -201,32 +265,45 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
   }
   ScanParams p = make_params(c, workspace);
   p.dtiles = static_cast<int>((c.dim + Cfg::DT - 1) / Cfg::DT);
-  if (c.batch * p.dtiles > INT32_MAX) return SSM_ERR_INVALID_ARG;
-  auto kern = ssm::scan_channel_kernel<IO, Cfg>;
+  const int64_t tiles = c.batch * p.dtiles;
+  if (tiles * (seg.nseg > 1 ? seg.nseg : 1) > INT32_MAX) return SSM_ERR_INVALID_ARG;
+  if constexpr (LPC == 1) {
+    if (seg.nseg > 1) {
+      // pass 1 (segments 0 .. nseg-2: each segment's end state from h = 0 and its
+      // step-size sum), then pass 2 (every segment, entering state rebuilt from them)
+      p.nseg = seg.nseg;
+      p.seg_len = seg.seg_len;
+      const size_t chans = static_cast<size_t>(c.batch) * static_cast<size_t>(c.dim);
+      uint8_t* base = static_cast<uint8_t*>(workspace);
+      p.seg_state = reinterpret_cast<float*>(base + kStatusBytes);
+      p.seg_sum = reinterpret_cast<float*>(
+          base + kStatusBytes + round_up(static_cast<size_t>(seg.nseg) * chans * N * 4, 256));
+      auto k1 = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeStates>;
+      auto k2 = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeCarry>;
+      cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Cfg::SMEM_ALLOC);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel)");
+      k1<<<static_cast<unsigned>(tiles * (seg.nseg - 1)), Cfg::THREADS, Cfg::SMEM_ALLOC, stream>>>(
+          maps, p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "scan_channel (segment states) launch");
+      k2<<<static_cast<unsigned>(tiles * seg.nseg), Cfg::THREADS, Cfg::SMEM_ALLOC, stream>>>(maps,
+                                                                                               p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "scan_channel (segments) launch");
+      return SSM_OK;
+    }
+  }
+  auto kern = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeFull>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel)");
-  const unsigned grid = static_cast<unsigned>(c.batch * p.dtiles);
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_ALLOC, stream>>>(maps, p);
+  kern<<<static_cast<unsigned>(tiles), Cfg::THREADS, Cfg::SMEM_ALLOC, stream>>>(maps, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "scan_channel launch");
   return SSM_OK;
-}
-
-// SM count of the current device (cached per device ordinal).
-int sm_count() {
-  static std::mutex mu;
-  static int cache[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    cache[dev] = n;
-  }
-  return cache[dev];
 }
 
 // Lanes per channel for the channel kernel.  Every SM sub-partition runs one warp
@@ -282,8 +359,13 @@ ssm_status launch_channel_lpc(const ScanCall& c, void* ws, cudaStream_t s) {
 }
 
 template <typename IO, int N>
-ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s) {
+ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s,
+                           const SegPlan& seg) {
   const bool gate = c.z != nullptr;
+  if (algo == SSM_ALGO_SEGMENTED) {
+    return gate ? launch_channel<IO, N, true, 1>(c, ws, s, seg)
+                : launch_channel<IO, N, false, 1>(c, ws, s, seg);
+  }
   if (algo == SSM_ALGO_CHANNEL) {
     switch (choose_lpc(c.batch, c.dim, N)) {
       case 4: return launch_channel_lpc<IO, N, 4>(c, ws, s);
@@ -300,11 +382,12 @@ ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStrea
 }
 
 template <typename IO>
-ssm_status dispatch_scan(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s) {
+ssm_status dispatch_scan(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s,
+                         const SegPlan& seg) {
   switch (c.dstate) {
-    case 4: return dispatch_scan_n<IO, 4>(c, algo, ws, s);
-    case 8: return dispatch_scan_n<IO, 8>(c, algo, ws, s);
-    case 16: return dispatch_scan_n<IO, 16>(c, algo, ws, s);
+    case 4: return dispatch_scan_n<IO, 4>(c, algo, ws, s, seg);
+    case 8: return dispatch_scan_n<IO, 8>(c, algo, ws, s, seg);
+    case 16: return dispatch_scan_n<IO, 16>(c, algo, ws, s, seg);
     default: return SSM_ERR_UNSUPPORTED;
   }
 }
@@ -392,11 +475,16 @@ ssm_status noalloc_scratch(void** out) {
 extern "C" {
 
 size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
-  (void)batch;
-  (void)dim;
-  (void)dstate;
-  (void)seqlen;
-  return kWorkspaceBytes;
+  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1) return kWorkspaceBytes;
+  if (batch > (int64_t(1) << 62) / dim / seqlen) return kWorkspaceBytes;
+  // the larger of the segmented plans for fp32 (8-position chunks) and for SSM_ALGO_SEGMENTED
+  // (at least two segments); bf16's 16-position chunks never need more segments
+  size_t need = kWorkspaceBytes;
+  for (const bool force : {false, true}) {
+    const size_t b = seg_workspace_bytes(batch, dim, dstate, seg_plan(batch, dim, seqlen, 8, force));
+    if (b > need) need = b;
+  }
+  return need;
 }
 
 ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
@@ -406,10 +494,9 @@ ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t
                              const float* h0, float* h_last, void* y, void* workspace,
                              size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream) {
   if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_CHANNEL && algo != SSM_ALGO_CHUNK &&
-      algo != SSM_ALGO_CHANNEL_L1 && algo != SSM_ALGO_CHANNEL_L2 && algo != SSM_ALGO_CHANNEL_L4)
+      algo != SSM_ALGO_CHANNEL_L1 && algo != SSM_ALGO_CHANNEL_L2 && algo != SSM_ALGO_CHANNEL_L4 &&
+      algo != SSM_ALGO_SEGMENTED)
     return SSM_ERR_UNSUPPORTED;
-  const bool fixed_split = algo == SSM_ALGO_CHANNEL_L1 || algo == SSM_ALGO_CHANNEL_L2 ||
-                           algo == SSM_ALGO_CHANNEL_L4;
   if ((algo == SSM_ALGO_CHANNEL_L2 && dstate < 8) || (algo == SSM_ALGO_CHANNEL_L4 && dstate < 16))
     return SSM_ERR_UNSUPPORTED;
   ScanCall c;
@@ -434,15 +521,39 @@ ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t
   ssm_status st = validate_scan(c, workspace, workspace_bytes);
   if (st != SSM_OK) return st;
 
-  if (algo == SSM_ALGO_AUTO)
-    algo = (c.batch * c.dim >= kChannelKernelMinChannels) ? SSM_ALGO_CHANNEL : SSM_ALGO_CHUNK;
-  if ((algo == SSM_ALGO_CHANNEL || fixed_split) && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;
+  const int lc = c.bf16 ? 16 : 8;  // channel kernel chunk (32-byte rows)
+  SegPlan seg;
+  if (algo == SSM_ALGO_SEGMENTED) {
+    seg = seg_plan(c.batch, c.dim, c.seqlen, lc, true);
+    if (seg.nseg < 2) {
+      algo = SSM_ALGO_CHANNEL_L1;  // too short to split
+    } else if (workspace_bytes < seg_workspace_bytes(c.batch, c.dim, c.dstate, seg)) {
+      g_last_cuda_error = "workspace smaller than ssm_scan_fwd_workspace_size()";
+      return SSM_ERR_INVALID_ARG;
+    }
+  } else if (algo == SSM_ALGO_AUTO) {
+    if (c.batch * c.dim >= kChannelKernelMinChannels) {
+      algo = SSM_ALGO_CHANNEL;
+    } else {
+      // few channels: split a long sequence across CTAs when the caller's workspace
+      // holds the segments' states; else lanes over positions (measured on B300: the
+      // 130M-like layer, 3072 channels x 2048 fp32, runs 179 us over positions and
+      // 306 us in 8 segments; a 1536-channel x 131072 bf16 scan 3.7 ms over positions
+      // and 1.7 ms in 37 segments)
+      if (c.seqlen >= kSegMinSeqlen) seg = seg_plan(c.batch, c.dim, c.seqlen, lc, false);
+      algo = (seg.nseg > 1 &&
+              workspace_bytes >= seg_workspace_bytes(c.batch, c.dim, c.dstate, seg))
+                 ? SSM_ALGO_SEGMENTED
+                 : SSM_ALGO_CHUNK;
+    }
+  }
+  if (algo != SSM_ALGO_CHUNK && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;  // TMA kernels only
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(ssm::DeviceStatus), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
-  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s)
-                : dispatch_scan<float>(c, algo, workspace, s);
+  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s, seg)
+                : dispatch_scan<float>(c, algo, workspace, s, seg);
 }
 
 ssm_status ssm_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ssm_dtype io,
@@ -460,7 +571,9 @@ ssm_status ssm_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int6
                                 const float* delta_bias, int delta_softplus, const float* A,
                                 const void* B, const void* C, const float* D, const void* z,
                                 const float* h0, float* h_last, void* y, ssm_stream_t stream) {
-  const size_t need = ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen);
+  // every plan needs the status words; the segmented long-sequence plan needs more
+  // and is then skipped by AUTO (it picks the kernels whose scratch fits)
+  const size_t need = kWorkspaceBytes;
   if (need > kNoAllocScratchBytes) {
     g_last_cuda_error = "ssm_scan_fwd_noalloc: these sizes need " + std::to_string(need) +
                         " bytes of scratch, more than the " +

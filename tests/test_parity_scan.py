@@ -15,7 +15,8 @@ from selective_state_space_115_b300 import workloads as W
 from tests.helpers import TOL, from_torch, rel_err, sample_rows, torch_f32, torch_io
 
 pytestmark = pytest.mark.gpu
-ALGOS = ["channel_l1", "channel_l2", "channel_l4", "chunk"]
+ALGOS = ["channel_l1", "channel_l2", "channel_l4", "chunk", "segmented"]
+FULL_ALGOS = ALGOS + ["auto"]
 MIN_DSTATE = {"channel_l2": 8, "channel_l4": 16}
 NTHREADS = os.cpu_count() or 1
 _ORACLE_CACHE = {}
@@ -88,7 +89,7 @@ def test_tiny(algo):
     assert rel_err(from_torch(hl), hr) <= TOL[cfg.io]
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", FULL_ALGOS)
 def test_130m_full(algo):
     cfg = W.SCAN_CONFIGS["130m"]
     x = workload_inputs("130m")
@@ -100,7 +101,7 @@ def test_130m_full(algo):
     assert rel_err(from_torch(hl), hr) <= TOL[cfg.io]
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", FULL_ALGOS)
 def test_2p8b_sampled(algo):
     cfg = W.SCAN_CONFIGS["2p8b"]
     x = workload_inputs("2p8b")
@@ -115,7 +116,7 @@ def test_2p8b_sampled(algo):
     assert rel_err(from_torch(hl).reshape(-1, cfg.dstate)[rows], hr) <= 1e-3
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", FULL_ALGOS)
 def test_long_sampled(algo):
     cfg = W.SCAN_CONFIGS["long"]
     x = workload_inputs("long")
