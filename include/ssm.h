@@ -109,6 +109,12 @@ typedef enum {
  */
 SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
 
+/* Workspace bytes ssm_scan_fwd_algo needs with this kernel family (AUTO: the same
+ * as ssm_scan_fwd_workspace_size; SEGMENTED: room for at least two segments;
+ * every other family: the 256 bytes of status words). */
+SSM_API size_t ssm_scan_fwd_algo_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                                int64_t seqlen, ssm_algo algo);
+
 /*
  * Selective-scan forward over a whole sequence (the pages' selective scan with
  * ZOH discretisation, fused: softplus, discretisation, recurrence,

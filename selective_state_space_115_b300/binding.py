@@ -39,7 +39,8 @@ _ALGOS = {"auto": ALGO_AUTO, "channel": ALGO_CHANNEL, "chunk": ALGO_CHUNK,
 _ALGOS.update({v: v for v in list(_ALGOS.values())})
 
 # every symbol include/ssm.h declares
-EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_algo",
+EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "ssm_scan_fwd",
+            "ssm_scan_fwd_algo",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -79,6 +80,8 @@ def library(path: Optional[str] = None):
         lib = ctypes.CDLL(p)
         lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
         lib.ssm_scan_fwd_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
+        lib.ssm_scan_fwd_algo_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_fwd_algo_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _int]
         scan_args = [_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
                      _vp, _vp, _vp, _vp, ctypes.c_size_t]
         lib.ssm_scan_fwd.restype = _int
@@ -192,7 +195,7 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     h_last = (torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
               if return_last_state else None)
     lib = library()
-    nbytes = int(lib.ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen))
+    nbytes = int(lib.ssm_scan_fwd_algo_workspace_size(batch, dim, dstate, seqlen, _ALGOS[algo]))
     ws = _workspace(dev, nbytes) if workspace is None else workspace
     stream = torch.cuda.current_stream(dev).cuda_stream
     with torch.cuda.device(dev):

@@ -474,17 +474,23 @@ ssm_status noalloc_scratch(void** out) {
 // ===========================================================================
 extern "C" {
 
-size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+size_t ssm_scan_fwd_algo_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                        int64_t seqlen, ssm_algo algo) {
   if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1) return kWorkspaceBytes;
   if (batch > (int64_t(1) << 62) / dim / seqlen) return kWorkspaceBytes;
-  // the larger of the segmented plans for fp32 (8-position chunks) and for SSM_ALGO_SEGMENTED
-  // (at least two segments); bf16's 16-position chunks never need more segments
-  size_t need = kWorkspaceBytes;
-  for (const bool force : {false, true}) {
-    const size_t b = seg_workspace_bytes(batch, dim, dstate, seg_plan(batch, dim, seqlen, 8, force));
-    if (b > need) need = b;
-  }
-  return need;
+  // the segmented plan for fp32 (8-position chunks); bf16's 16-position chunks never
+  // need more segments
+  SegPlan pl;
+  if (algo == SSM_ALGO_SEGMENTED)
+    pl = seg_plan(batch, dim, seqlen, 8, true);
+  else if (algo == SSM_ALGO_AUTO && batch * dim < kChannelKernelMinChannels &&
+           seqlen >= kSegMinSeqlen)
+    pl = seg_plan(batch, dim, seqlen, 8, false);
+  return seg_workspace_bytes(batch, dim, dstate, pl);
+}
+
+size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+  return ssm_scan_fwd_algo_workspace_size(batch, dim, dstate, seqlen, SSM_ALGO_AUTO);
 }
 
 ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,

@@ -44,6 +44,42 @@ def test_workspace_size():
     assert lib.ssm_scan_fwd_workspace_size(8, 5120, 16, 2048) % 16 == 0
 
 
+def _seg_bytes(chans, n, nseg):
+    rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    return 256 + rnd(nseg * chans * n * 4) + rnd(nseg * chans * 4)
+
+
+def test_workspace_size_follows_the_plan():
+    """Many channels or short sequences: status words only.  A long sequence over
+    few channels: room for each segment's end state and step-size sum, the segments
+    sized so one-lane-per-channel CTAs fill the GPU (3 per SM; without a device the
+    library assumes 148 SMs)."""
+    lib = binding.library()
+    ws = lib.ssm_scan_fwd_workspace_size
+    assert ws(8, 5120, 16, 2048) == 256        # 40960 channels: channel kernel, no split
+    assert ws(2, 1536, 16, 2048) == 256        # few channels, short: lanes over positions
+    # 1536 channels x 131072: 12 CTAs of 128 channels -> 444 // 12 = 37 segments
+    assert ws(1, 1536, 16, 131072) == _seg_bytes(1536, 16, 37)
+    assert ws(1, 1536, 8, 131072) == _seg_bytes(1536, 8, 37)
+    # each segment keeps at least 256 positions: 8192 positions -> at most 32 segments
+    assert ws(1, 128, 16, 8192) == _seg_bytes(128, 16, 32)
+    algo_ws = lib.ssm_scan_fwd_algo_workspace_size
+    assert algo_ws(1, 1536, 16, 131072, binding.ALGO_AUTO) == ws(1, 1536, 16, 131072)
+    assert algo_ws(1, 1536, 16, 131072, binding.ALGO_CHUNK) == 256
+    assert algo_ws(8, 5120, 16, 2048, binding.ALGO_CHANNEL_L2) == 256
+    # an explicit split asks for at least two segments even when channels are many
+    assert algo_ws(8, 5120, 16, 2048, binding.ALGO_SEGMENTED) == _seg_bytes(40960, 16, 2)
+    # too short to split (under two 8-position chunks): status words only
+    assert algo_ws(1, 4, 4, 8, binding.ALGO_SEGMENTED) == 256
+
+
+def test_segmented_rejects_a_small_workspace():
+    lib = binding.library()
+    st = scan(lib, batch=1, dim=256, dstate=16, seqlen=4096, wsb=256,
+              algo=binding.ALGO_SEGMENTED)
+    assert st == binding.SSM_ERR_INVALID_ARG
+
+
 # fake device addresses: validation must fail before anything dereferences them
 P = 0x7F0000000000
 WS = 0x7F0000100000
