@@ -73,7 +73,7 @@ struct ScanParams {
 //                segment with outputs
 constexpr int kModeFull = 0, kModeStates = 1, kModeCarry = 2;
 
-// |A| below this (or A == 0) sends a bf16 CTA to the accurate path: the fast
+// |A| below this (or A == 0) sends a bf16 channel group to the accurate path: the fast
 // path forms (Abar - 1) w as Abar (h + w) - w, whose absolute error grows like
 // 2^-22 |B u / A|.
 constexpr float kFastPathMinAbsA = 0.125f;
@@ -265,10 +265,10 @@ __device__ __forceinline__ void reduce_scatter(const float* v, float* out, float
     }
 #pragma unroll
     for (int k = 0; k < PB; ++k) {
-      float acc = r[k];
-#pragma unroll
-      for (int q = 1; q < LPC; ++q) acc += r[q * PB + k];
-      out[k] = acc;
+      if constexpr (LPC == 4)
+        out[k] = (r[k] + r[PB + k]) + (r[2 * PB + k] + r[3 * PB + k]);
+      else
+        out[k] = r[k] + r[PB + k];
     }
   }
 }
@@ -319,9 +319,13 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
       const int lc = blk * TB + j;  // position within the chunk
       const float* Bp = bcfB + lc * N + part * NS;
       const float* Cp = bcfC + lc * N + part * NS;
-      f2 a2 = mk2(0.0f, 0.0f);
+      // contraction in a fixed order for every lane split: a packed pair sum per
+      // group of 4 states, then a tree over the groups (and over lanes in
+      // reduce_scatter), so 1, 2 and 4 lanes per channel give identical bits
+      float pg[NS / 4];
 #pragma unroll
       for (int m = 0; m < NS; m += 4) {
+        f2 a2 = mk2(0.0f, 0.0f);
         const float4 Bv = lds128f(Bp + m);
         const float4 Cv = OUT ? lds128f(Cp + m) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
@@ -353,8 +357,14 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
           }
           if constexpr (OUT) a2 = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), a2);
         }
+        pg[m / 4] = a2.x + a2.y;
       }
-      acc[j] = a2.x + a2.y;
+      if constexpr (NS == 16)
+        acc[j] = (pg[0] + pg[1]) + (pg[2] + pg[3]);
+      else if constexpr (NS == 8)
+        acc[j] = pg[0] + pg[1];
+      else
+        acc[j] = pg[0];
     }
     if constexpr (!OUT) continue;
     // full contraction of this lane's positions, then D skip, gate, rounding
@@ -413,14 +423,12 @@ __global__ void __launch_bounds__(Cfg::THREADS)
 
   // per-lane parameters and state: states part*NS .. part*NS + NS - 1
   float Areg[NS], nIA[NS], h[NS];
-  bool small_a = false;
   const int64_t state0 = (static_cast<int64_t>(b) * p.dim + d) * N + part * NS;
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
     const float a = valid ? __ldg(p.A + static_cast<int64_t>(d) * N + part * NS + i) : -1.0f;
     Areg[i] = a;
     nIA[i] = (a == 0.0f) ? 0.0f : -1.0f / a;
-    small_a |= !(fabsf(a) >= kFastPathMinAbsA);
     h[i] = (MODE != kModeStates && valid && p.h0) ? __ldg(p.h0 + state0 + i) : 0.0f;
   }
   if constexpr (MODE == kModeCarry) {
@@ -442,7 +450,20 @@ __global__ void __launch_bounds__(Cfg::THREADS)
   float ssum = 0.0f;  // pass 1: sum of the segment's step sizes (log2 units)
   const float Dd = (valid && p.D) ? __ldg(p.D + d) : 0.0f;
   const float bias2 = (valid && p.bias) ? __ldg(p.bias + d) * kLog2e : 0.0f;
-  const bool accurate = (sizeof(IO) == 4) ? true : (__syncthreads_or(small_a) != 0);
+  // fast or accurate arithmetic, decided per aligned group of 32 channels (every
+  // warp of every lane split lies inside one group, so a channel's arithmetic does
+  // not depend on the split): accurate when any |A| of the group is below 1/8
+  bool accurate = true;
+  if constexpr (sizeof(IO) == 2) {
+    const int dg = (d0 + (tid >> 5) * (32 / Cfg::LPC)) / 32 * 32 + lane;  // lane's channel
+    bool small_a = false;
+    if (dg < p.dim) {
+#pragma unroll
+      for (int i = 0; i < N; ++i)
+        small_a |= !(fabsf(__ldg(p.A + static_cast<int64_t>(dg) * N + i)) >= kFastPathMinAbsA);
+    }
+    accurate = __any_sync(0xffffffffu, small_a);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);

@@ -304,6 +304,30 @@ def test_deterministic(algo):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("io,dstate", [(W.BF16, 16), (W.F32, 16), (W.BF16, 8)])
+def test_lane_splits_are_bit_identical(io, dstate):
+    """1, 2 and 4 lanes per channel evaluate every state update, the contraction
+    (per-4-state pair sums, then a tree) and the per-position work in the same order,
+    so they agree bit for bit -- including a channel group that takes the accurate
+    arithmetic (small |A|) next to groups on the fast path."""
+    cfg = W.ScanConfig("t", 2, 160, dstate, 512, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=23, with_h0=True)
+    A = x["A"].copy()
+    A[40, 2] = -1e-3  # channels 32..63 take the accurate path
+    x["A"] = A
+    outs = []
+    for algo in ("channel_l1", "channel_l2", "channel_l4"):
+        if dstate < MIN_DSTATE.get(algo, 0):
+            continue
+        y, hl = gpu_scan(x, io, algo, return_last_state=True)
+        outs.append((algo, from_torch(y), from_torch(hl)))
+    for algo, y, hl in outs[1:]:
+        assert np.array_equal(y, outs[0][1]), algo
+        assert np.array_equal(hl, outs[0][2]), algo
+    assert rel_err(outs[0][1], oracle_full(x, io)) <= TOL[io]
+
+
 def test_auto_matches_explicit_choice():
     cfg = W.SCAN_CONFIGS["2p8b"]
     x = W.make_scan_inputs(cfg, seed=0, batch=2)  # 10240 channels: the channel kernel
