@@ -73,6 +73,7 @@ def decode_bytes(cfg) -> int:
 # device sources each profiled kernel is compiled from
 KERNEL_SOURCES = {
     "scan_channel_2p8b": ("scan_channel.cuh", "ssm_device.cuh"),
+    "scan_channel_long": ("scan_channel.cuh", "ssm_device.cuh"),
     "state_update_decode": ("state_update.cuh", "ssm_device.cuh"),
 }
 
@@ -392,8 +393,9 @@ def run_gpu(args):
                     "bytes_per_step": bytes_step, "peak_kind": peak_kind},
             "roofline": {"bound": "alu", "achieved": achieved_exp, "peak": ex2_peak,
                          "unit": "Texp/s", "frac": achieved_exp / ex2_peak, "traffic": traffic,
-                         "kernel": "scan_channel_kernel<bf16, N=16, gate> (lanes-per-channel "
-                                   "split chosen by the library: 2 at this size)",
+                         "kernel": "scan_channel_mixed_kernel<bf16, N=16, gate> (the library's "
+                                   "choice at this size: two one-lane-per-channel CTAs per SM "
+                                   "plus the 24 leftover tiles as 96 four-lane CTAs)",
                          "units_per_launch": CFG.updates,
                          "peak_note": "148 SMs x 32 ex2/clk/SM (measured ex2.approx.f32 "
                                       "throughput) x 2032 MHz max SM clock"},

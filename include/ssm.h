@@ -97,7 +97,13 @@ typedef enum {
                                  a zero state, then every segment again from the state
                                  rebuilt from the earlier segments.  Needs the workspace
                                  that ssm_scan_fwd_workspace_size() reports; sequences
-                                 too short to split run as CHANNEL_L1 */
+                                 too short to split run as CHANNEL_L1 */,
+    SSM_ALGO_CHANNEL_MIXED = 7 /* dstate 16: every SM runs the same number k of
+                                 one-lane-per-channel CTAs of 128 channels, and the
+                                 tiles left over run as 32-channel CTAs with four lanes
+                                 per channel (each CTA takes its role when it starts;
+                                 the splits give identical bits).  CHANNEL picks it when
+                                 its cost model favours it; other dstate run CHANNEL */
 } ssm_algo;
 
 /*

@@ -33,9 +33,11 @@ ALGO_CHANNEL_L1 = 3
 ALGO_CHANNEL_L2 = 4
 ALGO_CHANNEL_L4 = 5
 ALGO_SEGMENTED = 6
+ALGO_CHANNEL_MIXED = 7
 _ALGOS = {"auto": ALGO_AUTO, "channel": ALGO_CHANNEL, "chunk": ALGO_CHUNK,
           "channel_l1": ALGO_CHANNEL_L1, "channel_l2": ALGO_CHANNEL_L2,
-          "channel_l4": ALGO_CHANNEL_L4, "segmented": ALGO_SEGMENTED}
+          "channel_l4": ALGO_CHANNEL_L4, "segmented": ALGO_SEGMENTED,
+          "channel_mixed": ALGO_CHANNEL_MIXED}
 _ALGOS.update({v: v for v in list(_ALGOS.values())})
 
 # every symbol include/ssm.h declares

@@ -392,25 +392,22 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// One CTA's work: channels d0 .. d0 + DT - 1 of batch row b over segment `seg`
+// (the whole sequence when nseg == 1).  `maps` must live in kernel parameter
+// space (a __grid_constant__ argument): TMA reads the descriptors from there.
 template <typename IO, typename Cfg, int MODE>
-__global__ void __launch_bounds__(Cfg::THREADS)
-    scan_channel_kernel(const __grid_constant__ ChanMaps maps, const ScanParams p) {
+__device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanParams& p, int b,
+                                             int d0, int seg, uint8_t* smem_raw) {
   constexpr int N = Cfg::N, NS = Cfg::NS, S = Cfg::S, LC = Cfg::LC;
   constexpr bool OUT = MODE != kModeStates;
   // bytes one chunk brings in: pass 1 needs u, delta and B only
   constexpr uint32_t TX = OUT ? Cfg::TX_BYTES : 2 * Cfg::DT * Cfg::RB + N * Cfg::RB;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + Cfg::ALIGN - 1) &
       ~static_cast<uintptr_t>(Cfg::ALIGN - 1));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
 
   const int tid = threadIdx.x;
-  // block index = (segment * batch + b) * dtiles + channel tile
-  const int rest = blockIdx.x / p.dtiles;
-  const int b = rest % p.batch;
-  const int seg = rest / p.batch;
-  const int d0 = (blockIdx.x % p.dtiles) * Cfg::DT;
   const int l_begin = seg * p.seg_len;
   const int l_end = (p.seqlen - l_begin < p.seg_len) ? p.seqlen : l_begin + p.seg_len;
   const int row = tid / Cfg::LPC;
@@ -585,6 +582,81 @@ __global__ void __launch_bounds__(Cfg::THREADS)
 #pragma unroll
       for (int i = 0; i < NS; ++i) p.h_last[state0 + i] = h[i];
     }
+  }
+}
+
+template <typename IO, typename Cfg, int MODE>
+__global__ void __launch_bounds__(Cfg::THREADS)
+    scan_channel_kernel(const __grid_constant__ ChanMaps maps, const ScanParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // block index = (segment * batch + b) * dtiles + channel tile
+  const int rest = blockIdx.x / p.dtiles;
+  channel_body<IO, Cfg, MODE>(maps, p, rest % p.batch, (blockIdx.x % p.dtiles) * Cfg::DT,
+                              rest / p.batch, smem_raw);
+}
+
+// ---------------------------------------------------------------------------
+// mixed split: whole SMs' worth of one-lane-per-channel CTAs plus the remainder
+// in four-lanes-per-channel CTAs
+// ---------------------------------------------------------------------------
+// With T 128-channel tiles on `sms` SMs, one lane per channel runs T / sms CTAs
+// per SM when that divides; otherwise the SMs that get one more CTA set the time.
+// The mixed launch gives every SM exactly k = floor(T / sms) one-lane CTAs (CfgA)
+// and splits the other T - k * sms tiles into 32-channel CTAs with four lanes per
+// channel (CfgB), which spread over the SMs at a quarter of the cost each.  The
+// block scheduler does not guarantee k CTAs per SM, so each CTA picks its role
+// when it starts: the first k CTAs to arrive on an SM take whole tiles, the
+// others take quarter tiles (each falls back to the other pool when its own is
+// empty; there are exactly as many CTAs as units).  1 and 4 lanes per channel
+// give identical bits, so the outcome does not depend on the assignment.
+struct MixSched {
+  int k;               // one-lane CTAs per SM
+  int n_tiles;         // whole tiles for CfgA: tiles 0 .. n_tiles - 1 (b-major)
+  int n_quarters;      // quarter tiles for CfgB: quarters of tiles n_tiles .. T - 1
+  int dtiles128;       // 128-channel tiles per batch row
+  unsigned* counters;  // [0] next whole tile, [1] next quarter, [2 + smid] arrivals
+  unsigned max_sm_slots;  // SM ids with an arrival counter
+};
+
+template <typename IO, typename CfgA, typename CfgB>
+__global__ void __launch_bounds__(CfgA::THREADS)
+    scan_channel_mixed_kernel(const __grid_constant__ ChanMaps mapsA,
+                              const __grid_constant__ ChanMaps mapsB, const ScanParams p,
+                              const MixSched m) {
+  static_assert(CfgA::THREADS == CfgB::THREADS, "one block shape for both roles");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int role_unit[2];
+  if (threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const int arrival = (smid < m.max_sm_slots)
+                            ? static_cast<int>(atomicAdd(&m.counters[2 + smid], 1u))
+                            : m.k;  // no counter for this SM: take quarter tiles
+    int role = -1, unit = 0;
+    if (arrival < m.k) {
+      const int t = static_cast<int>(atomicAdd(&m.counters[0], 1u));
+      if (t < m.n_tiles) role = 0, unit = t;
+    }
+    if (role < 0) {
+      const int q = static_cast<int>(atomicAdd(&m.counters[1], 1u));
+      if (q < m.n_quarters) role = 1, unit = q;
+    }
+    if (role < 0) {
+      const int t = static_cast<int>(atomicAdd(&m.counters[0], 1u));
+      if (t < m.n_tiles) role = 0, unit = t;
+    }
+    role_unit[0] = role;
+    role_unit[1] = unit;
+  }
+  __syncthreads();
+  const int role = role_unit[0], unit = role_unit[1];
+  if (role == 0) {
+    channel_body<IO, CfgA, kModeFull>(mapsA, p, unit / m.dtiles128, (unit % m.dtiles128) * 128,
+                                      0, smem_raw);
+  } else if (role == 1) {
+    const int tile = m.n_tiles + unit / 4;
+    const int d0 = (tile % m.dtiles128) * 128 + (unit % 4) * 32;
+    if (d0 < p.dim) channel_body<IO, CfgB, kModeFull>(mapsB, p, tile / m.dtiles128, d0, 0, smem_raw);
   }
 }
 

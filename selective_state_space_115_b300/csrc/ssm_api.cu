@@ -315,7 +315,7 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
 // relative costs below were measured on B300 with the 2.8B-like layer (bf16,
 // dstate 16, L 2048): one warp of NS = 16 / 8 / 4 states costs 1 / 0.58 / 0.37
 // when sub-partitions are full, and a lone warp takes 1.78 / 1.6 / 1.2.
-int choose_lpc(int64_t batch, int64_t dim, int64_t dstate) {
+int choose_lpc(int64_t batch, int64_t dim, int64_t dstate, double* cost_out = nullptr) {
   const int64_t sms = sm_count();
   int best = 1;
   double best_cost = 0.0;
@@ -333,7 +333,87 @@ int choose_lpc(int64_t batch, int64_t dim, int64_t dstate) {
       best_cost = cost;
     }
   }
+  if (cost_out) *cost_out = best_cost;
   return best;
+}
+
+// Mixed split (dstate 16): k = floor(T / SMs) one-lane CTAs per SM for T 128-channel
+// tiles, the remaining tiles as 32-channel four-lane CTAs.  In the units of the model
+// above its busiest sub-partition costs k x 1 + ceil(quarters / SMs) x 0.37.
+// Scheduler counters live in the workspace after the status words.
+constexpr size_t kMixCounterBytes = 1280;  // [2 + SMs] unsigned, up to 318 SMs
+constexpr int kMixMaxSms = 318;
+
+struct MixPlan {
+  bool use = false;
+  int k = 0, n_tiles = 0, n_quarters = 0, dtiles128 = 0;
+};
+
+MixPlan mix_plan(int64_t batch, int64_t dim) {
+  MixPlan m;
+  const int64_t sms = sm_count();
+  const int64_t dt = (dim + 127) / 128;
+  const int64_t tiles = batch * dt;
+  if (sms > kMixMaxSms || tiles * 4 > INT32_MAX) return m;
+  m.k = static_cast<int>(tiles / sms);
+  if (m.k > 2) m.k = 2;  // three 66 KB CTAs fill an SM's shared memory
+  m.n_tiles = static_cast<int>(m.k * sms);
+  m.n_quarters = static_cast<int>((tiles - m.n_tiles) * 4);
+  m.dtiles128 = static_cast<int>(dt);
+  m.use = true;
+  return m;
+}
+
+double mix_cost(const MixPlan& m) {
+  const int64_t sms = sm_count();
+  return m.k * 1.0 + double((m.n_quarters + sms - 1) / sms) * 0.37;
+}
+
+template <typename IO, bool GATE>
+ssm_status launch_mixed(const ScanCall& c, void* workspace, cudaStream_t stream,
+                        const MixPlan& m) {
+  using CfgA = ChanCfg<IO, 16, GATE, 1, ChanShape<1>::S, ChanShape<1>::RB>;
+  using CfgB = ChanCfg<IO, 16, GATE, 4, ChanShape<4>::S, ChanShape<4>::RB>;
+  static_assert(CfgA::LC == CfgB::LC, "one chunk width for both roles");
+  ChanMaps ma, mb;
+  std::memset(&ma, 0, sizeof(ma));
+  std::memset(&mb, 0, sizeof(mb));
+  const bool bf = c.bf16;
+  const uint64_t L = c.seqlen, Dm = c.dim, Bt = c.batch, Nn = 16;
+  bool ok = true;
+  for (int r = 0; r < 2 && ok; ++r) {
+    ChanMaps& mp = r ? mb : ma;
+    const uint32_t rows = r ? CfgB::DT : CfgA::DT;
+    ok = make_map(&mp.u, c.u, bf, L, Dm, Bt, CfgA::LC, rows) &&
+         make_map(&mp.delta, c.delta, bf, L, Dm, Bt, CfgA::LC, rows) &&
+         make_map(&mp.y, c.y, bf, L, Dm, Bt, CfgA::LC, rows) &&
+         make_map(&mp.B, c.B, bf, L, Nn, Bt, CfgA::LC, 16) &&
+         make_map(&mp.C, c.C, bf, L, Nn, Bt, CfgA::LC, 16) &&
+         (!GATE || make_map(&mp.z, c.z, bf, L, Dm, Bt, CfgA::LC, rows));
+  }
+  if (!ok) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled failed";
+    return SSM_ERR_CUDA;
+  }
+  ScanParams p = make_params(c, workspace);
+  ssm::MixSched sched;
+  sched.k = m.k;
+  sched.n_tiles = m.n_tiles;
+  sched.n_quarters = m.n_quarters;
+  sched.dtiles128 = m.dtiles128;
+  sched.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  sched.max_sm_slots = static_cast<unsigned>(kMixCounterBytes / sizeof(unsigned) - 2);
+  cudaError_t e = cudaMemsetAsync(sched.counters, 0, kMixCounterBytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scheduler counters)");
+  constexpr int smem = CfgA::SMEM_ALLOC > CfgB::SMEM_ALLOC ? CfgA::SMEM_ALLOC : CfgB::SMEM_ALLOC;
+  auto kern = ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel_mixed)");
+  const unsigned grid = static_cast<unsigned>(m.n_tiles + m.n_quarters);
+  kern<<<grid, CfgA::THREADS, smem, stream>>>(ma, mb, p, sched);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "scan_channel_mixed launch");
+  return SSM_OK;
 }
 
 template <typename IO, int N, bool GATE, bool VEC>
@@ -360,8 +440,12 @@ ssm_status launch_channel_lpc(const ScanCall& c, void* ws, cudaStream_t s) {
 
 template <typename IO, int N>
 ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s,
-                           const SegPlan& seg) {
+                           const SegPlan& seg, const MixPlan& mix) {
   const bool gate = c.z != nullptr;
+  if constexpr (N == 16) {
+    if (algo == SSM_ALGO_CHANNEL_MIXED)
+      return gate ? launch_mixed<IO, true>(c, ws, s, mix) : launch_mixed<IO, false>(c, ws, s, mix);
+  }
   if (algo == SSM_ALGO_SEGMENTED) {
     return gate ? launch_channel<IO, N, true, 1>(c, ws, s, seg)
                 : launch_channel<IO, N, false, 1>(c, ws, s, seg);
@@ -383,11 +467,11 @@ ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStrea
 
 template <typename IO>
 ssm_status dispatch_scan(const ScanCall& c, ssm_algo algo, void* ws, cudaStream_t s,
-                         const SegPlan& seg) {
+                         const SegPlan& seg, const MixPlan& mix) {
   switch (c.dstate) {
-    case 4: return dispatch_scan_n<IO, 4>(c, algo, ws, s, seg);
-    case 8: return dispatch_scan_n<IO, 8>(c, algo, ws, s, seg);
-    case 16: return dispatch_scan_n<IO, 16>(c, algo, ws, s, seg);
+    case 4: return dispatch_scan_n<IO, 4>(c, algo, ws, s, seg, mix);
+    case 8: return dispatch_scan_n<IO, 8>(c, algo, ws, s, seg, mix);
+    case 16: return dispatch_scan_n<IO, 16>(c, algo, ws, s, seg, mix);
     default: return SSM_ERR_UNSUPPORTED;
   }
 }
@@ -480,11 +564,15 @@ size_t ssm_scan_fwd_algo_workspace_size(int64_t batch, int64_t dim, int64_t dsta
   if (batch > (int64_t(1) << 62) / dim / seqlen) return kWorkspaceBytes;
   // the segmented plan for fp32 (8-position chunks); bf16's 16-position chunks never
   // need more segments
+  // the mixed split keeps scheduler counters after the status words
+  const bool many = batch * dim >= kChannelKernelMinChannels;
+  if (algo == SSM_ALGO_CHANNEL_MIXED ||
+      (dstate == 16 && (algo == SSM_ALGO_CHANNEL || (algo == SSM_ALGO_AUTO && many))))
+    return kStatusBytes + kMixCounterBytes;
   SegPlan pl;
   if (algo == SSM_ALGO_SEGMENTED)
     pl = seg_plan(batch, dim, seqlen, 8, true);
-  else if (algo == SSM_ALGO_AUTO && batch * dim < kChannelKernelMinChannels &&
-           seqlen >= kSegMinSeqlen)
+  else if (algo == SSM_ALGO_AUTO && !many && seqlen >= kSegMinSeqlen)
     pl = seg_plan(batch, dim, seqlen, 8, false);
   return seg_workspace_bytes(batch, dim, dstate, pl);
 }
@@ -501,7 +589,7 @@ ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t
                              size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream) {
   if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_CHANNEL && algo != SSM_ALGO_CHUNK &&
       algo != SSM_ALGO_CHANNEL_L1 && algo != SSM_ALGO_CHANNEL_L2 && algo != SSM_ALGO_CHANNEL_L4 &&
-      algo != SSM_ALGO_SEGMENTED)
+      algo != SSM_ALGO_SEGMENTED && algo != SSM_ALGO_CHANNEL_MIXED)
     return SSM_ERR_UNSUPPORTED;
   if ((algo == SSM_ALGO_CHANNEL_L2 && dstate < 8) || (algo == SSM_ALGO_CHANNEL_L4 && dstate < 16))
     return SSM_ERR_UNSUPPORTED;
@@ -554,12 +642,34 @@ ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t
     }
   }
   if (algo != SSM_ALGO_CHUNK && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;  // TMA kernels only
+  // the channel kernel with the split chosen per size: one split for every CTA, or
+  // (dstate 16) the mixed launch when its model cost is lower and the workspace
+  // holds its scheduler counters
+  MixPlan mix;
+  if (algo == SSM_ALGO_CHANNEL_MIXED) {
+    mix = mix_plan(c.batch, c.dim);
+    if (c.dstate != 16 || !mix.use) {
+      algo = SSM_ALGO_CHANNEL;
+    } else if (workspace_bytes < kStatusBytes + kMixCounterBytes) {
+      g_last_cuda_error = "workspace smaller than ssm_scan_fwd_algo_workspace_size()";
+      return SSM_ERR_INVALID_ARG;
+    }
+  } else if (algo == SSM_ALGO_CHANNEL && c.dstate == 16 &&
+             workspace_bytes >= kStatusBytes + kMixCounterBytes) {
+    double split_cost = 0.0;
+    choose_lpc(c.batch, c.dim, c.dstate, &split_cost);
+    const MixPlan m = mix_plan(c.batch, c.dim);
+    if (m.use && m.k >= 1 && m.n_quarters > 0 && mix_cost(m) < split_cost) {
+      mix = m;
+      algo = SSM_ALGO_CHANNEL_MIXED;
+    }
+  }
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(ssm::DeviceStatus), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
-  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s, seg)
-                : dispatch_scan<float>(c, algo, workspace, s, seg);
+  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s, seg, mix)
+                : dispatch_scan<float>(c, algo, workspace, s, seg, mix);
 }
 
 ssm_status ssm_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ssm_dtype io,

@@ -56,7 +56,9 @@ def test_workspace_size_follows_the_plan():
     library assumes 148 SMs)."""
     lib = binding.library()
     ws = lib.ssm_scan_fwd_workspace_size
-    assert ws(8, 5120, 16, 2048) == 256        # 40960 channels: channel kernel, no split
+    # 40960 channels: channel kernel, no split; room for the mixed launch's counters
+    assert ws(8, 5120, 16, 2048) == 256 + 1280
+    assert ws(8, 5120, 8, 2048) == 256         # the mixed launch is dstate 16 only
     assert ws(2, 1536, 16, 2048) == 256        # few channels, short: lanes over positions
     # 1536 channels x 131072: 12 CTAs of 128 channels -> 444 // 12 = 37 segments
     assert ws(1, 1536, 16, 131072) == _seg_bytes(1536, 16, 37)
@@ -67,6 +69,7 @@ def test_workspace_size_follows_the_plan():
     assert algo_ws(1, 1536, 16, 131072, binding.ALGO_AUTO) == ws(1, 1536, 16, 131072)
     assert algo_ws(1, 1536, 16, 131072, binding.ALGO_CHUNK) == 256
     assert algo_ws(8, 5120, 16, 2048, binding.ALGO_CHANNEL_L2) == 256
+    assert algo_ws(2, 64, 16, 2048, binding.ALGO_CHANNEL_MIXED) == 256 + 1280
     # an explicit split asks for at least two segments even when channels are many
     assert algo_ws(8, 5120, 16, 2048, binding.ALGO_SEGMENTED) == _seg_bytes(40960, 16, 2)
     # too short to split (under two 8-position chunks): status words only

@@ -15,9 +15,9 @@ from selective_state_space_115_b300 import workloads as W
 from tests.helpers import TOL, from_torch, rel_err, sample_rows, torch_f32, torch_io
 
 pytestmark = pytest.mark.gpu
-ALGOS = ["channel_l1", "channel_l2", "channel_l4", "chunk", "segmented"]
+ALGOS = ["channel_l1", "channel_l2", "channel_l4", "channel_mixed", "chunk", "segmented"]
 FULL_ALGOS = ALGOS + ["auto"]
-MIN_DSTATE = {"channel_l2": 8, "channel_l4": 16}
+MIN_DSTATE = {"channel_l2": 8, "channel_l4": 16, "channel_mixed": 16}
 NTHREADS = os.cpu_count() or 1
 _ORACLE_CACHE = {}
 _INPUT_CACHE = {}
@@ -326,6 +326,23 @@ def test_lane_splits_are_bit_identical(io, dstate):
         assert np.array_equal(y, outs[0][1]), algo
         assert np.array_equal(hl, outs[0][2]), algo
     assert rel_err(outs[0][1], oracle_full(x, io)) <= TOL[io]
+
+
+def test_mixed_split_matches_one_lane_bit_for_bit():
+    """150 tiles of 128 channels on a 148-SM B300: one one-lane CTA per SM plus 2
+    tiles run as eight 32-channel four-lane CTAs; the roles are taken at run time,
+    and the result equals the one-lane-per-channel launch bit for bit."""
+    io = W.BF16
+    cfg = W.ScanConfig("t", 2, 9600, 16, 256, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=29, with_h0=True)
+    ym, hm = gpu_scan(x, io, "channel_mixed", return_last_state=True)
+    y1, h1 = gpu_scan(x, io, "channel_l1", return_last_state=True)
+    assert np.array_equal(from_torch(ym), from_torch(y1))
+    assert np.array_equal(from_torch(hm), from_torch(h1))
+    rows = np.array([0, 127, 128, 9599, 9600 + 9471, 9600 + 9472, 2 * 9600 - 1], dtype=np.int64)
+    ref = oracle_rows(x, io, rows)
+    assert rel_err(from_torch(ym).reshape(-1, cfg.seqlen)[rows], ref) <= TOL[io]
 
 
 def test_auto_matches_explicit_choice():
