@@ -38,6 +38,7 @@ from selective_state_space_115_b300 import workloads as W  # noqa: E402
 METRIC = "selective-scan elements/s (B·D·L) and achieved HBM GB/s vs B300 roofline"
 CFG = W.SCAN_CONFIGS["2p8b"]
 DEC = W.DECODE_CONFIGS["decode"]
+DECODE_STEPS = DEC.steps
 SM_COUNT = 148
 SM_MAX_MHZ = 2032.0
 EX2_PER_CLK_SM = 32          # measured on this machine's B300 (ex2.approx.ftz.f32 throughput)
@@ -259,12 +260,18 @@ def run_reference(args):
 
 
 def bench_config(impl_note: str):
-    return {"workload": "Mamba-2.8B-like selective scan: bf16 io, fp32 state, batch 8, dim 5120, "
-                        "dstate 16, seqlen 2048, silu(z) gate, dt bias = inverse softplus of "
-                        "log-uniform dt, A[d,n] = -(n+1), D ~ N(0,1)",
-            "batch": CFG.batch, "dim": CFG.dim, "dstate": CFG.dstate, "seqlen": CFG.seqlen,
-            "io": "bf16", "impl": impl_note,
-            "l2": "inputs larger than L2 (672 MB per step vs 126 MB L2); no flush",
+    io = "bf16" if CFG.io == W.BF16 else "fp32"
+    names = {"2p8b": "Mamba-2.8B-like", "130m": "Mamba-130M-like", "long": "long-sequence",
+             "tiny": "tiny"}
+    gate = "silu(z) gate" if CFG.gate else "no gate"
+    desc = (f"{names.get(CFG.name, CFG.name)} selective scan: {io} io, fp32 state, batch "
+            f"{CFG.batch}, dim {CFG.dim}, dstate {CFG.dstate}, seqlen {CFG.seqlen}, {gate}, "
+            f"dt bias = inverse softplus of log-uniform dt, A[d,n] = -(n+1), D ~ N(0,1)")
+    mb = scan_bytes(CFG) / 1e6
+    l2 = (f"inputs larger than L2 ({mb:.0f} MB per step vs 126 MB L2); no flush" if mb > 126
+          else f"inputs ({mb:.0f} MB) fit in the 126 MB L2: unflushed, L2-warm")
+    return {"workload": desc, "batch": CFG.batch, "dim": CFG.dim, "dstate": CFG.dstate,
+            "seqlen": CFG.seqlen, "io": io, "impl": impl_note, "l2": l2,
             "parallelism": "one independent problem per GPU (weak scaling)"}
 
 
@@ -346,15 +353,15 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers
     e2e_steps = max(3, min(20, args.steps))
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    pin = lambda t: None if t is None else t.cpu().pin_memory()  # noqa: E731
     hu, hd, hz, hB, hC = pin(u), pin(dl), pin(z), pin(B), pin(C)
     hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hu, hd, hz, hB, hC))
+    h2d = sum(t.numel() * t.element_size() for t in (hu, hd, hz, hB, hC) if t is not None)
     d2h = hy.numel() * hy.element_size()
 
     def e2e_step():
-        du, dd, dz = hu.to(dev, non_blocking=True), hd.to(dev, non_blocking=True), \
-            hz.to(dev, non_blocking=True)
+        du, dd = hu.to(dev, non_blocking=True), hd.to(dev, non_blocking=True)
+        dz = None if hz is None else hz.to(dev, non_blocking=True)
         dB, dC = hB.to(dev, non_blocking=True), hC.to(dev, non_blocking=True)
         yy = S.scan_fwd(du, dd, A, dB, dC, D=Dv, z=dz, delta_bias=bias, algo=args.algo)
         hy.copy_(yy, non_blocking=True)
@@ -427,7 +434,7 @@ def run_decode(dev, S):
     A = torch.from_numpy(static["A"]).to(dev)
     Dv = torch.from_numpy(static["D"]).to(dev)
     bias = torch.from_numpy(static["delta_bias"]).to(dev)
-    steps = cfg.steps
+    steps = DECODE_STEPS
     bd = (steps, cfg.batch, cfg.dim)
     bn = (steps, cfg.batch, cfg.dstate)
     u = torch.randn(bd, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
@@ -475,8 +482,8 @@ def run_decode(dev, S):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     nb = decode_bytes(cfg)
     best = ms_plain if not isinstance(ms_graph, float) else min(ms_plain, ms_graph)
-    return {"workload": "decode: batch 256, dim 5120, dstate 16, bf16 io, fp32 state, "
-                        "1024 sequential steps, h in place",
+    return {"workload": f"decode: batch 256, dim 5120, dstate 16, bf16 io, fp32 state, "
+                        f"{steps} sequential steps, h in place",
             "ms_per_step_plain": ms_plain, "ms_per_step_graph": ms_graph,
             "bytes_per_step": nb, "gpu_launches": 2 * steps,
             "roofline": {"bound": "hbm", "achieved": nb / (best * 1e-3) / 1e9,
@@ -500,14 +507,31 @@ def main():
                     help="scan kernel family (default: the library's own choice)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch of the scan workload (smaller cases for ncu)")
+    ap.add_argument("--workload", default="2p8b", choices=sorted(W.SCAN_CONFIGS),
+                    help="scan workload (profiling of the other configurations; the bench "
+                         "line is quoted on 2p8b)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the decode loop and print its JSON (profiling)")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="decode loop length (default 1024; fewer for ncu)")
     args = ap.parse_args()
+    global CFG, DECODE_STEPS
+    CFG = W.SCAN_CONFIGS[args.workload]
     if args.batch:
-        global CFG
         CFG = dataclasses.replace(CFG, batch=args.batch)
+    if args.decode_steps:
+        DECODE_STEPS = args.decode_steps
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.decode_only:
+        import torch
+        from selective_state_space_115_b300 import binding as S
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(run_decode(dev, S)), flush=True)
+        return 0
     return run_gpu(args)
 
 
