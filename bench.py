@@ -91,6 +91,8 @@ def source_sha(kernel: str) -> str:
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
     current kernel sources (else None)."""
+    if kernel not in KERNEL_SOURCES:
+        return None
     path = os.path.join(ROOT, "profiles", f"{kernel}.md")
     try:
         text = open(path).read()
@@ -349,7 +351,8 @@ def run_gpu(args):
     bytes_step = scan_bytes(CFG)
     ex2_peak = EX2_PER_CLK_SM * SM_COUNT * SM_MAX_MHZ * 1e6 / 1e12   # Texp/s
     achieved_exp = CFG.updates / (dev_ms / args.steps * 1e-3) / 1e12
-    traffic = profiled_traffic("scan_channel_2p8b")
+    traffic = profiled_traffic({"2p8b": "scan_channel_2p8b", "long": "scan_channel_long"}.get(
+        CFG.name, ""))
 
     # ---- end to end through the public API with host buffers
     e2e_steps = max(3, min(20, args.steps))
@@ -488,7 +491,8 @@ def run_decode(dev, S):
             "bytes_per_step": nb, "gpu_launches": 2 * steps,
             "roofline": {"bound": "hbm", "achieved": nb / (best * 1e-3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s",
-                         "frac": nb / (best * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+                         "frac": nb / (best * 1e-3) / 1e9 / hbm_peak,
+                         "traffic": profiled_traffic("state_update_decode"),
                          "peak_kind": kind,
                          "note": "h (84 MB) fits in L2, so DRAM bytes can be below the "
                                  "algorithmic bytes"}}
