@@ -62,6 +62,12 @@ def _ptr(x: Optional[np.ndarray]):
     return x.ctypes.data_as(_dp)
 
 
+def _euler(discretization: str) -> int:
+    if discretization not in ("zoh", "euler"):
+        raise ValueError(f"unknown discretization {discretization!r}")
+    return int(discretization == "euler")
+
+
 class Oracle:
     """ctypes view of one compiled oracle library."""
 
@@ -69,22 +75,26 @@ class Oracle:
         lib = ctypes.CDLL(path)
         lib.oracle_scan_fwd.restype = ctypes.c_int
         lib.oracle_scan_fwd.argtypes = [_i64, _i64, _i64, _i64, _dp, _dp, _dp, ctypes.c_int,
-                                        _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+                                        _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int,
+                                        ctypes.c_int]
         lib.oracle_scan_rows.restype = ctypes.c_int
         lib.oracle_scan_rows.argtypes = [_i64, _i64, _i64, _i64,
                                          ctypes.POINTER(ctypes.c_int64), _i64,
                                          _dp, _dp, _dp, ctypes.c_int, _dp, _dp, _dp, _dp,
-                                         _dp, _dp, _dp, _dp]
+                                         _dp, _dp, _dp, _dp, ctypes.c_int]
         lib.oracle_state_update.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [_i64, _i64, _i64, _dp, _dp, _dp, _dp,
-                                            ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp]
+                                            ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp,
+                                            ctypes.c_int]
         self.lib = lib
         self.path = path
 
     def scan_fwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                 delta_softplus=True, h0=None, return_last_state=False, nthreads: int = 1):
+                 delta_softplus=True, h0=None, return_last_state=False, nthreads: int = 1,
+                 discretization: str = "zoh"):
         """Selective scan in fp64.  u, delta, z [b,d,l]; B, C [b,n,l]; A [d,n];
-        D, delta_bias [d]; h0 [b,d,n].  Returns y [b,d,l] (and h_last [b,d,n])."""
+        D, delta_bias [d]; h0 [b,d,n].  Returns y [b,d,l] (and h_last [b,d,n]).
+        discretization: "zoh" (Bbar = (Abar - 1) / A * B) or "euler" (Bbar = dt * B)."""
         u, delta, A, B, C = (_f64(a) for a in (u, delta, A, B, C))
         D, z, delta_bias, h0 = (_f64(a) for a in (D, z, delta_bias, h0))
         batch, dim, seqlen = u.shape
@@ -97,14 +107,15 @@ class Oracle:
         rc = self.lib.oracle_scan_fwd(batch, dim, dstate, seqlen, _ptr(u), _ptr(delta),
                                       _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
                                       _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(h0),
-                                      _ptr(h_last), _ptr(y), int(nthreads))
+                                      _ptr(h_last), _ptr(y), int(nthreads),
+                                      _euler(discretization))
         if rc != 0:
             raise RuntimeError("oracle_scan_fwd failed")
         return (y, h_last) if return_last_state else y
 
     def scan_rows(self, rows: Sequence[int], u_rows, delta_rows, A, B, C, batch: int, dim: int,
                   D=None, z_rows=None, delta_bias=None, delta_softplus=True, h0=None,
-                  return_last_state=False):
+                  return_last_state=False, discretization: str = "zoh"):
         """Scan only the listed rows (row = b*dim + d).  u_rows, delta_rows, z_rows
         are the [nrows, L] slices of those rows; B, C are the full [b,n,l]."""
         rows = np.ascontiguousarray(rows, dtype=np.int64)
@@ -118,13 +129,14 @@ class Oracle:
                                        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), nrows,
                                        _ptr(u_rows), _ptr(delta_rows), _ptr(delta_bias),
                                        int(bool(delta_softplus)), _ptr(A), _ptr(B), _ptr(C),
-                                       _ptr(D), _ptr(z_rows), _ptr(h0), _ptr(h_last), _ptr(y))
+                                       _ptr(D), _ptr(z_rows), _ptr(h0), _ptr(h_last), _ptr(y),
+                                       _euler(discretization))
         if rc != 0:
             raise RuntimeError("oracle_scan_rows failed")
         return (y, h_last) if return_last_state else y
 
     def state_update(self, h, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                     delta_softplus=True):
+                     delta_softplus=True, discretization: str = "zoh"):
         """One decode step in fp64.  h [b,d,n] (copied, not modified); u, delta, z [b,d];
         B, C [b,n].  Returns (y [b,d], h_new [b,d,n])."""
         h = np.array(h, dtype=np.float64, copy=True, order="C")
@@ -136,7 +148,8 @@ class Oracle:
         y = np.empty_like(u)
         rc = self.lib.oracle_state_update(batch, dim, dstate, _ptr(h), _ptr(u), _ptr(delta),
                                           _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
-                                          _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y))
+                                          _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
+                                          _euler(discretization))
         if rc != 0:
             raise RuntimeError("oracle_state_update failed")
         return y, h

@@ -16,6 +16,7 @@
  *       for n:
  *         Abar  = exp(dt * A[d,n])
  *         coef  = (exp(dt*A) - 1) / A[d,n]      (coef = dt when A[d,n] == 0)
+ *                 (coef = dt for every n with the Euler input term, `euler`)
  *         h[n]  = Abar * h[n] + coef * B[b,n,l] * u[b,d,l]
  *       y     = sum_n C[b,n,l] * h[n] + D[d] * u[b,d,l]
  *       y    *= silu(z[b,d,l])                  (when z is given)
@@ -41,6 +42,9 @@
  *    starts from torch.zeros) and "mamba 学习" (h_0 = 0).
  *  - decode step: Mamba_Model_Report.md section 6 (ssm_step: h = deltaA * h + BX;
  *    y = h @ C + D * x), with the same discretisation.
+ *  - Euler input term Bbar = dt * B (selected by `euler`): Mamba_Model_Report.md
+ *    section 4.2 (selective_scan: deltaB = delta * B, BX = deltaB * x), with the
+ *    same Abar = exp(dt * A).
  *
  * Pinned by tests/test_oracle_pins.py against brute-force unrolled sums,
  * the LTI convolution form, a geometric-series closed form, the A -> 0 limit,
@@ -75,7 +79,7 @@ static double oracle_silu(double z)
 static double oracle_step(int64_t dstate, double* h, double u, double delta_raw,
                           double bias, int delta_softplus, const double* A_row,
                           const double* B_col, const double* C_col, int64_t bc_stride,
-                          double Dd, const double* z)
+                          double Dd, const double* z, int euler)
 {
     double x = delta_raw + bias;
     double dt = delta_softplus ? oracle_softplus(x) : x;
@@ -84,6 +88,8 @@ static double oracle_step(int64_t dstate, double* h, double u, double delta_raw,
         double a = A_row[n];
         double Abar = exp(dt * a);
         double coef = (a == 0.0) ? dt : expm1(dt * a) / a;
+        if (euler)
+            coef = dt;
         h[n] = Abar * h[n] + coef * B_col[n * bc_stride] * u;
         acc += C_col[n * bc_stride] * h[n];
     }
@@ -98,7 +104,7 @@ static void oracle_scan_row(int64_t b, int64_t d, int64_t dim, int64_t dstate, i
                             const double* u, const double* delta, const double* delta_bias,
                             int delta_softplus, const double* A, const double* B,
                             const double* C, const double* D, const double* z,
-                            const double* h0, double* h_last, double* y, double* h)
+                            const double* h0, double* h_last, double* y, double* h, int euler)
 {
     const int64_t row = b * dim + d;
     for (int64_t n = 0; n < dstate; ++n)
@@ -110,7 +116,7 @@ static void oracle_scan_row(int64_t b, int64_t d, int64_t dim, int64_t dstate, i
         const double* Bcol = B + b * dstate * seqlen + l;
         const double* Ccol = C + b * dstate * seqlen + l;
         y[i] = oracle_step(dstate, h, u[i], delta[i], bias, delta_softplus, A + d * dstate,
-                           Bcol, Ccol, seqlen, Dd, z ? z + i : NULL);
+                           Bcol, Ccol, seqlen, Dd, z ? z + i : NULL, euler);
     }
     if (h_last)
         for (int64_t n = 0; n < dstate; ++n)
@@ -124,7 +130,7 @@ int oracle_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                     const double* u, const double* delta, const double* delta_bias,
                     int delta_softplus, const double* A, const double* B, const double* C,
                     const double* D, const double* z, const double* h0, double* h_last,
-                    double* y, int nthreads)
+                    double* y, int nthreads, int euler)
 {
     if (batch < 0 || dim < 0 || dstate <= 0 || seqlen < 0)
         return -1;
@@ -145,7 +151,7 @@ int oracle_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
 #endif
             for (int64_t r = 0; r < rows; ++r)
                 oracle_scan_row(r / dim, r % dim, dim, dstate, seqlen, u, delta, delta_bias,
-                                delta_softplus, A, B, C, D, z, h0, h_last, y, h);
+                                delta_softplus, A, B, C, D, z, h0, h_last, y, h, euler);
             free(h);
         }
     }
@@ -161,7 +167,7 @@ int oracle_scan_rows(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                      const double* u_rows, const double* delta_rows, const double* delta_bias,
                      int delta_softplus, const double* A, const double* B, const double* C,
                      const double* D, const double* z_rows, const double* h0,
-                     double* h_last_rows, double* y_rows)
+                     double* h_last_rows, double* y_rows, int euler)
 {
     if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || nrows < 0)
         return -1;
@@ -184,7 +190,7 @@ int oracle_scan_rows(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
             y_rows[i] = oracle_step(dstate, h, u_rows[i], delta_rows[i], bias, delta_softplus,
                                     A + d * dstate, B + b * dstate * seqlen + l,
                                     C + b * dstate * seqlen + l, seqlen, Dd,
-                                    z_rows ? z_rows + i : NULL);
+                                    z_rows ? z_rows + i : NULL, euler);
         }
         if (h_last_rows)
             for (int64_t n = 0; n < dstate; ++n)
@@ -199,7 +205,7 @@ int oracle_scan_rows(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
 int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double* h,
                         const double* u, const double* delta, const double* delta_bias,
                         int delta_softplus, const double* A, const double* B, const double* C,
-                        const double* D, const double* z, double* y)
+                        const double* D, const double* z, double* y, int euler)
 {
     if (batch < 0 || dim < 0 || dstate <= 0)
         return -1;
@@ -209,7 +215,7 @@ int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double* h,
             y[i] = oracle_step(dstate, h + i * dstate, u[i], delta[i],
                                delta_bias ? delta_bias[d] : 0.0, delta_softplus,
                                A + d * dstate, B + b * dstate, C + b * dstate, 1,
-                               D ? D[d] : 0.0, z ? z + i : NULL);
+                               D ? D[d] : 0.0, z ? z + i : NULL, euler);
         }
     }
     return 0;

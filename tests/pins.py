@@ -23,6 +23,8 @@ Sources of each fact:
     "mamba 学习", section "SSM 状态空间模型"; gate y * silu(z):
     Mamba_Model_Report.md, section 3 (MambaBlock.forward).
   * single-token step equals the scan: Mamba_Model_Report.md, section 6.
+  * Euler input term Bbar = delta * B with the same Abar = exp(delta A):
+    Mamba_Model_Report.md, section 4.2 (selective_scan: deltaB = delta * B).
 """
 from __future__ import annotations
 
@@ -79,7 +81,7 @@ def pin_zoh_matches_ode(orc):
 # ---------------------------------------------------------------------------
 # 2. brute-force unrolled sum (no loop-carried state)
 # ---------------------------------------------------------------------------
-def _unrolled(u, dt, A, B, C, D, h0):
+def _unrolled(u, dt, A, B, C, D, h0, euler=False):
     """y_k = sum_n C[n,k] (prod_{i<=k} Abar_i h0 + sum_{j<=k} prod_{j<i<=k} Abar_i Bbar_j u_j) + D u_k"""
     L = u.shape[0]
     n = A.shape[0]
@@ -87,6 +89,8 @@ def _unrolled(u, dt, A, B, C, D, h0):
     with np.errstate(divide="ignore", invalid="ignore"):
         coef = np.where(A[None, :] == 0.0, dt[:, None],
                         np.expm1(dt[:, None] * A[None, :]) / A[None, :])
+    if euler:
+        coef = np.broadcast_to(dt[:, None], (L, n))
     Bbar_u = coef * B.T * u[:, None]                                # [L, n]
     y = np.empty(L)
     for k in range(L):
@@ -290,6 +294,63 @@ def pin_rows_match_full(orc):
     _close(hr, hl.reshape(b * d, n)[rows], rtol=0, atol=0, what="scan_rows h_last")
 
 
+# ---------------------------------------------------------------------------
+# 10. the Euler input term (Bbar = dt B, Abar unchanged)
+# ---------------------------------------------------------------------------
+def pin_euler_unrolled_sum(orc):
+    """Brute-force unrolled sum with Bbar_j = dt_j B_j, through the scan and the
+    decode step (no loop-carried state in the reference)."""
+    rng = _rng(11)
+    b, d, n, L = 1, 3, 4, 29
+    u = rng.standard_normal((b, d, L))
+    raw = rng.standard_normal((b, d, L))
+    bias = rng.uniform(-3.0, 0.5, size=d)
+    A = -rng.uniform(0.2, 4.0, size=(d, n))
+    A[2, 1] = 0.0
+    B = rng.standard_normal((b, n, L))
+    C = rng.standard_normal((b, n, L))
+    D = rng.standard_normal(d)
+    h0 = rng.standard_normal((b, d, n))
+    y = orc.scan_fwd(u, raw, A, B, C, D=D, delta_bias=bias, h0=h0, discretization="euler")
+    h = h0.copy()
+    for l in range(L):
+        yl, h = orc.state_update(h, u[:, :, l], raw[:, :, l], A, B[:, :, l], C[:, :, l], D=D,
+                                 delta_bias=bias, discretization="euler")
+        _close(yl, y[:, :, l], rtol=1e-13, atol=1e-14, what=f"euler step {l} vs scan")
+    for di in range(d):
+        x = raw[0, di] + bias[di]
+        dt = np.log1p(np.exp(-np.abs(x))) + np.maximum(x, 0.0)
+        y_ref = _unrolled(u[0, di], dt, A[di], B[0], C[0], D[di], h0[0, di], euler=True)
+        _close(y[0, di], y_ref, rtol=1e-11, atol=1e-12, what=f"euler unrolled sum (0,{di})")
+
+
+def pin_euler_geometric_and_first_order(orc):
+    """N = 1, x = 1, constant parameters: h_k = dt B (1 - Abar^{k+1}) / (1 - Abar).
+    One step from h = 0: ZOH minus Euler is (expm1(q)/q - 1) dt B u = (q/2 + q^2/6 +
+    ...) dt B u, q = dt A (both input terms pinned against each other)."""
+    L = 40
+    for a, dt, bval in [(-1.0, 0.1, 1.0), (-2.5, 0.37, -0.7)]:
+        A = np.array([[a]])
+        y = orc.scan_fwd(np.ones((1, 1, L)), np.full((1, 1, L), dt), A,
+                         np.full((1, 1, L), bval), np.ones((1, 1, L)), delta_softplus=False,
+                         discretization="euler")[0, 0]
+        Abar = math.exp(a * dt)
+        k = np.arange(L)
+        _close(y, dt * bval * (1.0 - Abar ** (k + 1)) / (1.0 - Abar), rtol=1e-12, atol=1e-14,
+               what=f"euler geometric series a={a}")
+    dt, bval, uval = 1e-3, 0.9, 1.3
+    for a in (-0.5, -3.0):
+        args = (np.full((1, 1, 1), uval), np.full((1, 1, 1), dt), np.array([[a]]),
+                np.full((1, 1, 1), bval), np.ones((1, 1, 1)))
+        yz = orc.scan_fwd(*args, delta_softplus=False)[0, 0, 0]
+        ye = orc.scan_fwd(*args, delta_softplus=False, discretization="euler")[0, 0, 0]
+        q = dt * a
+        _close(ye, dt * bval * uval, rtol=1e-15, what="euler one step")
+        _close(yz - ye, (q / 2 + q * q / 6 + q ** 3 / 24) * dt * bval * uval, rtol=1e-6,
+               what="zoh - euler, first order")
+
+
 ALL_PINS = [pin_zoh_matches_ode, pin_unrolled_sum, pin_lti_convolution, pin_geometric_series,
             pin_zoh_small_A, pin_linearity, pin_softplus_bias_gate, pin_step_equals_scan,
-            pin_split_invariance, pin_rows_match_full]
+            pin_split_invariance, pin_rows_match_full, pin_euler_unrolled_sum,
+            pin_euler_geometric_and_first_order]

@@ -48,6 +48,13 @@ MUTANTS = [
     ("expm1_without_divide", "expm1(dt * a) / a;", "expm1(dt * a);"),
     ("decode_stride", "A + d * dstate, B + b * dstate, C + b * dstate, 1,",
      "A + d * dstate, B + b * dstate, C + b * dstate, dstate,"),
+    ("euler_coef_times_A", "        if (euler)\n            coef = dt;",
+     "        if (euler)\n            coef = dt * a;"),
+    ("euler_flag_ignored", "        if (euler)\n            coef = dt;", ""),
+    ("euler_flag_dropped_in_decode", "D ? D[d] : 0.0, z ? z + i : NULL, euler);",
+     "D ? D[d] : 0.0, z ? z + i : NULL, 0);"),
+    ("euler_half_step", "        if (euler)\n            coef = dt;",
+     "        if (euler)\n            coef = 0.5 * dt;"),
 ]
 
 
