@@ -76,6 +76,13 @@ typedef enum {
 
 typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype;
 
+/* Input term of the discretisation (Abar = exp(dt A) in both):
+ *   ZOH   Bbar = (exp(dt A) - 1) / A * B  (dt B where A == 0): the zero-order hold of
+ *         the velog review, section 2 "Discretization" -- the default;
+ *   EULER Bbar = dt * B: the form Mamba_Model_Report.md, section 4.2 (selective_scan:
+ *         deltaB = delta * B) computes. */
+typedef enum { SSM_DISC_ZOH = 0, SSM_DISC_EULER = 1 } ssm_discretization;
+
 /* Kernel family of the scan.  AUTO picks by the number of independent
  * (batch, dim) channels: many channels -> CHANNEL, few -> CHUNK. */
 typedef enum {
@@ -164,6 +171,16 @@ SSM_API ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate,
                              const float* h0, float* h_last, void* y, void* workspace,
                              size_t workspace_bytes, ssm_algo algo, ssm_stream_t stream);
 
+/* ssm_scan_fwd_algo with an explicit discretisation of the input term (ssm_scan_fwd
+ * and ssm_scan_fwd_algo use SSM_DISC_ZOH).  Every kernel family supports both. */
+SSM_API ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                   ssm_dtype io, const void* u, const void* delta,
+                                   const float* delta_bias, int delta_softplus, const float* A,
+                                   const void* B, const void* C, const float* D, const void* z,
+                                   const float* h0, float* h_last, void* y, void* workspace,
+                                   size_t workspace_bytes, ssm_discretization disc,
+                                   ssm_algo algo, ssm_stream_t stream);
+
 /*
  * ssm_scan_fwd for callers that cannot allocate device memory, such as code
  * running under an allocator it does not own (a custom arena, a memory pool that
@@ -209,6 +226,14 @@ SSM_API ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, 
                             const void* u, const void* delta, const float* delta_bias,
                             int delta_softplus, const float* A, const void* B, const void* C,
                             const float* D, const void* z, void* y, ssm_stream_t stream);
+
+/* ssm_state_update with an explicit discretisation of the input term. */
+SSM_API ssm_status ssm_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, ssm_dtype io,
+                                       float* h, const void* u, const void* delta,
+                                       const float* delta_bias, int delta_softplus,
+                                       const float* A, const void* B, const void* C,
+                                       const float* D, const void* z, void* y,
+                                       ssm_discretization disc, ssm_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads the status words of `workspace` (as filled

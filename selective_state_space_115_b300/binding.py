@@ -26,6 +26,10 @@ SSM_ERR_DEVICE_TIMEOUT = 4
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
 
+DISC_ZOH = 0
+DISC_EULER = 1
+_DISC = {"zoh": DISC_ZOH, "euler": DISC_EULER, DISC_ZOH: DISC_ZOH, DISC_EULER: DISC_EULER}
+
 ALGO_AUTO = 0
 ALGO_CHANNEL = 1
 ALGO_CHUNK = 2
@@ -42,7 +46,7 @@ _ALGOS.update({v: v for v in list(_ALGOS.values())})
 
 # every symbol include/ssm.h declares
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "ssm_scan_fwd",
-            "ssm_scan_fwd_algo",
+            "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -92,9 +96,14 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_fwd_algo.argtypes = scan_args + [_int, _vp]
         lib.ssm_scan_fwd_noalloc.restype = _int
         lib.ssm_scan_fwd_noalloc.argtypes = scan_args[:17] + [_vp]
+        lib.ssm_scan_fwd_ex.restype = _int
+        lib.ssm_scan_fwd_ex.argtypes = scan_args + [_int, _int, _vp]
         lib.ssm_state_update.restype = _int
         lib.ssm_state_update.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int, _vp,
                                          _vp, _vp, _vp, _vp, _vp, _vp]
+        lib.ssm_state_update_ex.restype = _int
+        lib.ssm_state_update_ex.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int,
+                                            _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp]
         lib.ssm_read_device_status.restype = _int
         lib.ssm_read_device_status.argtypes = [_vp, _vp]
         lib.ssm_status_string.restype = ctypes.c_char_p
@@ -169,12 +178,14 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True, h0=None,
-             return_last_state=False, algo="auto", out=None, workspace=None):
+             return_last_state=False, algo="auto", out=None, workspace=None,
+             discretization="zoh"):
     """Selective-scan forward on torch CUDA tensors.
 
     u, delta, z, out: [batch, dim, seqlen] (float32 or bfloat16); B, C: [batch, dstate, seqlen]
     (same dtype); A: [dim, dstate] float32; D, delta_bias: [dim] float32; h0: [batch, dim,
-    dstate] float32.  Returns y (and h_last [batch, dim, dstate] float32 when asked)."""
+    dstate] float32.  Returns y (and h_last [batch, dim, dstate] float32 when asked).
+    discretization: "zoh" (default) or "euler" (input term dt * B)."""
     if not isinstance(u, torch.Tensor) or not u.is_cuda:
         raise SsmError(SSM_ERR_INVALID_ARG, "u must be a CUDA tensor")
     if u.dim() != 3:
@@ -201,10 +212,11 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     ws = _workspace(dev, nbytes) if workspace is None else workspace
     stream = torch.cuda.current_stream(dev).cuda_stream
     with torch.cuda.device(dev):
-        st = lib.ssm_scan_fwd_algo(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
-                                   _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
-                                   _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(h_last), _ptr(y),
-                                   _ptr(ws), ws.numel(), _ALGOS[algo], ctypes.c_void_p(stream))
+        st = lib.ssm_scan_fwd_ex(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                 _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
+                                 _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(h_last), _ptr(y),
+                                 _ptr(ws), ws.numel(), _DISC[discretization], _ALGOS[algo],
+                                 ctypes.c_void_p(stream))
     _check(st, "ssm_scan_fwd")
     return (y, h_last) if return_last_state else y
 
@@ -219,7 +231,7 @@ def read_device_status(workspace: Optional[torch.Tensor] = None, device=None) ->
 
 
 def state_update(h, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                 out=None):
+                 out=None, discretization="zoh"):
     """One decode step; h [batch, dim, dstate] float32 is updated in place.
 
     u, delta, z, out: [batch, dim]; B, C: [batch, dstate]; A: [dim, dstate] float32.
@@ -242,9 +254,10 @@ def state_update(h, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_so
     _need(y, "out", (batch, dim), u.dtype, dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     with torch.cuda.device(dev):
-        st = library().ssm_state_update(batch, dim, dstate, io, _ptr(h), _ptr(u), _ptr(delta),
-                                        _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
-                                        _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
-                                        ctypes.c_void_p(stream))
+        st = library().ssm_state_update_ex(batch, dim, dstate, io, _ptr(h), _ptr(u),
+                                           _ptr(delta), _ptr(delta_bias),
+                                           int(bool(delta_softplus)), _ptr(A), _ptr(B), _ptr(C),
+                                           _ptr(D), _ptr(z), _ptr(y), _DISC[discretization],
+                                           ctypes.c_void_p(stream))
     _check(st, "ssm_state_update")
     return y

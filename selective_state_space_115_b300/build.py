@@ -1,6 +1,10 @@
 """Builds libssm.so (the CUDA library behind include/ssm.h) in-tree with nvcc for sm_103a.
 
-    python -m selective_state_space_115_b300.build [--force]
+Each csrc/*.cu translation unit (the C ABI, and the kernel instantiations split by
+element type and discretisation) compiles to an object in parallel; the objects
+link into one shared library.
+
+    python -m selective_state_space_115_b300.build [--force] [-v] [--ptxas-v]
 """
 from __future__ import annotations
 
@@ -9,16 +13,19 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libssm.so")
+OBJDIR = os.path.join(PKG, "_build")
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", ARCH, "--shared", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-fvisibility=hidden", "-cudart", "shared", "--expt-relaxed-constexpr"]
+COMPILE_FLAGS = ["-O3", "-std=c++17", "-lineinfo", ARCH, "-Xcompiler", "-fPIC", "-Xcompiler",
+                 "-fvisibility=hidden", "--expt-relaxed-constexpr"]
+LINK_FLAGS = [ARCH, "--shared", "-cudart", "shared"]
 
 
 def nvcc() -> str:
@@ -28,8 +35,12 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (CUDA 13 toolkit required to build libssm)")
 
 
+def units():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+    return sorted(units() + glob.glob(os.path.join(CSRC, "*.cuh"))
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
@@ -43,8 +54,29 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if not force and up_to_date():
         return LIB
-    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC,
-           os.path.join(CSRC, "ssm_api.cu"), "-o", LIB + ".tmp"]
+    os.makedirs(OBJDIR, exist_ok=True)
+    cc = nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        cmd = [cc, *COMPILE_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        return src, obj, r
+
+    jobs = min(len(units()), os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=jobs) as ex:
+        results = list(ex.map(compile_one, units()))
+    objs = []
+    for src, obj, r in results:
+        if r.stdout or r.stderr:
+            sys.stdout.write(r.stdout)
+            sys.stderr.write(r.stderr)
+        if r.returncode != 0:
+            raise subprocess.CalledProcessError(r.returncode, f"nvcc {os.path.basename(src)}")
+        objs.append(obj)
+    cmd = [cc, *LINK_FLAGS, *objs, "-o", LIB + ".tmp"]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)

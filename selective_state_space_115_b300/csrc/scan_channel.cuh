@@ -78,10 +78,11 @@ constexpr int kModeFull = 0, kModeStates = 1, kModeCarry = 2;
 // 2^-22 |B u / A|.
 constexpr float kFastPathMinAbsA = 0.125f;
 
-template <typename IO, int N_, bool GATE_, int LPC_, int S_, int RB_>
+template <typename IO, int N_, bool GATE_, int LPC_, int S_, int RB_, bool EULER_ = false>
 struct ChanCfg {
   static constexpr int N = N_;
   static constexpr bool GATE = GATE_;
+  static constexpr bool EULER = EULER_;     // input term dt * B instead of the ZOH form
   static constexpr int LPC = LPC_;          // lanes per channel
   static constexpr int NS = N / LPC;        // states per lane
   static constexpr int S = S_;              // pipeline stages
@@ -317,6 +318,8 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 #pragma unroll
     for (int j = 0; j < TB; ++j) {
       const int lc = blk * TB + j;  // position within the chunk
+      const float dtj = sj[j] * kLn2;  // dt (Euler input term)
+      (void)dtj;
       const float* Bp = bcfB + lc * N + part * NS;
       const float* Cp = bcfC + lc * N + part * NS;
       // contraction in a fixed order for every lane split: a packed pair sum per
@@ -337,9 +340,15 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
             const f2 q = mul2(mk2(sj[j], sj[j]), mk2(Areg[i], Areg[i + 1]));
             const f2 a = mk2(ex2(q.x), ex2(q.y));
             const f2 X = mul2(mk2(bv[pp], bv[pp + 1]), mk2(uj[j], uj[j]));
-            const f2 nw = mul2(X, mk2(nIA[i], nIA[i + 1]));       // -w = -B u / A
-            const f2 t = sub2(mk2(h[i], h[i + 1]), nw);           // h + w
-            const f2 hn = fma2(a, t, nw);                         // Abar (h + w) - w
+            f2 hn;
+            if constexpr (Cfg::EULER) {
+              const f2 W = mul2(X, mk2(dtj, dtj));                // dt B u
+              hn = fma2(a, mk2(h[i], h[i + 1]), W);               // Abar h + dt B u
+            } else {
+              const f2 nw = mul2(X, mk2(nIA[i], nIA[i + 1]));     // -w = -B u / A
+              const f2 t = sub2(mk2(h[i], h[i + 1]), nw);         // h + w
+              hn = fma2(a, t, nw);                                // Abar (h + w) - w
+            }
             h[i] = hn.x;
             h[i + 1] = hn.y;
           } else {
@@ -351,7 +360,8 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
               const float em1 = exp2m1_accurate(q, ahw);
               const float a = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
               // (Abar - 1) / A, or dt at A == 0
-              const float coef = (A0 == 0.0f) ? sj[j] * kLn2 : em1 * -nIA[i + e];
+              const float coef =
+                  (Cfg::EULER || A0 == 0.0f) ? sj[j] * kLn2 : em1 * -nIA[i + e];
               h[i + e] = fmaf(a, h[i + e], coef * (bv[pp + e] * uj[j]));
             }
           }

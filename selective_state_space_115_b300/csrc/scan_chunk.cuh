@@ -23,10 +23,11 @@
 
 namespace ssm {
 
-template <typename IO, int N_, bool GATE_, bool VEC_>
+template <typename IO, int N_, bool GATE_, bool VEC_, bool EULER_ = false>
 struct ChunkCfg {
   static constexpr int N = N_;
   static constexpr bool GATE = GATE_;
+  static constexpr bool EULER = EULER_;     // input term dt * B instead of the ZOH form
   static constexpr bool VEC = VEC_;
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
@@ -142,7 +143,11 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
         const float q = s[i] * An;
         const float ahw = ex2(q);
         const float X = Bv[i] * u[i];
-        if constexpr (!ACC) {
+        if constexpr (Cfg::EULER) {
+          a[i] = ACC ? ((fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + exp2m1_accurate(q, ahw) : ahw)
+                     : ahw;
+          bb[i] = (s[i] * kLn2) * X;         // dt B u
+        } else if constexpr (!ACC) {
           const float nK = X * (-IAn);       // -B u / A
           a[i] = ahw;
           bb[i] = fmaf(-ahw, nK, nK);        // (Abar - 1) B u / A

@@ -34,10 +34,11 @@ struct UpdateParams {
   void* y;           // [batch, dim]
 };
 
-template <typename IO, int N_, bool GATE_, bool VEC_>
+template <typename IO, int N_, bool GATE_, bool VEC_, bool EULER_ = false>
 struct UpdCfg {
   static constexpr int N = N_;
   static constexpr bool GATE = GATE_;
+  static constexpr bool EULER = EULER_;  // input term dt * B instead of the ZOH form
   static constexpr bool VEC = VEC_;  // h, A 16-byte aligned; B, C rows 4-element aligned
   static constexpr int THREADS = 256;
 };
@@ -115,7 +116,7 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
       const float abar = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
       // (Abar - 1) / A, or dt at A == 0; 1/A from the hardware reciprocal (a few
       // ulp, far below the series' truncation)
-      const float coef = (a0 == 0.0f) ? s * kLn2 : em1 * rcp(a0);
+      const float coef = (Cfg::EULER || a0 == 0.0f) ? s * kLn2 : em1 * rcp(a0);
       const float hn = fmaf(abar, hv[4 * k + i], coef * (Bv[i] * uv));
       hv[4 * k + i] = hn;
       if (i & 1)

@@ -160,6 +160,17 @@ def test_update_validation(kw, expect):
     assert update(lib, **kw) == expect
 
 
+def test_discretization_is_validated():
+    lib = binding.library()
+    args = [2, 8, 16, 64, 1] + [ctypes.c_void_p(P)] * 2 + [None, 1] + [ctypes.c_void_p(P)] * 3 + \
+        [None] * 4 + [ctypes.c_void_p(P), ctypes.c_void_p(WS), 256]
+    assert lib.ssm_scan_fwd_ex(*args, 7, binding.ALGO_AUTO, None) == binding.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_fwd_ex(*args, -1, binding.ALGO_AUTO, None) == binding.SSM_ERR_UNSUPPORTED
+    up = [4, 8, 16, 1] + [ctypes.c_void_p(P)] * 3 + [None, 1] + [ctypes.c_void_p(P)] * 3 + \
+        [None, None, ctypes.c_void_p(P)]
+    assert lib.ssm_state_update_ex(*up, 3, None) == binding.SSM_ERR_UNSUPPORTED
+
+
 def test_read_status_rejects_null():
     lib = binding.library()
     assert lib.ssm_read_device_status(None, None) == binding.SSM_ERR_INVALID_ARG

@@ -137,3 +137,27 @@ def test_steps_equal_scan(io, algo):
     y_steps = np.stack([from_torch(t) for t in ys], axis=-1)
     assert rel_err(y_steps, from_torch(y_scan)) <= TOL[io]
     assert rel_err(from_torch(h), from_torch(h_scan)) <= (1e-5 if io == W.F32 else 1e-3)
+
+
+@pytest.mark.parametrize("io", [W.F32, W.BF16])
+def test_decode_euler_input_term(io):
+    """Decode steps with Bbar = dt B against the oracle's Euler step."""
+    import torch
+    cfg = W.DecodeConfig("t", 3, 70, 16, 4, io, gate=True, h_std=0.1, description="")
+    static = W.make_decode_static(cfg, seed=6)
+    h = torch_f32(static["h"])
+    href = static["h"].astype(np.float64)
+    for t in range(cfg.steps):
+        st = W.make_decode_step(cfg, t, seed=6)
+        y = S().state_update(h, torch_io(st["u"], io), torch_io(st["delta"], io),
+                             torch_f32(static["A"]), torch_io(st["B"], io),
+                             torch_io(st["C"], io), D=torch_f32(static["D"]),
+                             z=torch_io(st["z"], io), delta_bias=torch_f32(static["delta_bias"]),
+                             discretization="euler")
+        torch.cuda.synchronize()
+        f = lambda a: W.to_f64(a, io)  # noqa: E731
+        yref, href = oracle.state_update(href, f(st["u"]), f(st["delta"]), static["A"],
+                                         f(st["B"]), f(st["C"]), D=static["D"], z=f(st["z"]),
+                                         delta_bias=static["delta_bias"], discretization="euler")
+        assert rel_err(from_torch(y), yref) <= TOL[io]
+        assert rel_err(from_torch(h), href) <= 1e-5

@@ -345,6 +345,44 @@ def test_mixed_split_matches_one_lane_bit_for_bit():
     assert rel_err(from_torch(ym).reshape(-1, cfg.seqlen)[rows], ref) <= TOL[io]
 
 
+EULER_CASES = [
+    # io, batch, dim, dstate, seqlen, gate, h0
+    (W.F32, 2, 37, 16, 69, True, True),
+    (W.BF16, 2, 160, 16, 512, True, True),
+    (W.BF16, 1, 40, 8, 1000, False, False),
+]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("io,batch,dim,dstate,seqlen,gate,h0", EULER_CASES)
+def test_euler_input_term(algo, io, batch, dim, dstate, seqlen, gate, h0):
+    """Bbar = dt B (Mamba_Model_Report.md section 4.2) on every kernel family."""
+    import torch
+    if dstate < MIN_DSTATE.get(algo, 0):
+        pytest.skip(f"{algo} needs dstate >= {MIN_DSTATE[algo]}")
+    cfg = W.ScanConfig("t", batch, dim, dstate, seqlen, io, gate=gate, dt_bias=True,
+                       d_skip="normal", description="")
+    x = W.make_scan_inputs(cfg, seed=41 + seqlen, with_h0=h0)
+    y, hl = S().scan_fwd(torch_io(x["u"], io), torch_io(x["delta"], io), torch_f32(x["A"]),
+                         torch_io(x["B"], io), torch_io(x["C"], io), D=torch_f32(x["D"]),
+                         z=torch_io(x.get("z"), io), delta_bias=torch_f32(x["delta_bias"]),
+                         h0=torch_f32(x.get("h0")), return_last_state=True, algo=algo,
+                         discretization="euler")
+    torch.cuda.synchronize()
+    assert S().read_device_status() == 0
+    ref, hr = oracle.scan_fwd(f64(x["u"], io), f64(x["delta"], io), x["A"], f64(x["B"], io),
+                              f64(x["C"], io), D=x["D"], z=f64(x.get("z"), io),
+                              delta_bias=x["delta_bias"], h0=x.get("h0"), return_last_state=True,
+                              nthreads=NTHREADS, discretization="euler")
+    assert rel_err(from_torch(y), ref) <= TOL[io]
+    assert rel_err(from_torch(hl), hr) <= (1e-4 if io == W.F32 else 1e-3)
+    # and it is not the ZOH result
+    zoh = oracle.scan_fwd(f64(x["u"], io), f64(x["delta"], io), x["A"], f64(x["B"], io),
+                          f64(x["C"], io), D=x["D"], z=f64(x.get("z"), io),
+                          delta_bias=x["delta_bias"], h0=x.get("h0"), nthreads=NTHREADS)
+    assert rel_err(from_torch(y), zoh) > 10 * TOL[io]
+
+
 def test_auto_matches_explicit_choice():
     cfg = W.SCAN_CONFIGS["2p8b"]
     x = W.make_scan_inputs(cfg, seed=0, batch=2)  # 10240 channels: the channel kernel
