@@ -86,6 +86,12 @@ class Oracle:
         lib.oracle_state_update.argtypes = [_i64, _i64, _i64, _dp, _dp, _dp, _dp,
                                             ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp,
                                             ctypes.c_int]
+        lib.oracle_conv1d_fwd.restype = ctypes.c_int
+        lib.oracle_conv1d_fwd.argtypes = [_i64, _i64, _i64, _i64, _dp, _dp, _dp, _dp,
+                                          ctypes.c_int, _dp, _dp]
+        lib.oracle_conv1d_update.restype = ctypes.c_int
+        lib.oracle_conv1d_update.argtypes = [_i64, _i64, _i64, _dp, _dp, _dp, _dp, ctypes.c_int,
+                                             _dp]
         self.lib = lib
         self.path = path
 
@@ -155,6 +161,41 @@ class Oracle:
         return y, h
 
 
+    def conv1d_fwd(self, x, weight, bias=None, state_in=None, apply_silu=True,
+                   return_state=False):
+        """Causal depthwise convolution over time in fp64.  x [b,d,l]; weight [d,W];
+        bias [d]; state_in [b,d,W-1] (inputs before position 0).  Returns out [b,d,l]
+        (and the last W-1 inputs [b,d,W-1])."""
+        x, weight, bias, state_in = (_f64(a) for a in (x, weight, bias, state_in))
+        batch, dim, seqlen = x.shape
+        width = weight.shape[1]
+        assert weight.shape == (dim, width)
+        assert state_in is None or state_in.shape == (batch, dim, width - 1)
+        out = np.empty_like(x)
+        state_out = np.empty((batch, dim, width - 1)) if return_state else None
+        rc = self.lib.oracle_conv1d_fwd(batch, dim, seqlen, width, _ptr(x), _ptr(weight),
+                                        _ptr(bias), _ptr(state_in), int(bool(apply_silu)),
+                                        _ptr(out), _ptr(state_out))
+        if rc != 0:
+            raise RuntimeError("oracle_conv1d_fwd failed")
+        return (out, state_out) if return_state else out
+
+    def conv1d_update(self, state, x, weight, bias=None, apply_silu=True):
+        """One decode position: state [b,d,W-1] (copied, not modified), x [b,d].
+        Returns (out [b,d], new state [b,d,W-1])."""
+        state = np.array(state, dtype=np.float64, copy=True, order="C")
+        x, weight, bias = (_f64(a) for a in (x, weight, bias))
+        batch, dim = x.shape
+        width = weight.shape[1]
+        assert state.shape == (batch, dim, width - 1)
+        out = np.empty_like(x)
+        rc = self.lib.oracle_conv1d_update(batch, dim, width, _ptr(state), _ptr(x), _ptr(weight),
+                                           _ptr(bias), int(bool(apply_silu)), _ptr(out))
+        if rc != 0:
+            raise RuntimeError("oracle_conv1d_update failed")
+        return out, state
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -173,3 +214,11 @@ def scan_rows(*args, **kwargs):
 
 def state_update(*args, **kwargs):
     return default().state_update(*args, **kwargs)
+
+
+def conv1d_fwd(*args, **kwargs):
+    return default().conv1d_fwd(*args, **kwargs)
+
+
+def conv1d_update(*args, **kwargs):
+    return default().conv1d_update(*args, **kwargs)

@@ -46,6 +46,10 @@
  *    section 4.2 (selective_scan: deltaB = delta * B, BX = deltaB * x), with the
  *    same Abar = exp(dt * A).
  *
+ * The file also holds the causal depthwise convolution that precedes the scan in
+ * the report's MambaBlock (oracle_conv1d_fwd, oracle_conv1d_update; definitions
+ * and passages at the end).
+ *
  * Pinned by tests/test_oracle_pins.py against brute-force unrolled sums,
  * the LTI convolution form, a geometric-series closed form, the A -> 0 limit,
  * linearity in u, step/scan equivalence and split invariance.
@@ -216,6 +220,84 @@ int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double* h,
                                delta_bias ? delta_bias[d] : 0.0, delta_softplus,
                                A + d * dstate, B + b * dstate, C + b * dstate, 1,
                                D ? D[d] : 0.0, z ? z + i : NULL, euler);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Causal depthwise convolution over time (the step before the scan).
+ *
+ *   out[b,d,l] = act( bias[d] + sum_{k=0}^{W-1} w[d,k] * x[b,d,l-(W-1)+k] )
+ *
+ * where x at a position before 0 is the carried-in window state_in[b,d,(W-1)+p]
+ * (zero without a state), and act is silu or the identity.  This is the
+ * MambaBlock's nn.Conv1d(groups=d_inner, kernel_size=d_conv, padding=d_conv-1)
+ * truncated to the first L outputs, followed by silu (Mamba_Model_Report.md
+ * section 3, MambaBlock.forward: x = self.conv1d(x)[:, :, :L]; x = F.silu(x)).
+ * state_out[b,d,j] (optional) receives the last W-1 inputs, positions
+ * L-(W-1)+j, which is the decode cache the report keeps (section 6: inputs,
+ * (B, ED, d_conv-1)).
+ * ------------------------------------------------------------------------ */
+static double oracle_conv_input(const double* x_row, const double* state_row, int64_t width,
+                                int64_t p)
+{
+    if (p >= 0)
+        return x_row[p];
+    if (p < -(width - 1) || !state_row)
+        return 0.0;
+    return state_row[(width - 1) + p];
+}
+
+int oracle_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                      const double* x, const double* weight, const double* bias,
+                      const double* state_in, int apply_silu, double* out, double* state_out)
+{
+    if (batch < 0 || dim < 0 || seqlen < 0 || width < 1)
+        return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t row = b * dim + d;
+            const double* xr = x + row * seqlen;
+            const double* sr = state_in ? state_in + row * (width - 1) : NULL;
+            for (int64_t l = 0; l < seqlen; ++l) {
+                double acc = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < width; ++k)
+                    acc += weight[d * width + k] * oracle_conv_input(xr, sr, width,
+                                                                     l - (width - 1) + k);
+                out[row * seqlen + l] = apply_silu ? oracle_silu(acc) : acc;
+            }
+            if (state_out)
+                for (int64_t j = 0; j < width - 1; ++j)
+                    state_out[row * (width - 1) + j] =
+                        oracle_conv_input(xr, sr, width, seqlen - (width - 1) + j);
+        }
+    }
+    return 0;
+}
+
+/* One decode position (Mamba_Model_Report.md section 6, step): the window is the
+ * cached W-1 inputs followed by x; out = act(bias + sum_k w[k] window[k]); the
+ * cache drops its oldest input and appends x.  state [b,d,W-1] is updated in place. */
+int oracle_conv1d_update(int64_t batch, int64_t dim, int64_t width, double* state,
+                         const double* x, const double* weight, const double* bias,
+                         int apply_silu, double* out)
+{
+    if (batch < 0 || dim < 0 || width < 1)
+        return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t row = b * dim + d;
+            double* s = state + row * (width - 1);
+            double acc = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < width - 1; ++k)
+                acc += weight[d * width + k] * s[k];
+            acc += weight[d * width + width - 1] * x[row];
+            out[row] = apply_silu ? oracle_silu(acc) : acc;
+            for (int64_t k = 0; k + 1 < width - 1; ++k)
+                s[k] = s[k + 1];
+            if (width > 1)
+                s[width - 2] = x[row];
         }
     }
     return 0;

@@ -25,6 +25,9 @@ Sources of each fact:
   * single-token step equals the scan: Mamba_Model_Report.md, section 6.
   * Euler input term Bbar = delta * B with the same Abar = exp(delta A):
     Mamba_Model_Report.md, section 4.2 (selective_scan: deltaB = delta * B).
+  * causal depthwise conv1d (groups = channels, padding W - 1, first L outputs)
+    then silu, and its decode cache of the last W - 1 inputs:
+    Mamba_Model_Report.md, sections 3 (MambaBlock.forward) and 6 (step).
 """
 from __future__ import annotations
 
@@ -350,7 +353,64 @@ def pin_euler_geometric_and_first_order(orc):
                what="zoh - euler, first order")
 
 
+# ---------------------------------------------------------------------------
+# 11. causal depthwise convolution (MambaBlock conv1d, and its decode cache)
+# ---------------------------------------------------------------------------
+def pin_conv1d_matches_convolution(orc):
+    """Each channel's output is the full linear convolution of its input with the
+    reversed filter, truncated to the first L outputs (np.convolve), plus the bias,
+    then silu; and the same as torch's grouped Conv1d with padding W - 1."""
+    import torch
+    import torch.nn.functional as F
+
+    rng = _rng(12)
+    b, d, L = 2, 5, 23
+    for width in (2, 4, 7):
+        x = rng.standard_normal((b, d, L))
+        w = rng.standard_normal((d, width))
+        bias = rng.standard_normal(d)
+        out = orc.conv1d_fwd(x, w, bias, apply_silu=False)
+        outs = orc.conv1d_fwd(x, w, bias, apply_silu=True)
+        for bi in range(b):
+            for di in range(d):
+                ref = np.convolve(x[bi, di], w[di, ::-1])[:L] + bias[di]
+                _close(out[bi, di], ref, rtol=1e-13, atol=1e-13, what=f"conv W={width}")
+        tx = torch.tensor(x, dtype=torch.float64)
+        ref = F.conv1d(tx, torch.tensor(w[:, None, :]), torch.tensor(bias), padding=width - 1,
+                       groups=d)[:, :, :L]
+        _close(out, ref.numpy(), rtol=1e-13, atol=1e-13, what=f"torch conv1d W={width}")
+        _close(outs, F.silu(ref).numpy(), rtol=1e-13, atol=1e-13, what=f"conv + silu W={width}")
+
+
+def pin_conv1d_state_and_step(orc):
+    """A carried-in window continues the sequence (two halves with the state passed
+    on equal one pass), and the decode update applied position by position equals
+    the full convolution, its cache equal to the last W - 1 inputs."""
+    rng = _rng(13)
+    b, d, L, m, width = 2, 3, 17, 6, 4
+    x = rng.standard_normal((b, d, L))
+    w = rng.standard_normal((d, width))
+    bias = rng.standard_normal(d)
+    s0 = rng.standard_normal((b, d, width - 1))
+    full, s_end = orc.conv1d_fwd(x, w, bias, state_in=s0, return_state=True)
+    ya, sa = orc.conv1d_fwd(x[..., :m], w, bias, state_in=s0, return_state=True)
+    yb, sb = orc.conv1d_fwd(x[..., m:], w, bias, state_in=sa, return_state=True)
+    _close(np.concatenate([ya, yb], -1), full, rtol=1e-14, atol=1e-14, what="conv halves")
+    _close(sb, s_end, rtol=0, atol=0, what="conv state after halves")
+    _close(s_end, x[..., L - (width - 1):], rtol=0, atol=0, what="conv state = last inputs")
+    st = s0.copy()
+    for l in range(L):
+        yl, st = orc.conv1d_update(st, x[..., l], w, bias)
+        _close(yl, full[..., l], rtol=1e-14, atol=1e-14, what=f"conv step {l}")
+    _close(st, s_end, rtol=0, atol=0, what="conv cache after steps")
+    # without a state the inputs before position 0 are zero: a lone first position
+    y1 = orc.conv1d_fwd(x[..., :1], w, bias, apply_silu=False)
+    _close(y1[..., 0], w[None, :, -1] * x[..., 0] + bias[None, :], rtol=1e-15, atol=1e-15,
+           what="first position, zero history")
+
+
 ALL_PINS = [pin_zoh_matches_ode, pin_unrolled_sum, pin_lti_convolution, pin_geometric_series,
             pin_zoh_small_A, pin_linearity, pin_softplus_bias_gate, pin_step_equals_scan,
             pin_split_invariance, pin_rows_match_full, pin_euler_unrolled_sum,
-            pin_euler_geometric_and_first_order]
+            pin_euler_geometric_and_first_order, pin_conv1d_matches_convolution,
+            pin_conv1d_state_and_step]

@@ -55,6 +55,17 @@ MUTANTS = [
      "D ? D[d] : 0.0, z ? z + i : NULL, 0);"),
     ("euler_half_step", "        if (euler)\n            coef = dt;",
      "        if (euler)\n            coef = 0.5 * dt;"),
+    ("conv_anticausal", "l - (width - 1) + k);", "l + k);"),
+    ("conv_reversed_taps", "acc += weight[d * width + k] * oracle_conv_input(",
+     "acc += weight[d * width + (width - 1 - k)] * oracle_conv_input("),
+    ("conv_dropped_bias", "                double acc = bias ? bias[d] : 0.0;\n",
+     "                double acc = 0.0;\n"),
+    ("conv_state_ignored", "    if (p < -(width - 1) || !state_row)", "    if (1)"),
+    ("conv_update_no_shift", "                s[k] = s[k + 1];", "                ;"),
+    ("conv_silu_before_bias",
+     "                out[row * seqlen + l] = apply_silu ? oracle_silu(acc) : acc;",
+     "                out[row * seqlen + l] = apply_silu ? oracle_silu(acc - (bias ? bias[d] : 0.0))"
+     " + (bias ? bias[d] : 0.0) : acc;"),
 ]
 
 
