@@ -381,6 +381,7 @@ def run_gpu(args):
 
     # ---- decode state update (rank 0's measurement)
     decode = run_decode(dev, S) if (rank == 0 and not args.no_decode) else None
+    conv = run_conv(dev, S) if (rank == 0 and not args.no_decode) else None
     barrier(world)
 
     # ---- CPU baseline (rank 0, N = 1 only)
@@ -417,6 +418,8 @@ def run_gpu(args):
         }
         if decode:
             line["decode"] = decode
+        if conv:
+            line["conv1d"] = conv
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -424,6 +427,40 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def run_conv(dev, S, iters=50):
+    """The causal depthwise conv1d + silu that precedes the scan, on the scan
+    workload's x shape (width 4), through the C ABI."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    shape = (CFG.batch, CFG.dim, CFG.seqlen)
+    dt = torch.bfloat16 if CFG.io == W.BF16 else torch.float32
+    x = torch.randn(shape, generator=g, device=dev).to(dt)
+    w = torch.randn((CFG.dim, 4), generator=g, device=dev) * 0.5
+    bias = torch.randn((CFG.dim,), generator=g, device=dev)
+    out = torch.empty_like(x)
+    for _ in range(3):
+        S.conv1d_fwd(x, w, bias, out=out)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        S.conv1d_fwd(x, w, bias, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    nbytes = 2 * x.numel() * x.element_size() + 4 * 5 * CFG.dim
+    peaks, kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"causal depthwise conv1d + silu, width 4, x {list(shape)} "
+                        f"{'bf16' if CFG.io == W.BF16 else 'fp32'}",
+            "ms_per_call": ms, "bytes_per_call": nbytes, "gpu_launches": iters,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "traffic": None, "peak_kind": kind}}
 
 
 def run_decode(dev, S):

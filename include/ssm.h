@@ -236,6 +236,43 @@ SSM_API ssm_status ssm_state_update_ex(int64_t batch, int64_t dim, int64_t dstat
                                        ssm_discretization disc, ssm_stream_t stream);
 
 /*
+ * Causal depthwise convolution over time, the step before the scan in the
+ * MambaBlock of Mamba_Model_Report.md (section 3: nn.Conv1d with groups = channels,
+ * kernel_size = width, padding = width - 1, the first L outputs, then silu):
+ *
+ *   out[b,d,l] = act(bias[d] + sum_{k<width} weight[d,k] * x[b,d,l-(width-1)+k])
+ *
+ * with act = silu (apply_silu != 0) or the identity, and x before position 0 taken
+ * from conv_state (the width - 1 inputs that precede the sequence) or zero.
+ *
+ *  io           dtype of x, out and the two states (float32 or bfloat16)
+ *  x, out       [batch, dim, seqlen], required; must not overlap
+ *  weight       [dim, width] float32, required;  bias [dim] float32 or NULL
+ *  conv_state   [batch, dim, width - 1] or NULL (zero history)
+ *  conv_state_out [batch, dim, width - 1] or NULL: receives the last width - 1
+ *               inputs (the decode cache; section 6 of the report)
+ *  width        1 .. 8 (SSM_ERR_UNSUPPORTED otherwise)
+ * Arithmetic is fp32; bf16 outputs are rounded to nearest even.  Validated on the
+ * host first; enqueued on `stream`; no workspace, no device-side waits.
+ */
+SSM_API ssm_status ssm_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                                  ssm_dtype io, const void* x, const float* weight,
+                                  const float* bias, const void* conv_state, int apply_silu,
+                                  void* out, void* conv_state_out, ssm_stream_t stream);
+
+/*
+ * One decode position of the convolution above (Mamba_Model_Report.md section 6,
+ * step): the window is conv_state[b,d,:] (the last width - 1 inputs) followed by
+ * x[b,d]; out[b,d] = act(bias[d] + sum_k weight[d,k] window[k]); conv_state drops
+ * its oldest input and appends x (in place).
+ *  conv_state [batch, dim, width - 1] io dtype, in/out;  x, out [batch, dim]
+ */
+SSM_API ssm_status ssm_conv1d_update(int64_t batch, int64_t dim, int64_t width, ssm_dtype io,
+                                     void* conv_state, const void* x, const float* weight,
+                                     const float* bias, int apply_silu, void* out,
+                                     ssm_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads the status words of `workspace` (as filled
  * by the last ssm_scan_fwd that used it).  Returns SSM_OK, SSM_ERR_DEVICE_TIMEOUT,
  * or SSM_ERR_CUDA if the synchronisation or the copy failed.

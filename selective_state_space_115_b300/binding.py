@@ -46,7 +46,8 @@ _ALGOS.update({v: v for v in list(_ALGOS.values())})
 
 # every symbol include/ssm.h declares
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "ssm_scan_fwd",
-            "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex",
+            "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_conv1d_fwd",
+            "ssm_conv1d_update",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -104,6 +105,12 @@ def library(path: Optional[str] = None):
         lib.ssm_state_update_ex.restype = _int
         lib.ssm_state_update_ex.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int,
                                             _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp]
+        lib.ssm_conv1d_fwd.restype = _int
+        lib.ssm_conv1d_fwd.argtypes = [_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int,
+                                       _vp, _vp, _vp]
+        lib.ssm_conv1d_update.restype = _int
+        lib.ssm_conv1d_update.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int, _vp,
+                                          _vp]
         lib.ssm_read_device_status.restype = _int
         lib.ssm_read_device_status.argtypes = [_vp, _vp]
         lib.ssm_status_string.restype = ctypes.c_char_p
@@ -260,4 +267,57 @@ def state_update(h, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_so
                                            _ptr(D), _ptr(z), _ptr(y), _DISC[discretization],
                                            ctypes.c_void_p(stream))
     _check(st, "ssm_state_update")
+    return y
+
+
+def conv1d_fwd(x, weight, bias=None, conv_state=None, apply_silu=True, return_state=False,
+               out=None):
+    """Causal depthwise convolution over time (+ silu) on torch CUDA tensors.
+
+    x, out: [batch, dim, seqlen] (float32 or bfloat16); weight [dim, width] float32;
+    bias [dim] float32; conv_state [batch, dim, width - 1] (x's dtype): the inputs
+    before position 0.  Returns out (and the last width - 1 inputs when asked)."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dim() != 3:
+        raise SsmError(SSM_ERR_INVALID_ARG, "x must be a [batch, dim, seqlen] CUDA tensor")
+    batch, dim, seqlen = x.shape
+    width = weight.shape[-1]
+    dev = x.device
+    io = _io_dtype(x)
+    _need(x, "x", (batch, dim, seqlen), x.dtype, dev)
+    _need(weight, "weight", (dim, width), torch.float32, dev)
+    _need(bias, "bias", (dim,), torch.float32, dev, optional=True)
+    _need(conv_state, "conv_state", (batch, dim, width - 1), x.dtype, dev, optional=True)
+    y = torch.empty_like(x) if out is None else out
+    _need(y, "out", (batch, dim, seqlen), x.dtype, dev)
+    st_out = torch.empty((batch, dim, width - 1), dtype=x.dtype, device=dev) \
+        if return_state else None
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = library().ssm_conv1d_fwd(batch, dim, seqlen, width, io, _ptr(x), _ptr(weight),
+                                      _ptr(bias), _ptr(conv_state), int(bool(apply_silu)),
+                                      _ptr(y), _ptr(st_out), ctypes.c_void_p(stream))
+    _check(st, "ssm_conv1d_fwd")
+    return (y, st_out) if return_state else y
+
+
+def conv1d_update(conv_state, x, weight, bias=None, apply_silu=True, out=None):
+    """One decode position of conv1d_fwd; conv_state [batch, dim, width - 1] is
+    updated in place.  x, out: [batch, dim].  Returns out."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dim() != 2:
+        raise SsmError(SSM_ERR_INVALID_ARG, "x must be a [batch, dim] CUDA tensor")
+    batch, dim = x.shape
+    width = weight.shape[-1]
+    dev = x.device
+    io = _io_dtype(x)
+    _need(weight, "weight", (dim, width), torch.float32, dev)
+    _need(bias, "bias", (dim,), torch.float32, dev, optional=True)
+    _need(conv_state, "conv_state", (batch, dim, width - 1), x.dtype, dev)
+    y = torch.empty_like(x) if out is None else out
+    _need(y, "out", (batch, dim), x.dtype, dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = library().ssm_conv1d_update(batch, dim, width, io, _ptr(conv_state), _ptr(x),
+                                         _ptr(weight), _ptr(bias), int(bool(apply_silu)),
+                                         _ptr(y), ctypes.c_void_p(stream))
+    _check(st, "ssm_conv1d_update")
     return y

@@ -301,6 +301,66 @@ ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, ssm_dtyp
                              C, D, z, y, SSM_DISC_ZOH, stream);
 }
 
+ssm_status ssm_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                          ssm_dtype io, const void* x, const float* weight, const float* bias,
+                          const void* conv_state, int apply_silu, void* out,
+                          void* conv_state_out, ssm_stream_t stream) {
+  ssm_status st = validate_common(batch, dim, 4, io);
+  if (st != SSM_OK) return st;
+  if (seqlen < 1 || seqlen > INT32_MAX - 16) return SSM_ERR_INVALID_ARG;
+  if (width < 1 || width > ssm::kConvMaxWidth) return SSM_ERR_UNSUPPORTED;
+  if (batch > (int64_t(1) << 62) / dim / seqlen) return SSM_ERR_INVALID_ARG;
+  if (!x || !weight || !out) return SSM_ERR_INVALID_ARG;
+  const size_t esz = (io == SSM_DTYPE_BF16) ? 2 : 4;
+  const void* io_ptrs[4] = {x, out, conv_state, conv_state_out};
+  for (const void* q : io_ptrs)
+    if (q && !aligned(q, esz)) return SSM_ERR_INVALID_ARG;
+  if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_INVALID_ARG;
+  ssm::ConvParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.rows = batch * dim;
+  p.dim = static_cast<int>(dim);
+  p.seqlen = static_cast<int>(seqlen);
+  p.width = static_cast<int>(width);
+  p.silu = apply_silu ? 1 : 0;
+  p.x = x;
+  p.w = weight;
+  p.bias = bias;
+  p.state_in = conv_state;
+  p.out = out;
+  p.state_out = conv_state_out;
+  const bool vec = (seqlen * static_cast<int64_t>(esz)) % 16 == 0 && aligned(x, 16) &&
+                   aligned(out, 16);
+  return launch_conv1d_fwd(io == SSM_DTYPE_BF16, p, vec, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ssm_status ssm_conv1d_update(int64_t batch, int64_t dim, int64_t width, ssm_dtype io,
+                             void* conv_state, const void* x, const float* weight,
+                             const float* bias, int apply_silu, void* out, ssm_stream_t stream) {
+  ssm_status st = validate_common(batch, dim, 4, io);
+  if (st != SSM_OK) return st;
+  if (width < 1 || width > ssm::kConvMaxWidth) return SSM_ERR_UNSUPPORTED;
+  if (batch > (int64_t(1) << 40) / dim) return SSM_ERR_INVALID_ARG;
+  if (!x || !weight || !out || (width > 1 && !conv_state)) return SSM_ERR_INVALID_ARG;
+  const size_t esz = (io == SSM_DTYPE_BF16) ? 2 : 4;
+  const void* io_ptrs[3] = {x, out, conv_state};
+  for (const void* q : io_ptrs)
+    if (q && !aligned(q, esz)) return SSM_ERR_INVALID_ARG;
+  if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_INVALID_ARG;
+  ssm::ConvParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.rows = batch * dim;
+  p.dim = static_cast<int>(dim);
+  p.width = static_cast<int>(width);
+  p.silu = apply_silu ? 1 : 0;
+  p.x = x;
+  p.w = weight;
+  p.bias = bias;
+  p.out = out;
+  p.state = conv_state;
+  return launch_conv1d_update(io == SSM_DTYPE_BF16, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t stream) {
   if (!workspace || !aligned(workspace, 16)) return SSM_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -16,6 +16,7 @@
 #include "scan_channel.cuh"
 #include "scan_chunk.cuh"
 #include "state_update.cuh"
+#include "conv1d.cuh"
 
 namespace ssm_host {
 
@@ -318,5 +319,10 @@ ssm_status dispatch_scan_n(const ScanCall& c, ssm_algo algo, void* ws, cudaStrea
                            const SegPlan& seg, const MixPlan& mix);
 template <typename IO, int N, bool EULER>
 ssm_status dispatch_update_n(const ssm::UpdateParams& p, bool vec, cudaStream_t s);
+
+// Causal conv1d launches (defined in inst_conv.cu).  `vec`: x, out 16-byte aligned
+// and rows a multiple of 16 bytes long.
+ssm_status launch_conv1d_fwd(bool bf16, const ssm::ConvParams& p, bool vec, cudaStream_t s);
+ssm_status launch_conv1d_update(bool bf16, const ssm::ConvParams& p, cudaStream_t s);
 
 }  // namespace ssm_host

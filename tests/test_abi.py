@@ -171,6 +171,35 @@ def test_discretization_is_validated():
     assert lib.ssm_state_update_ex(*up, 3, None) == binding.SSM_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(width=0), binding.SSM_ERR_UNSUPPORTED),
+    (dict(width=9), binding.SSM_ERR_UNSUPPORTED),
+    (dict(seqlen=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(batch=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(io=5), binding.SSM_ERR_UNSUPPORTED),
+    (dict(x=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(w=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(out=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(x=P + 1), binding.SSM_ERR_INVALID_ARG),
+    (dict(w=P + 2), binding.SSM_ERR_INVALID_ARG),
+])
+def test_conv1d_validation(kw, expect):
+    lib = binding.library()
+    a = dict(batch=2, dim=8, seqlen=64, width=4, io=1, x=P, w=P, bias=None, state=None, silu=1,
+             out=P + 4096, state_out=None)
+    a.update(kw)
+    v = lambda q: None if q is None else ctypes.c_void_p(q)  # noqa: E731
+    st = lib.ssm_conv1d_fwd(a["batch"], a["dim"], a["seqlen"], a["width"], a["io"], v(a["x"]),
+                            v(a["w"]), v(a["bias"]), v(a["state"]), a["silu"], v(a["out"]),
+                            v(a["state_out"]), None)
+    assert st == expect
+    if "seqlen" not in kw:
+        st = lib.ssm_conv1d_update(a["batch"], a["dim"], a["width"], a["io"], v(P + 8192),
+                                   v(a["x"]), v(a["w"]), v(a["bias"]), a["silu"], v(a["out"]),
+                                   None)
+        assert st == expect
+
+
 def test_read_status_rejects_null():
     lib = binding.library()
     assert lib.ssm_read_device_status(None, None) == binding.SSM_ERR_INVALID_ARG
