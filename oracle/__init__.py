@@ -86,6 +86,11 @@ class Oracle:
         lib.oracle_state_update.argtypes = [_i64, _i64, _i64, _dp, _dp, _dp, _dp,
                                             ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp,
                                             ctypes.c_int]
+        lib.oracle_scan_bwd.restype = ctypes.c_int
+        lib.oracle_scan_bwd.argtypes = [_i64, _i64, _i64, _i64, _dp, _dp, _dp, ctypes.c_int,
+                                        _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                        _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int,
+                                        ctypes.c_int]
         lib.oracle_conv1d_fwd.restype = ctypes.c_int
         lib.oracle_conv1d_fwd.argtypes = [_i64, _i64, _i64, _i64, _dp, _dp, _dp, _dp,
                                           ctypes.c_int, _dp, _dp]
@@ -161,6 +166,36 @@ class Oracle:
         return y, h
 
 
+    def scan_bwd(self, u, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
+                 delta_softplus=True, h0=None, dh_last=None, nthreads: int = 1,
+                 discretization: str = "zoh"):
+        """Gradient of the scan in fp64 for the loss sum(dy * y) (+ sum(dh_last * h_last)).
+        Returns a dict with du, ddelta [b,d,l], dA [d,n], dB, dC [b,n,l], dD (when D),
+        dz (when z), ddelta_bias (when delta_bias), dh0 [b,d,n]."""
+        u, delta, A, B, C, dy = (_f64(a) for a in (u, delta, A, B, C, dy))
+        D, z, delta_bias, h0, dh_last = (_f64(a) for a in (D, z, delta_bias, h0, dh_last))
+        batch, dim, seqlen = u.shape
+        dstate = A.shape[1]
+        assert delta.shape == u.shape and dy.shape == u.shape and A.shape == (dim, dstate)
+        assert B.shape == (batch, dstate, seqlen) and C.shape == (batch, dstate, seqlen)
+        assert z is None or z.shape == u.shape
+        out = {"du": np.empty_like(u), "ddelta": np.empty_like(u),
+               "dA": np.empty((dim, dstate)), "dB": np.empty_like(B), "dC": np.empty_like(C),
+               "dD": np.empty(dim) if D is not None else None,
+               "dz": np.empty_like(u) if z is not None else None,
+               "ddelta_bias": np.empty(dim) if delta_bias is not None else None,
+               "dh0": np.empty((batch, dim, dstate))}
+        rc = self.lib.oracle_scan_bwd(batch, dim, dstate, seqlen, _ptr(u), _ptr(delta),
+                                      _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
+                                      _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(dy),
+                                      _ptr(dh_last), _ptr(out["du"]), _ptr(out["ddelta"]),
+                                      _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                                      _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]),
+                                      _ptr(out["dh0"]), int(nthreads), _euler(discretization))
+        if rc != 0:
+            raise RuntimeError("oracle_scan_bwd failed")
+        return out
+
     def conv1d_fwd(self, x, weight, bias=None, state_in=None, apply_silu=True,
                    return_state=False):
         """Causal depthwise convolution over time in fp64.  x [b,d,l]; weight [d,W];
@@ -214,6 +249,10 @@ def scan_rows(*args, **kwargs):
 
 def state_update(*args, **kwargs):
     return default().state_update(*args, **kwargs)
+
+
+def scan_bwd(*args, **kwargs):
+    return default().scan_bwd(*args, **kwargs)
 
 
 def conv1d_fwd(*args, **kwargs):

@@ -46,9 +46,10 @@
  *    section 4.2 (selective_scan: deltaB = delta * B, BX = deltaB * x), with the
  *    same Abar = exp(dt * A).
  *
- * The file also holds the causal depthwise convolution that precedes the scan in
- * the report's MambaBlock (oracle_conv1d_fwd, oracle_conv1d_update; definitions
- * and passages at the end).
+ * The file also holds the scan's gradient (oracle_scan_bwd, the reverse-mode
+ * derivative of the loop above, written out below) and the causal depthwise
+ * convolution that precedes the scan in the report's MambaBlock
+ * (oracle_conv1d_fwd, oracle_conv1d_update; definitions and passages at the end).
  *
  * Pinned by tests/test_oracle_pins.py against brute-force unrolled sums,
  * the LTI convolution form, a geometric-series closed form, the A -> 0 limit,
@@ -301,4 +302,241 @@ int oracle_conv1d_update(int64_t batch, int64_t dim, int64_t width, double* stat
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Gradient of the scan (reverse mode), for training.  Mamba_Model_Report.md
+ * section 4.1 gives the recurrence H[t] = A[t] H[t-1] + X[t] a backward pass
+ * built from a reverse scan (pscan_rev) that yields the gradients of A and X;
+ * "Mamba学习记录" (lengnian), Part3, lists recomputation of intermediate
+ * results among the hardware-aware algorithm's means.  The oracle is the chain
+ * rule applied to the loop of oracle_step, one position at a time in reverse,
+ * with every forward state kept (no recomputation needed at oracle sizes):
+ *
+ *   given dy[b,d,l] (and optionally dh_last[b,d,n]), with the forward states
+ *   h_l (h_{-1} = h0) of the channel kept in full:
+ *     g[n] = dh_last[n] (or 0)                        g = dLoss/dh_l
+ *     for l = L-1 .. 0:
+ *       y0   = sum_n C[n,l] h_l[n] + D u_l            (output before the gate)
+ *       dz_l = dy_l * y0 * silu'(z_l);  dy0 = dy_l * silu(z_l)   (no z: dy0 = dy_l)
+ *       dD  += dy0 u_l;  du_l = D dy0
+ *       for n:
+ *         g[n]      += C[n,l] dy0                     (y0 depends on h_l)
+ *         dC[n,l]   += dy0 h_l[n]                     (summed over the channels d)
+ *         h_l = Abar h_{l-1} + coef B u, so with p = g[n] h_{l-1}[n], r = g[n] B u:
+ *         dB[n,l]   += g[n] coef u                    (summed over d)
+ *         du_l      += g[n] coef B[n,l]
+ *         ddt       += p * dAbar/ddt + r * dcoef/ddt
+ *         dA[d,n]   += p * dAbar/da  + r * dcoef/da   (summed over b, l)
+ *         g[n]       = Abar g[n]                      (dLoss/dh_{l-1})
+ *       dx = ddt * softplus'(x) (= ddt * sigmoid(x); ddt without softplus)
+ *       ddelta_l = dx;  dbias[d] += dx
+ *     dh0 = g
+ *
+ * with Abar = exp(dt a): dAbar/ddt = a Abar, dAbar/da = dt Abar; and
+ * ZOH coef = expm1(dt a)/a: dcoef/ddt = Abar, dcoef/da = (dt Abar - coef)/a
+ * (at a == 0: coef = dt, dcoef/ddt = 1, dcoef/da = dt^2/2, the limit); Euler
+ * coef = dt: dcoef/ddt = 1, dcoef/da = 0.  For 0 < |dt a| < 1e-3, dcoef/da is
+ * taken from its Taylor series dt^2 (1/2 + q/3 + q^2/8 + q^3/30) (q = dt a;
+ * the first dropped term, q^4/144, is below 1e-14 of the sum) because the
+ * difference above cancels there.
+ * silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z))).
+ *
+ * Pinned by tests/pins.py: central finite differences of the forward oracle
+ * on every input, and the exact identities of a function linear in (u, h0),
+ * in B and in C.
+ * ------------------------------------------------------------------------ */
+static double oracle_sigmoid(double x)
+{
+    return 1.0 / (1.0 + exp(-x));
+}
+
+/* dcoef/da of the ZOH input coefficient coef = expm1(dt a)/a */
+static double oracle_dcoef_da(double dt, double a, double Abar, double coef)
+{
+    if (a == 0.0)
+        return 0.5 * dt * dt;
+    const double q = dt * a;
+    if (fabs(q) < 1e-3)
+        return dt * dt * (0.5 + q * (1.0 / 3.0 + q * (1.0 / 8.0 + q * (1.0 / 30.0))));
+    return (dt * Abar - coef) / a;
+}
+
+/* Backward of one channel (b, d).  hs is scratch of (L + 1) * dstate doubles;
+ * dB_acc, dC_acc ([batch, dstate, L]), dA_acc ([dim, dstate]), dD_acc, dbias_acc
+ * ([dim]) are accumulated into; du, ddelta, dz, dh0 are written for this row. */
+static void oracle_bwd_row(int64_t b, int64_t d, int64_t dim, int64_t dstate, int64_t seqlen,
+                           const double* u, const double* delta, const double* delta_bias,
+                           int delta_softplus, const double* A, const double* B,
+                           const double* C, const double* D, const double* z,
+                           const double* h0, const double* dy, const double* dh_last,
+                           double* du, double* ddelta, double* dz, double* dh0,
+                           double* dA_acc, double* dB_acc, double* dC_acc, double* dD_acc,
+                           double* dbias_acc, double* hs, double* g, int euler)
+{
+    const int64_t row = b * dim + d;
+    const double bias = delta_bias ? delta_bias[d] : 0.0;
+    const double Dd = D ? D[d] : 0.0;
+    const double* Arow = A + d * dstate;
+    const double* Bb = B + b * dstate * seqlen;
+    const double* Cb = C + b * dstate * seqlen;
+
+    /* forward, keeping every state: hs[(l + 1) * dstate + n] = h_l[n] */
+    for (int64_t n = 0; n < dstate; ++n)
+        hs[n] = h0 ? h0[row * dstate + n] : 0.0;
+    for (int64_t l = 0; l < seqlen; ++l) {
+        const int64_t i = row * seqlen + l;
+        const double x = delta[i] + bias;
+        const double dt = delta_softplus ? oracle_softplus(x) : x;
+        for (int64_t n = 0; n < dstate; ++n) {
+            const double a = Arow[n];
+            const double Abar = exp(dt * a);
+            const double coef = euler ? dt : (a == 0.0 ? dt : expm1(dt * a) / a);
+            hs[(l + 1) * dstate + n] = Abar * hs[l * dstate + n] + coef * Bb[n * seqlen + l] * u[i];
+        }
+    }
+
+    /* reverse */
+    for (int64_t n = 0; n < dstate; ++n)
+        g[n] = dh_last ? dh_last[row * dstate + n] : 0.0;
+    for (int64_t l = seqlen - 1; l >= 0; --l) {
+        const int64_t i = row * seqlen + l;
+        const double x = delta[i] + bias;
+        const double dt = delta_softplus ? oracle_softplus(x) : x;
+        const double* h_l = hs + (l + 1) * dstate;
+        const double* h_prev = hs + l * dstate;
+        double y0 = Dd * u[i];
+        for (int64_t n = 0; n < dstate; ++n)
+            y0 += Cb[n * seqlen + l] * h_l[n];
+        double dy0 = dy[i];
+        if (z) {
+            const double sg = oracle_sigmoid(z[i]);
+            dz[i] = dy[i] * y0 * sg * (1.0 + z[i] * (1.0 - sg));
+            dy0 = dy[i] * z[i] * sg;
+        }
+        dD_acc[d] += dy0 * u[i];
+        double du_l = Dd * dy0;
+        double ddt = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) {
+            const double a = Arow[n];
+            const double Bv = Bb[n * seqlen + l];
+            g[n] += Cb[n * seqlen + l] * dy0;
+            dC_acc[b * dstate * seqlen + n * seqlen + l] += dy0 * h_l[n];
+            const double Abar = exp(dt * a);
+            double coef, dcoef_ddt, dcoef_da;
+            if (euler) {
+                coef = dt;
+                dcoef_ddt = 1.0;
+                dcoef_da = 0.0;
+            } else if (a == 0.0) {
+                coef = dt;
+                dcoef_ddt = 1.0;
+                dcoef_da = oracle_dcoef_da(dt, a, Abar, coef);
+            } else {
+                coef = expm1(dt * a) / a;
+                dcoef_ddt = Abar;
+                dcoef_da = oracle_dcoef_da(dt, a, Abar, coef);
+            }
+            const double p = g[n] * h_prev[n];
+            const double r = g[n] * Bv * u[i];
+            dB_acc[b * dstate * seqlen + n * seqlen + l] += g[n] * coef * u[i];
+            du_l += g[n] * coef * Bv;
+            ddt += p * a * Abar + r * dcoef_ddt;
+            dA_acc[d * dstate + n] += p * dt * Abar + r * dcoef_da;
+            g[n] = Abar * g[n];
+        }
+        const double dx = delta_softplus ? ddt * oracle_sigmoid(x) : ddt;
+        ddelta[i] = dx;
+        dbias_acc[d] += dx;
+        du[i] = du_l;
+    }
+    if (dh0)
+        for (int64_t n = 0; n < dstate; ++n)
+            dh0[row * dstate + n] = g[n];
+}
+
+/* Gradient of the full scan.  Per-row outputs du, ddelta [b,d,l], dz [b,d,l]
+ * (when z), dh0 [b,d,n] (optional); reductions dA [d,n], dB, dC [b,n,l], dD,
+ * ddelta_bias [d] (each optional except dB, dC, dA).  Rows are spread over
+ * `nthreads` threads with private accumulators summed in thread order at the end.
+ * Returns 0 on success, -1 on bad sizes or allocation failure. */
+int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                    const double* u, const double* delta, const double* delta_bias,
+                    int delta_softplus, const double* A, const double* B, const double* C,
+                    const double* D, const double* z, const double* h0, const double* dy,
+                    const double* dh_last, double* du, double* ddelta, double* dA, double* dB,
+                    double* dC, double* dD, double* dz, double* ddelta_bias, double* dh0,
+                    int nthreads, int euler)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0 || seqlen < 0)
+        return -1;
+    const int64_t rows = batch * dim;
+    const size_t nbc = (size_t)(batch * dstate * seqlen), na = (size_t)(dim * dstate);
+    if (nthreads < 1)
+        nthreads = 1;
+#ifndef _OPENMP
+    nthreads = 1;
+#endif
+    /* private accumulators: [thread][dA | dB | dC | dD | dbias] */
+    const size_t per = na + 2 * nbc + 2 * (size_t)dim;
+    double* acc = (double*)calloc(per * (size_t)nthreads, sizeof(double));
+    if (!acc)
+        return -1;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+    {
+        int t = 0;
+#ifdef _OPENMP
+        t = omp_get_thread_num();
+#endif
+        double* mine = acc + per * (size_t)t;
+        double* hs = (double*)malloc(sizeof(double) * (size_t)((seqlen + 1) * dstate));
+        double* g = (double*)malloc(sizeof(double) * (size_t)dstate);
+        if (!hs || !g) {
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+            for (int64_t r = 0; r < rows; ++r)
+                oracle_bwd_row(r / dim, r % dim, dim, dstate, seqlen, u, delta, delta_bias,
+                               delta_softplus, A, B, C, D, z, h0, dy, dh_last, du, ddelta, dz,
+                               dh0, mine, mine + na, mine + na + nbc, mine + na + 2 * nbc,
+                               mine + na + 2 * nbc + dim, hs, g, euler);
+        }
+        free(hs);
+        free(g);
+    }
+    if (!failed) {
+        for (size_t k = 0; k < na; ++k) {
+            double s = 0.0;
+            for (int t = 0; t < nthreads; ++t)
+                s += acc[per * (size_t)t + k];
+            dA[k] = s;
+        }
+        for (size_t k = 0; k < nbc; ++k) {
+            double sb = 0.0, sc = 0.0;
+            for (int t = 0; t < nthreads; ++t) {
+                sb += acc[per * (size_t)t + na + k];
+                sc += acc[per * (size_t)t + na + nbc + k];
+            }
+            dB[k] = sb;
+            dC[k] = sc;
+        }
+        for (int64_t k = 0; k < dim; ++k) {
+            double sd = 0.0, sbias = 0.0;
+            for (int t = 0; t < nthreads; ++t) {
+                sd += acc[per * (size_t)t + na + 2 * nbc + (size_t)k];
+                sbias += acc[per * (size_t)t + na + 2 * nbc + (size_t)dim + (size_t)k];
+            }
+            if (dD)
+                dD[k] = sd;
+            if (ddelta_bias)
+                ddelta_bias[k] = sbias;
+        }
+    }
+    free(acc);
+    return failed ? -1 : 0;
 }

@@ -28,6 +28,11 @@ Sources of each fact:
   * causal depthwise conv1d (groups = channels, padding W - 1, first L outputs)
     then silu, and its decode cache of the last W - 1 inputs:
     Mamba_Model_Report.md, sections 3 (MambaBlock.forward) and 6 (step).
+  * the scan's gradient (Mamba_Model_Report.md, section 4.1: the backward of
+    the recurrence through a reverse scan) is the derivative of the forward:
+    central finite differences of the pinned forward oracle fix every partial
+    derivative; a function linear in some inputs equals the sum of each input
+    times its gradient (Euler's theorem on homogeneous functions), exactly.
 """
 from __future__ import annotations
 
@@ -409,8 +414,126 @@ def pin_conv1d_state_and_step(orc):
            what="first position, zero history")
 
 
+# ---------------------------------------------------------------------------
+# gradient of the scan
+# ---------------------------------------------------------------------------
+def _bwd_case(seed, euler=False, softplus=True, gate=True, skip=True):
+    rng = _rng(seed)
+    b, d, n, L = 2, 3, 4, 6
+    case = {
+        "u": rng.standard_normal((b, d, L)),
+        "delta": (rng.standard_normal((b, d, L)) if softplus
+                  else rng.uniform(0.05, 0.8, size=(b, d, L))),
+        "A": -rng.uniform(0.5, 3.0, size=(d, n)),
+        "B": rng.standard_normal((b, n, L)),
+        "C": rng.standard_normal((b, n, L)),
+        "D": rng.standard_normal(d) if skip else None,
+        "z": rng.standard_normal((b, d, L)) if gate else None,
+        "delta_bias": rng.uniform(-1.0, 0.5, size=d),
+        "h0": rng.standard_normal((b, d, n)) * 0.5,
+    }
+    # the A -> 0 limit and the small-|dt A| series branch of dcoef/dA
+    case["A"][0, 1] = 0.0
+    case["A"][1, 2] = -5e-4
+    case["A"][2, 0] = 3e-4
+    dy = rng.standard_normal((b, d, L))
+    dhl = rng.standard_normal((b, d, n))
+    return case, dy, dhl, dict(delta_softplus=softplus,
+                               discretization="euler" if euler else "zoh")
+
+
+def _loss(orc, case, dy, dhl, kw):
+    y, hl = orc.scan_fwd(case["u"], case["delta"], case["A"], case["B"], case["C"],
+                         D=case["D"], z=case["z"], delta_bias=case["delta_bias"],
+                         h0=case["h0"], return_last_state=True, **kw)
+    return float(np.sum(dy * y) + np.sum(dhl * hl))
+
+
+def pin_bwd_finite_differences(orc):
+    """Every gradient against central differences of the forward oracle's
+    loss sum(dy * y) + sum(dh_last * h_last), with and without each option."""
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
+    variants = [dict(), dict(euler=True), dict(softplus=False, gate=False, skip=False)]
+    for k, var in enumerate(variants):
+        case, dy, dhl, kw = _bwd_case(40 + k, **var)
+        g = orc.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dy,
+                         D=case["D"], z=case["z"], delta_bias=case["delta_bias"],
+                         h0=case["h0"], dh_last=dhl, **kw)
+        for key, gname in names.items():
+            if case[key] is None:
+                continue
+            x = case[key]
+            fd = np.empty_like(x)
+            for i in range(x.size):
+                old = x.flat[i]
+                step = 1e-6 * max(1.0, abs(old))
+                x.flat[i] = old + step
+                fp = _loss(orc, case, dy, dhl, kw)
+                x.flat[i] = old - step
+                fm = _loss(orc, case, dy, dhl, kw)
+                x.flat[i] = old
+                fd.flat[i] = (fp - fm) / (2 * step)
+            _close(g[gname], fd, rtol=1e-6, atol=2e-7, what=f"{gname} vs finite differences "
+                                                              f"({var or 'zoh, all options'})")
+
+
+def pin_bwd_homogeneity(orc):
+    """Exact identities: the loss is linear in (u, h0) jointly, in B (h0 = 0) and
+    in C (no D, dh_last = 0), so it equals sum(input * gradient) over those."""
+    for k, euler in enumerate((False, True)):
+        case, dy, dhl, kw = _bwd_case(50 + k, euler=euler)
+        f = _loss(orc, case, dy, dhl, kw)
+        g = orc.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dy,
+                         D=case["D"], z=case["z"], delta_bias=case["delta_bias"],
+                         h0=case["h0"], dh_last=dhl, **kw)
+        _close(np.sum(g["du"] * case["u"]) + np.sum(g["dh0"] * case["h0"]), f, rtol=1e-12,
+               atol=1e-12, what="linear in (u, h0)")
+        case["h0"] = np.zeros_like(case["h0"])
+        case["D"] = None
+        f = _loss(orc, case, dy, dhl, kw)
+        g = orc.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dy,
+                         z=case["z"], delta_bias=case["delta_bias"], h0=case["h0"],
+                         dh_last=dhl, **kw)
+        _close(np.sum(g["dB"] * case["B"]), f, rtol=1e-12, atol=1e-12, what="linear in B")
+        f = _loss(orc, case, dy, np.zeros_like(dhl), kw)
+        g = orc.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dy,
+                         z=case["z"], delta_bias=case["delta_bias"], h0=case["h0"], **kw)
+        _close(np.sum(g["dC"] * case["C"]), f, rtol=1e-12, atol=1e-12, what="linear in C")
+
+
+def pin_bwd_split_chain(orc):
+    """The gradient over [0, L) equals the gradient over [m, L) chained into the
+    one over [0, m) through the state at m (its dh0 becomes the first part's
+    dh_last)."""
+    case, dy, dhl, kw = _bwd_case(60)
+    m = 2
+    c = {k: case[k] for k in ("A", "D", "delta_bias")}
+    full = orc.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dy,
+                        D=case["D"], z=case["z"], delta_bias=case["delta_bias"], h0=case["h0"],
+                        dh_last=dhl, **kw)
+    _, hm = orc.scan_fwd(case["u"][..., :m], case["delta"][..., :m], case["A"],
+                         case["B"][..., :m], case["C"][..., :m], D=case["D"],
+                         z=case["z"][..., :m], delta_bias=case["delta_bias"], h0=case["h0"],
+                         return_last_state=True, **kw)
+    part = lambda sl, h0, dh: orc.scan_bwd(  # noqa: E731
+        case["u"][..., sl], case["delta"][..., sl], c["A"], case["B"][..., sl],
+        case["C"][..., sl], dy[..., sl], D=c["D"], z=case["z"][..., sl],
+        delta_bias=c["delta_bias"], h0=h0, dh_last=dh, **kw)
+    second = part(slice(m, None), hm, dhl)
+    first = part(slice(0, m), case["h0"], second["dh0"])
+    for key in ("du", "ddelta", "dz", "dB", "dC"):
+        _close(np.concatenate([first[key], second[key]], axis=-1), full[key], rtol=1e-12,
+               atol=1e-13, what=f"split {key}")
+    for key in ("dA", "dD", "ddelta_bias"):
+        _close(first[key] + second[key], full[key], rtol=1e-12, atol=1e-13,
+               what=f"split {key}")
+    _close(first["dh0"], full["dh0"], rtol=1e-12, atol=1e-13, what="split dh0")
+
+
 ALL_PINS = [pin_zoh_matches_ode, pin_unrolled_sum, pin_lti_convolution, pin_geometric_series,
             pin_zoh_small_A, pin_linearity, pin_softplus_bias_gate, pin_step_equals_scan,
             pin_split_invariance, pin_rows_match_full, pin_euler_unrolled_sum,
             pin_euler_geometric_and_first_order, pin_conv1d_matches_convolution,
-            pin_conv1d_state_and_step]
+            pin_conv1d_state_and_step, pin_bwd_finite_differences, pin_bwd_homogeneity,
+            pin_bwd_split_chain]

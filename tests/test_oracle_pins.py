@@ -23,7 +23,8 @@ def test_oracle_pin(orc, pin):
 MUTANTS = [
     ("euler_instead_of_zoh",
      "double coef = (a == 0.0) ? dt : expm1(dt * a) / a;", "double coef = dt;"),
-    ("sign_of_Abar", "double Abar = exp(dt * a);", "double Abar = exp(-dt * a);"),
+    ("sign_of_Abar", "double a = A_row[n];\n        double Abar = exp(dt * a);",
+     "double a = A_row[n];\n        double Abar = exp(-dt * a);"),
     ("exclusive_output_convention",
      "h[n] = Abar * h[n] + coef * B_col[n * bc_stride] * u;\n"
      "        acc += C_col[n * bc_stride] * h[n];",
@@ -45,7 +46,12 @@ MUTANTS = [
     ("softplus_branch", "return x + log1p(exp(-x));", "return x + log1p(exp(x));"),
     ("dropped_input_u", "coef * B_col[n * bc_stride] * u;\n        acc",
      "coef * B_col[n * bc_stride];\n        acc"),
-    ("expm1_without_divide", "expm1(dt * a) / a;", "expm1(dt * a);"),
+    ("expm1_without_divide", "(a == 0.0) ? dt : expm1(dt * a) / a;",
+     "(a == 0.0) ? dt : expm1(dt * a);"),
+    ("bwd_forward_expm1_without_divide", "(a == 0.0 ? dt : expm1(dt * a) / a);",
+     "(a == 0.0 ? dt : expm1(dt * a));"),
+    ("bwd_reverse_expm1_without_divide", "                coef = expm1(dt * a) / a;",
+     "                coef = expm1(dt * a);"),
     ("decode_stride", "A + d * dstate, B + b * dstate, C + b * dstate, 1,",
      "A + d * dstate, B + b * dstate, C + b * dstate, dstate,"),
     ("euler_coef_times_A", "        if (euler)\n            coef = dt;",
@@ -66,6 +72,25 @@ MUTANTS = [
      "                out[row * seqlen + l] = apply_silu ? oracle_silu(acc) : acc;",
      "                out[row * seqlen + l] = apply_silu ? oracle_silu(acc - (bias ? bias[d] : 0.0))"
      " + (bias ? bias[d] : 0.0) : acc;"),
+    ("bwd_no_state_decay", "            g[n] = Abar * g[n];", "            g[n] = g[n];"),
+    ("bwd_h_l_for_h_prev", "const double p = g[n] * h_prev[n];", "const double p = g[n] * h_l[n];"),
+    ("bwd_no_softplus_derivative", "ddt * oracle_sigmoid(x) : ddt;", "ddt : ddt;"),
+    ("bwd_dcoef_ddt_one", "                dcoef_ddt = Abar;", "                dcoef_ddt = 1.0;"),
+    ("bwd_dC_from_h_prev", "+= dy0 * h_l[n];", "+= dy0 * h_prev[n];"),
+    ("bwd_gate_derivative_sigmoid_only", "dy[i] * y0 * sg * (1.0 + z[i] * (1.0 - sg));",
+     "dy[i] * y0 * sg;"),
+    ("bwd_series_coefficient", "q * (1.0 / 3.0 + q", "q * (1.0 / 6.0 + q"),
+    ("bwd_dA_without_Abar", "p * dt * Abar + r * dcoef_da", "p * dt + r * dcoef_da"),
+    ("bwd_dh_last_ignored", "g[n] = dh_last ? dh_last[row * dstate + n] : 0.0;", "g[n] = 0.0;"),
+    ("bwd_dB_without_u", "+= g[n] * coef * u[i];", "+= g[n] * coef;"),
+    ("bwd_dD_before_gate", "dD_acc[d] += dy0 * u[i];", "dD_acc[d] += dy[i] * u[i];"),
+    ("bwd_bias_grad_dropped", "        dbias_acc[d] += dx;\n", ""),
+    ("bwd_euler_dcoef_ddt", "                coef = dt;\n                dcoef_ddt = 1.0;\n"
+     "                dcoef_da = 0.0;",
+     "                coef = dt;\n                dcoef_ddt = Abar;\n                dcoef_da = 0.0;"),
+    ("bwd_zero_A_limit", "        return 0.5 * dt * dt;", "        return 0.0;"),
+    ("bwd_gate_grad_before_contraction", "        double y0 = Dd * u[i];", "        double y0 = 0.0;"),
+    ("bwd_du_missing_skip", "double du_l = Dd * dy0;", "double du_l = 0.0;"),
 ]
 
 
