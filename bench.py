@@ -382,6 +382,23 @@ def run_gpu(args):
     # ---- decode state update (rank 0's measurement)
     decode = run_decode(dev, S) if (rank == 0 and not args.no_decode) else None
     conv = run_conv(dev, S) if (rank == 0 and not args.no_decode) else None
+    euler = None
+    if rank == 0 and not args.no_decode:
+        # the same scan with the Euler input term (Bbar = dt B)
+        def step_euler():
+            S.scan_fwd(u, dl, A, B, C, D=Dv, z=z, delta_bias=bias, algo=args.algo, out=y,
+                       discretization="euler")
+        for _ in range(3):
+            step_euler()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(50):
+            step_euler()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_e = ev0.elapsed_time(ev1) / 50
+        euler = {"ms_per_step": ms_e, "value": elems / (ms_e * 1e-3), "unit": "elements/s",
+                 "roofline_frac": CFG.updates / (ms_e * 1e-3) / 1e12 / ex2_peak}
     barrier(world)
 
     # ---- CPU baseline (rank 0, N = 1 only)
@@ -420,6 +437,8 @@ def run_gpu(args):
             line["decode"] = decode
         if conv:
             line["conv1d"] = conv
+        if euler:
+            line["scan_euler"] = euler
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
