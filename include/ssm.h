@@ -236,6 +236,50 @@ SSM_API ssm_status ssm_state_update_ex(int64_t batch, int64_t dim, int64_t dstat
                                        ssm_discretization disc, ssm_stream_t stream);
 
 /*
+ * Gradient of ssm_scan_fwd (reverse mode), for training.
+ *
+ * Given dy = dLoss/dy [batch, dim, seqlen] (and optionally dh_last =
+ * dLoss/dh_last [batch, dim, dstate]), returns the gradients of every input of
+ * the scan: Mamba_Model_Report.md section 4.1 builds the recurrence's backward
+ * from a reverse scan (pscan_rev) over the adjoint g_l = dLoss/dh_l, and
+ * "Mamba学习记录" (lengnian), Part3, lists recomputation of intermediate results
+ * among the hardware-aware algorithm's means: the states are recomputed from
+ * checkpoints here, not stored by the forward pass.
+ *
+ *  forward inputs   exactly as passed to ssm_scan_fwd (u, delta, delta_bias,
+ *                   delta_softplus, A, B, C, D, z, h0; same dtypes and layouts)
+ *  dy               [batch, dim, seqlen] io dtype, required
+ *  dh_last          [batch, dim, dstate] float32 or NULL (zero)
+ *  du, ddelta       [batch, dim, seqlen] io dtype, required (overwritten)
+ *  dA               [dim, dstate] float32, required
+ *  dB, dC           [batch, dstate, seqlen] io dtype, required
+ *  dD               [dim] float32; required iff D is given, else ignored
+ *  dz               [batch, dim, seqlen] io dtype; required iff z is given
+ *  ddelta_bias      [dim] float32 or NULL (not computed)
+ *  dh0              [batch, dim, dstate] float32 or NULL (not computed)
+ *  workspace        ssm_scan_bwd_workspace_size(...) bytes, 256-byte aligned;
+ *                   its contents need not be preserved between calls
+ *  disc             the discretisation the forward used
+ *
+ * Outputs must not overlap inputs or each other.  The reductions over channels
+ * (dB, dC) and over batch rows and positions (dA, dD, ddelta_bias) are summed in
+ * a fixed order: results are bit-reproducible for a given shape.  Arithmetic is
+ * fp32; bf16 outputs are rounded to nearest even.  Validated on the host first
+ * (nothing is enqueued when a check fails); enqueued on `stream`.
+ */
+SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                           int64_t seqlen);
+SSM_API ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                ssm_dtype io, const void* u, const void* delta,
+                                const float* delta_bias, int delta_softplus, const float* A,
+                                const void* B, const void* C, const float* D, const void* z,
+                                const float* h0, const void* dy, const float* dh_last, void* du,
+                                void* ddelta, float* dA, void* dB, void* dC, float* dD, void* dz,
+                                float* ddelta_bias, float* dh0, void* workspace,
+                                size_t workspace_bytes, ssm_discretization disc,
+                                ssm_stream_t stream);
+
+/*
  * Causal depthwise convolution over time, the step before the scan in the
  * MambaBlock of Mamba_Model_Report.md (section 3: nn.Conv1d with groups = channels,
  * kernel_size = width, padding = width - 1, the first L outputs, then silu):

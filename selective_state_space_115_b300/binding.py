@@ -47,7 +47,7 @@ _ALGOS.update({v: v for v in list(_ALGOS.values())})
 # every symbol include/ssm.h declares
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "ssm_scan_fwd",
             "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_conv1d_fwd",
-            "ssm_conv1d_update",
+            "ssm_conv1d_update", "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -111,6 +111,11 @@ def library(path: Optional[str] = None):
         lib.ssm_conv1d_update.restype = _int
         lib.ssm_conv1d_update.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int, _vp,
                                           _vp]
+        lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_bwd_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
+        lib.ssm_scan_bwd.restype = _int
+        lib.ssm_scan_bwd.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
+                                     + [_vp] * 18 + [ctypes.c_size_t, _int, _vp])
         lib.ssm_read_device_status.restype = _int
         lib.ssm_read_device_status.argtypes = [_vp, _vp]
         lib.ssm_status_string.restype = ctypes.c_char_p
@@ -226,6 +231,68 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                                  ctypes.c_void_p(stream))
     _check(st, "ssm_scan_fwd")
     return (y, h_last) if return_last_state else y
+
+
+_bwd_ws_cache = {}
+
+
+def scan_bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
+    return int(library().ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen))
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True,
+             h0=None, dh_last=None, want_dh0=True, discretization="zoh", workspace=None):
+    """Gradient of scan_fwd for the upstream gradient dy [batch, dim, seqlen] (and
+    dh_last [batch, dim, dstate] float32 for the final state).  Takes the forward's
+    inputs as passed to scan_fwd.  Returns a dict: du, ddelta, dz (io dtype,
+    [batch, dim, seqlen]); dB, dC (io dtype, [batch, dstate, seqlen]); dA [dim, dstate],
+    dD [dim] (when D), ddelta_bias [dim] (when delta_bias), dh0 [batch, dim, dstate]
+    (when want_dh0), all float32."""
+    if not isinstance(u, torch.Tensor) or not u.is_cuda:
+        raise SsmError(SSM_ERR_INVALID_ARG, "u must be a CUDA tensor")
+    if u.dim() != 3:
+        raise SsmError(SSM_ERR_INVALID_ARG, "u must be [batch, dim, seqlen]")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    dev = u.device
+    io = _io_dtype(u)
+    for t, name, shape in ((delta, "delta", (batch, dim, seqlen)), (dy, "dy", (batch, dim, seqlen)),
+                           (B, "B", (batch, dstate, seqlen)), (C, "C", (batch, dstate, seqlen))):
+        _need(t, name, shape, u.dtype, dev)
+    _need(z, "z", (batch, dim, seqlen), u.dtype, dev, optional=True)
+    _need(A, "A", (dim, dstate), torch.float32, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    _need(h0, "h0", (batch, dim, dstate), torch.float32, dev, optional=True)
+    _need(dh_last, "dh_last", (batch, dim, dstate), torch.float32, dev, optional=True)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dz": torch.empty_like(u) if z is not None else None,
+         "dB": torch.empty_like(B), "dC": torch.empty_like(C),
+         "dA": torch.empty((dim, dstate), **f32),
+         "dD": torch.empty((dim,), **f32) if D is not None else None,
+         "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
+         "dh0": torch.empty((batch, dim, dstate), **f32) if want_dh0 else None}
+    lib = library()
+    nbytes = int(lib.ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen))
+    if workspace is None:
+        ws = _bwd_ws_cache.get(dev.index)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+            _bwd_ws_cache[dev.index] = ws
+    else:
+        ws = workspace
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_bwd(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                              _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
+                              _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(dy), _ptr(dh_last),
+                              _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                              _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]),
+                              _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), _ptr(ws), ws.numel(),
+                              _DISC[discretization], ctypes.c_void_p(stream))
+    _check(st, "ssm_scan_bwd")
+    return g
 
 
 def read_device_status(workspace: Optional[torch.Tensor] = None, device=None) -> int:

@@ -1,0 +1,69 @@
+// inst_bwd.cuh -- launches of the scan-gradient kernels, instantiated per io type
+// by inst_bwd_bf16.cu and inst_bwd_f32.cu.
+#pragma once
+
+#include "ssm_host.cuh"
+
+namespace ssm_host {
+
+template <typename IO, int N, bool GATE, bool EULER, bool VEC>
+static ssm_status bwd_main(const ssm::BwdParams& p, cudaStream_t s) {
+  using Cfg = ssm::BwdCfg<IO, N, GATE, EULER, VEC, kBwdThreads>;
+  auto kern = ssm::scan_bwd_kernel<Cfg>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  });
+  if (attr != cudaSuccess) return cuda_fail(attr, "scan_bwd smem attribute");
+  const int64_t grid = p.batch * p.tiles;
+  if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;
+  kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM, s>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "scan_bwd launch");
+  return SSM_OK;
+}
+
+template <typename IO, int N>
+static ssm_status bwd_main_n(const ssm::BwdParams& p, bool gate, bool euler, bool vec,
+                             cudaStream_t s) {
+  if (gate) {
+    if (euler) return vec ? bwd_main<IO, N, true, true, true>(p, s) : bwd_main<IO, N, true, true, false>(p, s);
+    return vec ? bwd_main<IO, N, true, false, true>(p, s) : bwd_main<IO, N, true, false, false>(p, s);
+  }
+  if (euler) return vec ? bwd_main<IO, N, false, true, true>(p, s) : bwd_main<IO, N, false, true, false>(p, s);
+  return vec ? bwd_main<IO, N, false, false, true>(p, s) : bwd_main<IO, N, false, false, false>(p, s);
+}
+
+template <typename IO>
+ssm_status launch_scan_bwd(const ssm::BwdParams& p, int dstate, bool gate, bool euler, bool vec,
+                           void* dB, void* dC, float* dA, float* dD, float* dbias,
+                           cudaStream_t s) {
+  ssm_status st = SSM_OK;
+  if (p.batch * p.dim > 0) {
+    switch (dstate) {
+      case 4: st = bwd_main_n<IO, 4>(p, gate, euler, vec, s); break;
+      case 8: st = bwd_main_n<IO, 8>(p, gate, euler, vec, s); break;
+      case 16: st = bwd_main_n<IO, 16>(p, gate, euler, vec, s); break;
+      default: return SSM_ERR_UNSUPPORTED;
+    }
+    if (st != SSM_OK) return st;
+  }
+  const int64_t nbc = p.batch * 2 * dstate * static_cast<int64_t>(p.seqlen);
+  if (nbc > 0) {
+    ssm::scan_bwd_reduce_bc_kernel<IO><<<static_cast<unsigned>((nbc + 255) / 256), 256, 0, s>>>(
+        p.part_bc, p.tiles, p.batch, dstate, p.seqlen, static_cast<IO*>(dB), static_cast<IO*>(dC));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "scan_bwd reduce launch");
+  }
+  const int64_t npar = static_cast<int64_t>(p.dim) * dstate + p.dim;
+  if (npar > 0) {
+    ssm::scan_bwd_reduce_param_kernel<><<<static_cast<unsigned>((npar + 255) / 256), 256, 0, s>>>(
+        p.part_a, p.part_dd, p.batch, p.dim, dstate, dA, dD, dbias);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "scan_bwd reduce launch");
+  }
+  return SSM_OK;
+}
+
+}  // namespace ssm_host

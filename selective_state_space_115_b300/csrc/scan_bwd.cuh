@@ -1,0 +1,669 @@
+// scan_bwd.cuh -- gradient of the selective scan (reverse mode), for training.
+//
+// Mamba_Model_Report.md, section 4.1, differentiates the recurrence
+// H[t] = A[t] H[t-1] + X[t] with a reverse scan (pscan_rev): the adjoint
+// g_l = dLoss/dh_l runs from the end, g_{l-1} = Abar_l g_l + (terms of l-1), and
+// each position's partials follow from g_l and the state before it.  With the
+// ZOH step h_l = Abar h_{l-1} + coef B u (Abar = exp(dt A), coef = expm1(dt A)/A)
+// the partials per (channel, position, state) are
+//
+//   dC  += dy0 h_l                 dB += g coef u          du += g coef B
+//   ddt += Abar g (A h_{l-1} + B u)                   (Euler: A Abar g h_{l-1} + g B u)
+//   dA  += g (dt Abar h_{l-1} + dcoef/dA B u)         (Euler: dcoef/dA = 0)
+//
+// with dy0 the gradient of the output before the silu gate, and ddelta = ddt *
+// sigmoid(delta + bias) through the softplus.  "Mamba学习记录" (lengnian), Part3,
+// names recomputation among the hardware-aware algorithm's means of keeping
+// intermediate results cheap: the states are not stored by the forward pass but
+// recomputed here.
+//
+// Layout and schedule (one CTA = THREADS/4 channels of one batch row, four lanes
+// per channel, each lane owning N/4 states):
+//   phase 1  forward over the whole sequence, writing the state entering every
+//            block of 16 positions to a workspace checkpoint [block][row][N];
+//   phase 2  blocks in reverse: recompute the block's 16 states per lane into
+//            registers from its checkpoint, then run the adjoint backwards
+//            through the block.
+// u, delta, z, dy stream through a two-stage shared-memory ring filled by
+// cp.async; B and C are prefetched into registers one block ahead and parked in
+// shared memory as fp32 [position][state].  dB and dC are sums over the channels:
+// each warp reduce-scatters its 8 channels with shuffles, the CTA sums its warps
+// through shared memory and writes one partial per (CTA, batch row, state,
+// position); a second kernel adds the partials of a batch row in a fixed order,
+// so the result does not depend on scheduling.  dA, dD and the bias gradient are
+// per-channel sums over positions, added over the batch rows by that kernel.
+#pragma once
+
+#include "ssm_device.cuh"
+
+namespace ssm {
+
+constexpr int kBwdPos = 16;  // positions per block = checkpoint stride
+constexpr int kBwdLpc = 4;   // lanes per channel
+
+struct BwdParams {
+  int64_t batch;
+  int dim, seqlen, nblk, tiles;  // tiles: CTAs per batch row
+  int softplus;
+  const void* u;
+  const void* delta;
+  const void* z;
+  const void* dy;
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;
+  const float* bias;
+  const float* h0;
+  const float* dh_last;
+  void* du;
+  void* ddelta;
+  void* dz;
+  float* dh0;
+  float* ckpt;     // [nblk][batch * dim][N]: state entering each block
+  float* part_bc;  // [tiles][batch][2][N][seqlen]: per-CTA partial dB (0), dC (1)
+  float* part_a;   // [batch * dim][N]: per-channel dA
+  float* part_dd;  // [batch * dim][2]: per-channel dD, bias gradient
+};
+
+template <typename IO, int N_, bool GATE_, bool EULER_, bool VEC_, int THREADS_ = 128>
+struct BwdCfg {
+  using io_t = IO;
+  static constexpr int N = N_, NS = N_ / kBwdLpc;
+  static constexpr bool GATE = GATE_, EULER = EULER_;
+  static constexpr bool VEC = VEC_;  // 16-byte aligned rows: cp.async staging, vector stores
+  static constexpr int THREADS = THREADS_, WARPS = THREADS_ / 32, CH = THREADS_ / kBwdLpc;
+  static constexpr int ES = sizeof(IO);
+  static constexpr int ROWB = kBwdPos * ES;  // one channel's block row (bytes)
+  static constexpr int CHB = CH * ROWB;      // one per-channel tile: [CH][16]
+  static constexpr int STAGE = 4 * CHB;      // u, delta, z, dy
+  static constexpr int BCS = N + 4;          // row of the fp32 B / C tile (padded)
+  static constexpr int BCB = 2 * kBwdPos * BCS * 4;
+  static constexpr int SCS = 20;             // per-channel row of S / SG / DY0 (padded)
+  static constexpr int REDS = kBwdPos * 8 + 4;  // per-channel stride of RED (padded)
+  static constexpr int WBS = kBwdPos + 1;       // position row of WB (padded)
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_BC = OFF_STAGE + 2 * STAGE;
+  static constexpr int OFF_S = OFF_BC + 2 * BCB;
+  static constexpr int OFF_SG = OFF_S + CH * SCS * 4;
+  static constexpr int OFF_DY0 = OFF_SG + CH * SCS * 4;
+  static constexpr int OFF_RED = OFF_DY0 + CH * SCS * 4;
+  static constexpr int OFF_WB = OFF_RED + CH * REDS * 4;
+  static constexpr int OFF_OUT = OFF_WB + WARPS * 2 * N * WBS * 4;
+  static constexpr int SMEM = OFF_OUT + 3 * CHB;
+  static_assert(N % kBwdLpc == 0 && NS >= 1 && NS <= 4, "dstate 4, 8 or 16");
+  static constexpr int BC_EPT = (N * kBwdPos + THREADS - 1) / THREADS;  // B/C elements per thread
+  static_assert(OFF_BC % 16 == 0 && OFF_S % 16 == 0 && OFF_RED % 16 == 0 && OFF_OUT % 16 == 0,
+                "16-byte aligned regions");
+};
+
+// d coef / d A of the ZOH coefficient coef = (e^{dt A} - 1) / A, with q = dt A
+// log2(e): the difference (dt Abar - coef) / A cancels for small |q|, where the
+// Taylor series dt^2 (1/2 + x/3 + x^2/8 + x^3/30 + x^4/144) (x = dt A) is used
+// instead (truncation below 2e-8 relative for |q| < 1/8); at A = 0 it gives the
+// limit dt^2 / 2.
+__device__ __forceinline__ float dcoef_dA(float dt, float q, float ra, float abar, float coef) {
+  const float x = q * kLn2;
+  float ps = fmaf(x, 1.0f / 144.0f, 1.0f / 30.0f);
+  ps = fmaf(ps, x, 0.125f);
+  ps = fmaf(ps, x, 1.0f / 3.0f);
+  ps = fmaf(ps, x, 0.5f);
+  const float series = dt * dt * ps;
+  const float direct = fmaf(dt, abar, -coef) * ra;
+  return (fabsf(q) < kExpm1SeriesMaxQ) ? series : direct;
+}
+
+// the ZOH (or Euler) input coefficient for one state: FAST takes Abar - 1
+// directly (bf16 io with |A| >= 1/8, as the forward's fast path), otherwise the
+// expm1 series near zero and the dt limit at A = 0
+template <bool EULER, bool FAST>
+__device__ __forceinline__ float bwd_coef(float q, float dt, float a, float ra, float abar) {
+  if constexpr (EULER) {
+    return dt;
+  } else if constexpr (FAST) {
+    return fmaf(abar, ra, -ra);
+  } else {
+    const float em1 = exp2m1_accurate(q, abar);
+    return (a == 0.0f) ? dt : em1 * ra;
+  }
+}
+
+// Warp reduce-scatter over the 8 channels of a warp: v holds this lane's NS
+// states of one channel; returns the sum over the warp's channels of state
+// n0 + *n_off, which lanes with `bwd_rs_holder(lane)` hold without duplicates.
+template <int NS>
+__device__ __forceinline__ float bwd_rs(const float (&v)[NS], int lane, int* n_off) {
+  constexpr unsigned kAll = 0xffffffffu;
+  if constexpr (NS == 4) {
+    const bool hi = (lane & 16) != 0;
+    float k0 = hi ? v[2] : v[0], k1 = hi ? v[3] : v[1];
+    const float s0 = hi ? v[0] : v[2], s1 = hi ? v[1] : v[3];
+    k0 += __shfl_xor_sync(kAll, s0, 16);
+    k1 += __shfl_xor_sync(kAll, s1, 16);
+    const bool h8 = (lane & 8) != 0;
+    float x = (h8 ? k1 : k0) + __shfl_xor_sync(kAll, h8 ? k0 : k1, 8);
+    x += __shfl_xor_sync(kAll, x, 4);
+    *n_off = (hi ? 2 : 0) + (h8 ? 1 : 0);
+    return x;
+  } else if constexpr (NS == 2) {
+    const bool hi = (lane & 16) != 0;
+    float x = (hi ? v[1] : v[0]) + __shfl_xor_sync(kAll, hi ? v[0] : v[1], 16);
+    x += __shfl_xor_sync(kAll, x, 8);
+    x += __shfl_xor_sync(kAll, x, 4);
+    *n_off = hi ? 1 : 0;
+    return x;
+  } else {
+    float x = v[0];
+    x += __shfl_xor_sync(kAll, x, 16);
+    x += __shfl_xor_sync(kAll, x, 8);
+    x += __shfl_xor_sync(kAll, x, 4);
+    *n_off = 0;
+    return x;
+  }
+}
+template <int NS>
+__device__ __forceinline__ bool bwd_rs_holder(int lane) {
+  return (lane & (NS == 4 ? 4 : NS == 2 ? 12 : 28)) == 0;
+}
+
+// Stage the per-channel tiles (u, delta and, when `full`, z and dy) of positions
+// l0 .. l0+15 of the CTA's channels; positions past the end and channels past
+// dim read as zero.
+template <typename Cfg>
+__device__ __forceinline__ void bwd_stage(const BwdParams& p, unsigned char* st, int64_t rowbase,
+                                          int d0, int l0, bool full) {
+  using IO = typename Cfg::io_t;
+  const void* src[4] = {p.u, p.delta, p.z, p.dy};
+  const int ntens = full ? 4 : 2;
+  if constexpr (Cfg::VEC) {
+    constexpr int CPR = Cfg::ROWB / 16;  // 16-byte chunks per row
+    constexpr int PPC = 16 / Cfg::ES;    // positions per chunk
+    const int total = ntens * Cfg::CH * CPR;
+    for (int c = threadIdx.x; c < total; c += Cfg::THREADS) {
+      const int k = c % CPR, ch = (c / CPR) % Cfg::CH, t = c / (CPR * Cfg::CH);
+      if (t == 2 && !Cfg::GATE) continue;
+      const int d = d0 + ch, l = l0 + k * PPC;
+      const bool ok = d < p.dim && l < p.seqlen;
+      const IO* g = static_cast<const IO*>(src[t]) +
+                    (ok ? (rowbase + d) * static_cast<int64_t>(p.seqlen) + l : 0);
+      cp_async16_zfill(st + t * Cfg::CHB + ch * Cfg::ROWB + k * 16, g, ok);
+    }
+  } else {
+    const int total = ntens * Cfg::CH * kBwdPos;
+    for (int e = threadIdx.x; e < total; e += Cfg::THREADS) {
+      const int pp = e % kBwdPos, ch = (e / kBwdPos) % Cfg::CH, t = e / (kBwdPos * Cfg::CH);
+      if (t == 2 && !Cfg::GATE) continue;
+      const int d = d0 + ch, l = l0 + pp;
+      IO v = IO(0);
+      if (d < p.dim && l < p.seqlen)
+        v = static_cast<const IO*>(src[t])[(rowbase + d) * static_cast<int64_t>(p.seqlen) + l];
+      reinterpret_cast<IO*>(st + t * Cfg::CHB + ch * Cfg::ROWB)[pp] = v;
+    }
+  }
+}
+
+// B (and C) of positions l0 .. l0+15 of batch row b: element e = t + i * THREADS
+// (state e / 16, position e % 16) goes to thread t's register i as raw io bits;
+// bwd_bc_park converts and stores them as fp32 [position][state].
+template <typename Cfg>
+__device__ __forceinline__ void bwd_bc_fetch(const BwdParams& p, int64_t b, int l0, bool withC,
+                                             typename Cfg::io_t (&rb)[Cfg::BC_EPT],
+                                             typename Cfg::io_t (&rc)[Cfg::BC_EPT]) {
+  using IO = typename Cfg::io_t;
+#pragma unroll
+  for (int i = 0; i < Cfg::BC_EPT; ++i) {
+    rb[i] = IO(0);
+    rc[i] = IO(0);
+    const int e = threadIdx.x + i * Cfg::THREADS;
+    if (e < Cfg::N * kBwdPos) {
+      const int n = e / kBwdPos, l = l0 + e % kBwdPos;
+      if (l < p.seqlen) {
+        const int64_t off = (b * Cfg::N + n) * static_cast<int64_t>(p.seqlen) + l;
+        rb[i] = static_cast<const IO*>(p.B)[off];
+        if (withC) rc[i] = static_cast<const IO*>(p.C)[off];
+      }
+    }
+  }
+}
+template <typename Cfg>
+__device__ __forceinline__ void bwd_bc_park(float* bc, const typename Cfg::io_t (&rb)[Cfg::BC_EPT],
+                                            const typename Cfg::io_t (&rc)[Cfg::BC_EPT]) {
+  using IO = typename Cfg::io_t;
+#pragma unroll
+  for (int i = 0; i < Cfg::BC_EPT; ++i) {
+    const int e = threadIdx.x + i * Cfg::THREADS;
+    if (e < Cfg::N * kBwdPos) {
+      const int n = e / kBwdPos, pp = e % kBwdPos;
+      bc[pp * Cfg::BCS + n] = Io<IO>::load(&rb[i]);
+      bc[kBwdPos * Cfg::BCS + pp * Cfg::BCS + n] = Io<IO>::load(&rc[i]);
+    }
+  }
+}
+
+template <typename IO>
+__device__ __forceinline__ float ld_io(const unsigned char* tile, int ch_rowb, int pp) {
+  return Io<IO>::load(reinterpret_cast<const IO*>(tile + ch_rowb) + pp);
+}
+
+// step size in log2 units, s = dt * log2(e), and sigmoid(delta + bias), for this
+// lane's four positions part*4 .. part*4+3 of its channel
+template <typename Cfg>
+__device__ __forceinline__ void bwd_prologue(const BwdParams& p, const unsigned char* stage,
+                                             int chl, int part, float bias, float* S, float* SG,
+                                             bool want_sigmoid) {
+  using IO = typename Cfg::io_t;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pp = part * 4 + i;
+    const float x = ld_io<IO>(stage + Cfg::CHB, chl * Cfg::ROWB, pp) + bias;
+    const float x2 = x * kLog2e;
+    float s = x2, sg = 1.0f;
+    if (p.softplus) {
+      if constexpr (sizeof(IO) == 2) {
+        s = softplus_log2_fast(x2);
+        sg = rcp(1.0f + ex2(-x2));
+      } else {
+        s = softplus_log2_accurate(x2);
+        sg = 1.0f / (1.0f + expf(-x));
+      }
+    }
+    S[chl * Cfg::SCS + pp] = s;
+    if (want_sigmoid) SG[chl * Cfg::SCS + pp] = sg;
+  }
+}
+
+// phase 1 body for one block: advance this lane's states over the block
+template <typename Cfg, bool FAST>
+__device__ __forceinline__ void bwd_advance(const BwdParams& p, const unsigned char* stage,
+                                            const float* bc, const float* S, int chl, int n0,
+                                            int l0, const float (&a)[Cfg::NS],
+                                            const float (&ra)[Cfg::NS], float (&h)[Cfg::NS]) {
+  using IO = typename Cfg::io_t;
+  constexpr int NS = Cfg::NS;
+#pragma unroll
+  for (int pp = 0; pp < kBwdPos; ++pp) {
+    if (l0 + pp < p.seqlen) {
+      const float s = S[chl * Cfg::SCS + pp];
+      const float dt = s * kLn2;
+      const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        const float q = s * a[k];
+        const float ab = ex2(q);
+        const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
+        h[k] = fmaf(ab, h[k], coef * (bc[pp * Cfg::BCS + n0 + k] * uf));
+      }
+    }
+  }
+}
+
+// phase 2 body for one block: recompute the states, then the adjoint backwards
+template <typename Cfg, bool FAST>
+__device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned char* stage,
+                                          const float* bc, const float* S, float* DY0, float* RED,
+                                          float* WB, unsigned char* OUT, int chl, int part,
+                                          int lane, int warp, int n0, int l0, float Dd,
+                                          const float (&a)[Cfg::NS], const float (&ra)[Cfg::NS],
+                                          const float (&he)[Cfg::NS], float (&g)[Cfg::NS],
+                                          float (&an)[Cfg::NS], float (&dA)[Cfg::NS],
+                                          float& dD_acc) {
+  using IO = typename Cfg::io_t;
+  constexpr int NS = Cfg::NS, N = Cfg::N;
+  constexpr unsigned kAll = 0xffffffffu;
+  const float* Bt = bc;
+  const float* Ct = bc + kBwdPos * Cfg::BCS;
+
+  // ---- forward recompute: traj[pp] = h after position pp
+  float traj[kBwdPos][NS];
+  {
+    float h[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) h[k] = he[k];
+#pragma unroll
+    for (int pp = 0; pp < kBwdPos; ++pp) {
+      if (l0 + pp < p.seqlen) {
+        const float s = S[chl * Cfg::SCS + pp];
+        const float dt = s * kLn2;
+        const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
+        float y = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          const float q = s * a[k];
+          const float ab = ex2(q);
+          const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
+          h[k] = fmaf(ab, h[k], coef * (Bt[pp * Cfg::BCS + n0 + k] * uf));
+          traj[pp][k] = h[k];
+          y = fmaf(Ct[pp * Cfg::BCS + n0 + k], h[k], y);
+        }
+        y += __shfl_xor_sync(kAll, y, 1);
+        y += __shfl_xor_sync(kAll, y, 2);
+        const float y0 = fmaf(Dd, uf, y);
+        const float dyf = ld_io<IO>(stage + 3 * Cfg::CHB, chl * Cfg::ROWB, pp);
+        float dy0 = dyf, dzv = 0.0f;
+        if constexpr (Cfg::GATE) {
+          const float zf = ld_io<IO>(stage + 2 * Cfg::CHB, chl * Cfg::ROWB, pp);
+          float sg;
+          if constexpr (sizeof(IO) == 2)
+            sg = rcp(1.0f + ex2(-zf * kLog2e));
+          else
+            sg = 1.0f / (1.0f + expf(-zf));
+          dy0 = dyf * zf * sg;
+          dzv = dyf * y0 * sg * fmaf(zf, 1.0f - sg, 1.0f);
+        }
+        if (part == (pp & 3)) {
+          DY0[chl * Cfg::SCS + pp] = dy0;
+          dD_acc = fmaf(dy0, uf, dD_acc);
+          if constexpr (Cfg::GATE)
+            Io<IO>::store(reinterpret_cast<IO*>(OUT + 2 * Cfg::CHB + chl * Cfg::ROWB) + pp, dzv);
+        }
+      }
+    }
+  }
+  __syncwarp();
+
+  // ---- adjoint, positions in reverse
+  float dAb[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) dAb[k] = 0.0f;
+#pragma unroll
+  for (int pp = kBwdPos - 1; pp >= 0; --pp) {
+    if (l0 + pp < p.seqlen) {
+      const float s = S[chl * Cfg::SCS + pp];
+      const float dt = s * kLn2;
+      const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
+      const float dy0 = DY0[chl * Cfg::SCS + pp];
+      float du_p = 0.0f, ddt_p = 0.0f;
+      float dBv[NS], dCv[NS];
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        const float hp = (pp > 0) ? traj[pp > 0 ? pp - 1 : 0][k] : he[k];
+        const float Bv = Bt[pp * Cfg::BCS + n0 + k];
+        const float Cv = Ct[pp * Cfg::BCS + n0 + k];
+        const float q = s * a[k];
+        const float ab = ex2(q);
+        const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
+        const float gk = fmaf(g[k], an[k], Cv * dy0);
+        dCv[k] = dy0 * traj[pp][k];
+        dBv[k] = coef * (gk * uf);
+        const float gB = gk * Bv;
+        du_p = fmaf(coef, gB, du_p);
+        const float bu = Bv * uf;
+        const float ga = gk * ab;
+        if constexpr (Cfg::EULER) {
+          ddt_p = fmaf(ga * a[k], hp, fmaf(gk, bu, ddt_p));
+          dAb[k] = fmaf(ga * dt, hp, dAb[k]);
+        } else {
+          ddt_p = fmaf(ga, fmaf(a[k], hp, bu), ddt_p);
+          const float dcda = dcoef_dA(dt, q, ra[k], ab, coef);
+          dAb[k] = fmaf(ga * dt, hp, fmaf(gk * dcda, bu, dAb[k]));
+        }
+        g[k] = gk;
+        an[k] = ab;
+      }
+      RED[chl * Cfg::REDS + pp * 8 + part] = du_p;
+      RED[chl * Cfg::REDS + pp * 8 + 4 + part] = ddt_p;
+      int off;
+      const float sb = bwd_rs<NS>(dBv, lane, &off);
+      const float sc = bwd_rs<NS>(dCv, lane, &off);
+      if (bwd_rs_holder<NS>(lane)) {
+        WB[((warp * 2 + 0) * N + n0 + off) * Cfg::WBS + pp] = sb;
+        WB[((warp * 2 + 1) * N + n0 + off) * Cfg::WBS + pp] = sc;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NS; ++k) dA[k] += dAb[k];
+}
+
+template <typename Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams p) {
+  using IO = typename Cfg::io_t;
+  constexpr int NS = Cfg::NS, N = Cfg::N, CH = Cfg::CH;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, part = lane & 3;
+  const int chl = tid >> 2;  // channel within the CTA
+  const int64_t b = blockIdx.x / p.tiles;
+  const int d0 = static_cast<int>(blockIdx.x % p.tiles) * CH;
+  const int d = d0 + chl;
+  const bool chv = d < p.dim;
+  const int dc = chv ? d : p.dim - 1;  // clamped for parameter reads
+  const int64_t rowbase = b * p.dim;
+  const int64_t row = rowbase + dc;
+  const int64_t rows = p.batch * p.dim;
+  const int n0 = part * NS;
+
+  unsigned char* stage_base = smem + Cfg::OFF_STAGE;
+  float* BC = reinterpret_cast<float*>(smem + Cfg::OFF_BC);
+  float* S = reinterpret_cast<float*>(smem + Cfg::OFF_S);
+  float* SG = reinterpret_cast<float*>(smem + Cfg::OFF_SG);
+  float* DY0 = reinterpret_cast<float*>(smem + Cfg::OFF_DY0);
+  float* RED = reinterpret_cast<float*>(smem + Cfg::OFF_RED);
+  float* WB = reinterpret_cast<float*>(smem + Cfg::OFF_WB);
+  unsigned char* OUT = smem + Cfg::OFF_OUT;
+  auto stage = [&](int i) { return stage_base + i * Cfg::STAGE; };
+  auto bcbuf = [&](int i) { return BC + i * (Cfg::BCB / 4); };
+
+  float a[NS], ra[NS];
+  bool big = true;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    a[k] = __ldg(p.A + static_cast<int64_t>(dc) * N + n0 + k);
+    ra[k] = (a[k] != 0.0f) ? 1.0f / a[k] : 0.0f;
+    big = big && fabsf(a[k]) >= kExpm1SeriesMaxQ;
+  }
+  // bf16 io with every |A| of the warp >= 1/8: Abar - 1 as the ZOH coefficient
+  const bool fast = (sizeof(IO) == 2) && !Cfg::EULER && __all_sync(0xffffffffu, big);
+  const float bias = p.bias ? __ldg(p.bias + dc) : 0.0f;
+  const float Dd = p.D ? __ldg(p.D + dc) : 0.0f;
+
+  float h[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) h[k] = (chv && p.h0) ? p.h0[row * N + n0 + k] : 0.0f;
+
+  const int nblk = p.nblk;
+  IO rb[Cfg::BC_EPT], rc[Cfg::BC_EPT];
+  // ---------------- phase 1: forward, checkpoint entering each block
+  if (nblk > 0) {
+    bwd_stage<Cfg>(p, stage(0), rowbase, d0, 0, false);
+    cp_async_commit();
+    bwd_bc_fetch<Cfg>(p, b, 0, false, rb, rc);
+    bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
+  }
+  for (int j = 0; j < nblk; ++j) {
+    const int l0 = j * kBwdPos, buf = j & 1;
+    cp_async_wait_all();
+    __syncthreads();  // stage j and B of block j visible; block j-1 fully consumed
+    const bool more = j + 1 < nblk;
+    if (more) {
+      bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 + kBwdPos, false);
+      cp_async_commit();
+      bwd_bc_fetch<Cfg>(p, b, l0 + kBwdPos, false, rb, rc);
+    }
+    bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, false);
+    if (chv) {
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+        p.ckpt[(static_cast<int64_t>(j) * rows + row) * N + n0 + k] = h[k];
+    }
+    __syncwarp();
+    if constexpr (sizeof(IO) == 2 && !Cfg::EULER) {
+      if (fast)
+        bwd_advance<Cfg, true>(p, stage(buf), bcbuf(buf), S, chl, n0, l0, a, ra, h);
+      else
+        bwd_advance<Cfg, false>(p, stage(buf), bcbuf(buf), S, chl, n0, l0, a, ra, h);
+    } else {
+      bwd_advance<Cfg, false>(p, stage(buf), bcbuf(buf), S, chl, n0, l0, a, ra, h);
+    }
+    if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
+  }
+
+  // ---------------- phase 2: blocks in reverse
+  float g[NS], an[NS], dA[NS], he[NS], hn[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    g[k] = (chv && p.dh_last) ? p.dh_last[row * N + n0 + k] : 0.0f;
+    an[k] = 1.0f;
+    dA[k] = 0.0f;
+    hn[k] = 0.0f;
+  }
+  float dD_acc = 0.0f, db_acc = 0.0f;
+  __syncthreads();  // phase 1's last block consumed
+  if (nblk > 0) {
+    const int l0 = (nblk - 1) * kBwdPos;
+    bwd_stage<Cfg>(p, stage(0), rowbase, d0, l0, true);
+    cp_async_commit();
+    bwd_bc_fetch<Cfg>(p, b, l0, true, rb, rc);
+    bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
+    if (chv) {
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+        hn[k] = p.ckpt[(static_cast<int64_t>(nblk - 1) * rows + row) * N + n0 + k];
+    }
+  }
+  for (int it = 0; it < nblk; ++it) {
+    const int j = nblk - 1 - it, l0 = j * kBwdPos, buf = it & 1;
+    cp_async_wait_all();
+    __syncthreads();  // stage of block j visible; the previous block fully consumed
+#pragma unroll
+    for (int k = 0; k < NS; ++k) he[k] = hn[k];
+    const bool more = j > 0;
+    if (more) {
+      bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 - kBwdPos, true);
+      cp_async_commit();
+      bwd_bc_fetch<Cfg>(p, b, l0 - kBwdPos, true, rb, rc);
+      if (chv) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+          hn[k] = p.ckpt[(static_cast<int64_t>(j - 1) * rows + row) * N + n0 + k];
+      }
+    }
+    bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, p.softplus != 0);
+    __syncwarp();
+    if constexpr (sizeof(IO) == 2 && !Cfg::EULER) {
+      if (fast)
+        bwd_block<Cfg, true>(p, stage(buf), bcbuf(buf), S, DY0, RED, WB, OUT, chl, part, lane,
+                             warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
+      else
+        bwd_block<Cfg, false>(p, stage(buf), bcbuf(buf), S, DY0, RED, WB, OUT, chl, part, lane,
+                              warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
+    } else {
+      bwd_block<Cfg, false>(p, stage(buf), bcbuf(buf), S, DY0, RED, WB, OUT, chl, part, lane,
+                            warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
+    }
+    __syncwarp();
+    // per-position totals over the channel's four lanes: du (with the D skip) and
+    // ddelta (through the softplus) for this lane's positions part*4 .. +3
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pp = part * 4 + i;
+      if (l0 + pp < p.seqlen) {
+        const float4 r0 = lds128f(RED + chl * Cfg::REDS + pp * 8);
+        const float4 r1 = lds128f(RED + chl * Cfg::REDS + pp * 8 + 4);
+        const float du = fmaf(Dd, DY0[chl * Cfg::SCS + pp], (r0.x + r0.y) + (r0.z + r0.w));
+        float dx = (r1.x + r1.y) + (r1.z + r1.w);
+        if (p.softplus) dx *= SG[chl * Cfg::SCS + pp];
+        db_acc += dx;
+        Io<IO>::store(reinterpret_cast<IO*>(OUT + chl * Cfg::ROWB) + pp, du);
+        Io<IO>::store(reinterpret_cast<IO*>(OUT + Cfg::CHB + chl * Cfg::ROWB) + pp, dx);
+      }
+    }
+    __syncthreads();  // WB and OUT complete
+    // dB / dC partials of this CTA: sum the warps
+    for (int v = tid; v < 2 * N * kBwdPos; v += Cfg::THREADS) {
+      const int pp = v % kBwdPos, n = (v / kBwdPos) % N, t = v / (kBwdPos * N);
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < Cfg::WARPS; ++w) sum += WB[((w * 2 + t) * N + n) * Cfg::WBS + pp];
+      const int l = l0 + pp;
+      if (l < p.seqlen)
+        p.part_bc[((static_cast<int64_t>(blockIdx.x % p.tiles) * p.batch + b) * 2 + t) * N *
+                      static_cast<int64_t>(p.seqlen) +
+                  static_cast<int64_t>(n) * p.seqlen + l] = sum;
+    }
+    // du, ddelta, dz tiles
+    {
+      void* dst[3] = {p.du, p.ddelta, p.dz};
+      const int ntens = Cfg::GATE ? 3 : 2;
+      if constexpr (Cfg::VEC) {
+        constexpr int CPR = Cfg::ROWB / 16, PPC = 16 / Cfg::ES;
+        for (int c = tid; c < ntens * CH * CPR; c += Cfg::THREADS) {
+          const int k = c % CPR, ch = (c / CPR) % CH, t = c / (CPR * CH);
+          const int dd = d0 + ch, l = l0 + k * PPC;
+          if (dd < p.dim && l < p.seqlen)
+            *reinterpret_cast<uint4*>(static_cast<IO*>(dst[t]) +
+                                      (rowbase + dd) * static_cast<int64_t>(p.seqlen) + l) =
+                lds128(OUT + t * Cfg::CHB + ch * Cfg::ROWB + k * 16);
+        }
+      } else {
+        for (int e = tid; e < ntens * CH * kBwdPos; e += Cfg::THREADS) {
+          const int pp = e % kBwdPos, ch = (e / kBwdPos) % CH, t = e / (kBwdPos * CH);
+          const int dd = d0 + ch, l = l0 + pp;
+          if (dd < p.dim && l < p.seqlen)
+            static_cast<IO*>(dst[t])[(rowbase + dd) * static_cast<int64_t>(p.seqlen) + l] =
+                reinterpret_cast<const IO*>(OUT + t * Cfg::CHB + ch * Cfg::ROWB)[pp];
+        }
+      }
+    }
+    if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
+  }
+
+  // ---------------- per-channel results
+  dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
+  dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 2);
+  db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 1);
+  db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 2);
+  if (chv) {
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      p.part_a[row * N + n0 + k] = dA[k];
+      if (p.dh0) p.dh0[row * N + n0 + k] = an[k] * g[k];
+    }
+    if (part == 0) {
+      p.part_dd[row * 2 + 0] = dD_acc;
+      p.part_dd[row * 2 + 1] = db_acc;
+    }
+  }
+}
+
+// dB, dC [batch][N][seqlen] = sum over a batch row's CTAs of the partials, in
+// CTA order.
+template <typename IO>
+__global__ void __launch_bounds__(256) scan_bwd_reduce_bc_kernel(const float* part, int tiles,
+                                                                 int64_t batch, int N, int seqlen,
+                                                                 IO* dB, IO* dC) {
+  const int64_t per_tile = batch * 2 * N * static_cast<int64_t>(seqlen);
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (e >= per_tile) return;
+  float sum = 0.0f;
+  for (int t = 0; t < tiles; ++t) sum += part[t * per_tile + e];
+  const int64_t ns = static_cast<int64_t>(N) * seqlen;
+  const int64_t bt = e / ns, rem = e % ns;  // bt = b * 2 + (0: dB, 1: dC)
+  IO* out = (bt & 1) ? dC : dB;
+  Io<IO>::store(out + (bt >> 1) * ns + rem, sum);
+}
+
+// dA [dim][N], dD, bias gradient [dim] = sums over the batch rows, in row order
+// (a template only so that every translation unit may include this header)
+template <int kUnused = 0>
+__global__ void __launch_bounds__(256) scan_bwd_reduce_param_kernel(
+    const float* part_a, const float* part_dd, int64_t batch, int dim, int N, float* dA, float* dD,
+    float* dbias) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  const int64_t na = static_cast<int64_t>(dim) * N;
+  if (i < na) {
+    float s = 0.0f;
+    for (int64_t b = 0; b < batch; ++b) s += part_a[b * na + i];
+    dA[i] = s;
+  } else if (i < na + dim) {
+    const int64_t dd = i - na;
+    float sd = 0.0f, sb = 0.0f;
+    for (int64_t b = 0; b < batch; ++b) {
+      sd += part_dd[(b * dim + dd) * 2];
+      sb += part_dd[(b * dim + dd) * 2 + 1];
+    }
+    if (dD) dD[dd] = sd;
+    if (dbias) dbias[dd] = sb;
+  }
+}
+
+}  // namespace ssm

@@ -301,6 +301,82 @@ ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, ssm_dtyp
                              C, D, z, y, SSM_DISC_ZOH, stream);
 }
 
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1) return kStatusBytes;
+  return bwd_layout(batch, dim, dstate, seqlen).total;
+}
+
+ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ssm_dtype io,
+                        const void* u, const void* delta, const float* delta_bias,
+                        int delta_softplus, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* h0, const void* dy,
+                        const float* dh_last, void* du, void* ddelta, float* dA, void* dB,
+                        void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                        void* workspace, size_t workspace_bytes, ssm_discretization disc,
+                        ssm_stream_t stream) {
+  ssm_status st = validate_common(batch, dim, dstate, io);
+  if (st != SSM_OK) return st;
+  if (seqlen < 1 || seqlen > INT32_MAX - 4096) return SSM_ERR_INVALID_ARG;
+  if (batch > (int64_t(1) << 62) / dim / seqlen / dstate) return SSM_ERR_INVALID_ARG;
+  if (disc != SSM_DISC_ZOH && disc != SSM_DISC_EULER) return SSM_ERR_INVALID_ARG;
+  if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC)
+    return SSM_ERR_INVALID_ARG;
+  if ((z != nullptr) != (dz != nullptr)) return SSM_ERR_INVALID_ARG;
+  if (D && !dD) return SSM_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return SSM_ERR_INVALID_ARG;
+  const BwdLayout w = bwd_layout(batch, dim, dstate, seqlen);
+  if (workspace_bytes < w.total) return SSM_ERR_INVALID_ARG;
+  const size_t esz = (io == SSM_DTYPE_BF16) ? 2 : 4;
+  const void* io_ptrs[12] = {u, delta, B, C, z, dy, du, ddelta, dB, dC, dz, nullptr};
+  for (const void* q : io_ptrs)
+    if (q && !aligned(q, esz)) return SSM_ERR_INVALID_ARG;
+  const void* f_ptrs[10] = {delta_bias, A, D, h0, dh_last, dA, dD, ddelta_bias, dh0, nullptr};
+  for (const void* q : f_ptrs)
+    if (q && !aligned(q, 4)) return SSM_ERR_INVALID_ARG;
+  // cp.async staging and 16-byte output stores need 16-byte rows
+  bool vec = (seqlen * static_cast<int64_t>(esz)) % 16 == 0;
+  const void* v_ptrs[7] = {u, delta, z, dy, du, ddelta, dz};
+  for (const void* q : v_ptrs)
+    if (q && !aligned(q, 16)) vec = false;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  ssm::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = batch;
+  p.dim = static_cast<int>(dim);
+  p.seqlen = static_cast<int>(seqlen);
+  p.nblk = static_cast<int>(w.nblk);
+  p.tiles = static_cast<int>(w.tiles);
+  p.softplus = delta_softplus ? 1 : 0;
+  p.u = u;
+  p.delta = delta;
+  p.z = z;
+  p.dy = dy;
+  p.B = B;
+  p.C = C;
+  p.A = A;
+  p.D = D;
+  p.bias = delta_bias;
+  p.h0 = h0;
+  p.dh_last = dh_last;
+  p.du = du;
+  p.ddelta = ddelta;
+  p.dz = dz;
+  p.dh0 = dh0;
+  p.ckpt = reinterpret_cast<float*>(ws + w.off_ckpt);
+  p.part_bc = reinterpret_cast<float*>(ws + w.off_bc);
+  p.part_a = reinterpret_cast<float*>(ws + w.off_a);
+  p.part_dd = reinterpret_cast<float*>(ws + w.off_dd);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool euler = disc == SSM_DISC_EULER;
+  float* dD_out = D ? dD : nullptr;
+  if (io == SSM_DTYPE_BF16)
+    return launch_scan_bwd<uint16_t>(p, static_cast<int>(dstate), z != nullptr, euler, vec, dB,
+                                     dC, dA, dD_out, ddelta_bias, s);
+  return launch_scan_bwd<float>(p, static_cast<int>(dstate), z != nullptr, euler, vec, dB, dC, dA,
+                                dD_out, ddelta_bias, s);
+}
+
 ssm_status ssm_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
                           ssm_dtype io, const void* x, const float* weight, const float* bias,
                           const void* conv_state, int apply_silu, void* out,

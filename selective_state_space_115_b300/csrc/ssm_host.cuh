@@ -17,6 +17,7 @@
 #include "scan_chunk.cuh"
 #include "state_update.cuh"
 #include "conv1d.cuh"
+#include "scan_bwd.cuh"
 
 namespace ssm_host {
 
@@ -237,6 +238,33 @@ inline size_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, co
 }
 
 // ---------------------------------------------------------------------------
+// scan gradient workspace: [0, 256) status words; the block checkpoints
+// [nblk][batch * dim][N]; the per-CTA dB / dC partials [tiles][batch][2][N][L];
+// the per-channel dA [batch * dim][N]; dD and the bias gradient [batch * dim][2]
+// ---------------------------------------------------------------------------
+constexpr int kBwdThreads = 128;
+constexpr int kBwdChannels = kBwdThreads / ssm::kBwdLpc;
+
+struct BwdLayout {
+  int64_t nblk = 0, tiles = 0;
+  size_t off_ckpt = 0, off_bc = 0, off_a = 0, off_dd = 0, total = 0;
+};
+
+inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+  BwdLayout w;
+  w.nblk = (seqlen + ssm::kBwdPos - 1) / ssm::kBwdPos;
+  w.tiles = (dim + kBwdChannels - 1) / kBwdChannels;
+  const size_t rows = static_cast<size_t>(batch) * static_cast<size_t>(dim);
+  w.off_ckpt = kStatusBytes;
+  w.off_bc = w.off_ckpt + round_up(static_cast<size_t>(w.nblk) * rows * dstate * 4, 256);
+  w.off_a = w.off_bc + round_up(static_cast<size_t>(w.tiles) * batch * 2 * dstate *
+                                    static_cast<size_t>(seqlen) * 4, 256);
+  w.off_dd = w.off_a + round_up(rows * dstate * 4, 256);
+  w.total = w.off_dd + round_up(rows * 2 * 4, 256);
+  return w;
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 // Channel-kernel shapes: 32-byte chunk rows (16 bf16 / 8 fp32 positions) and a
@@ -323,6 +351,11 @@ ssm_status dispatch_update_n(const ssm::UpdateParams& p, bool vec, cudaStream_t 
 // Causal conv1d launches (defined in inst_conv.cu).  `vec`: x, out 16-byte aligned
 // and rows a multiple of 16 bytes long.
 ssm_status launch_conv1d_fwd(bool bf16, const ssm::ConvParams& p, bool vec, cudaStream_t s);
+// scan gradient: the main kernel and the two reductions (inst_bwd_*.cu)
+template <typename IO>
+ssm_status launch_scan_bwd(const ssm::BwdParams& p, int dstate, bool gate, bool euler, bool vec,
+                           void* dB, void* dC, float* dA, float* dD, float* dbias,
+                           cudaStream_t s);
 ssm_status launch_conv1d_update(bool bf16, const ssm::ConvParams& p, cudaStream_t s);
 
 }  // namespace ssm_host

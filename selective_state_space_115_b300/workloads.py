@@ -196,3 +196,19 @@ def make_decode_step(cfg: DecodeConfig, step: int, seed: int = 0, batch: Optiona
     z = rng.standard_normal((b, d), dtype=f32) if cfg.gate else None
     return {"u": encode(u, cfg.io), "delta": encode(delta, cfg.io), "B": encode(Bm, cfg.io),
             "C": encode(Cm, cfg.io), "z": None if z is None else encode(z, cfg.io)}
+
+
+def make_scan_grads(cfg: ScanConfig, seed: int = 0, batch: Optional[int] = None,
+                    dim: Optional[int] = None, seqlen: Optional[int] = None,
+                    dstate: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Upstream gradients for the scan's backward: dy [b, d, L] ~ N(0, 1) in the io
+    dtype and dh_last [b, d, n] ~ N(0, 1) float32, from their own stream
+    (default_rng([seed, 7])) so they do not disturb the forward inputs' draws."""
+    b = cfg.batch if batch is None else batch
+    d = cfg.dim if dim is None else dim
+    n = cfg.dstate if dstate is None else dstate
+    L = cfg.seqlen if seqlen is None else seqlen
+    rng = np.random.default_rng([seed, 7])
+    dy = rng.standard_normal((b, d, L), dtype=np.float32)
+    dh_last = rng.standard_normal((b, d, n), dtype=np.float32)
+    return {"dy": encode(dy, cfg.io), "dh_last": dh_last}

@@ -203,3 +203,58 @@ def test_conv1d_validation(kw, expect):
 def test_read_status_rejects_null():
     lib = binding.library()
     assert lib.ssm_read_device_status(None, None) == binding.SSM_ERR_INVALID_ARG
+
+
+def _bwd_bytes(batch, dim, n, seqlen):
+    rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    nblk = (seqlen + 15) // 16
+    tiles = (dim + 31) // 32
+    rows = batch * dim
+    return (256 + rnd(nblk * rows * n * 4) + rnd(tiles * batch * 2 * n * seqlen * 4)
+            + rnd(rows * n * 4) + rnd(rows * 2 * 4))
+
+
+def test_bwd_workspace_size():
+    """Checkpoints every 16 positions, one dB/dC partial per 32-channel CTA, the
+    per-channel dA / dD / bias sums."""
+    ws = binding.library().ssm_scan_bwd_workspace_size
+    for shape in ((8, 5120, 16, 2048), (1, 1536, 16, 131072), (2, 37, 8, 69), (1, 1, 4, 1)):
+        assert ws(*shape) == _bwd_bytes(*shape), shape
+
+
+def _bwd_call(lib, **kw):
+    a = dict(batch=2, dim=8, dstate=16, seqlen=64, io=1, u=P, delta=P, bias=None, softplus=1,
+             A=P, B=P, C=P, D=None, z=None, h0=None, dy=P, dh_last=None, du=P + 4096,
+             ddelta=P + 8192, dA=P + 12288, dB=P + 16384, dC=P + 20480, dD=None, dz=None,
+             dbias=None, dh0=None, ws=WS, ws_bytes=1 << 30, disc=0)
+    a.update(kw)
+    v = lambda q: None if q is None else ctypes.c_void_p(q)  # noqa: E731
+    return lib.ssm_scan_bwd(a["batch"], a["dim"], a["dstate"], a["seqlen"], a["io"], v(a["u"]),
+                            v(a["delta"]), v(a["bias"]), a["softplus"], v(a["A"]), v(a["B"]),
+                            v(a["C"]), v(a["D"]), v(a["z"]), v(a["h0"]), v(a["dy"]),
+                            v(a["dh_last"]), v(a["du"]), v(a["ddelta"]), v(a["dA"]), v(a["dB"]),
+                            v(a["dC"]), v(a["dD"]), v(a["dz"]), v(a["dbias"]), v(a["dh0"]),
+                            v(a["ws"]), a["ws_bytes"], a["disc"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dstate=12), binding.SSM_ERR_UNSUPPORTED),
+    (dict(io=3), binding.SSM_ERR_UNSUPPORTED),
+    (dict(seqlen=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(batch=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(dy=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(du=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(dA=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(dC=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(z=P), binding.SSM_ERR_INVALID_ARG),            # z without dz
+    (dict(dz=P), binding.SSM_ERR_INVALID_ARG),           # dz without z
+    (dict(D=P), binding.SSM_ERR_INVALID_ARG),            # D without dD
+    (dict(disc=2), binding.SSM_ERR_INVALID_ARG),
+    (dict(ws=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(ws=WS + 16), binding.SSM_ERR_INVALID_ARG),     # not 256-byte aligned
+    (dict(ws_bytes=1024), binding.SSM_ERR_INVALID_ARG),  # too small
+    (dict(u=P + 1), binding.SSM_ERR_INVALID_ARG),        # misaligned bf16
+    (dict(dA=P + 2), binding.SSM_ERR_INVALID_ARG),       # misaligned fp32
+])
+def test_bwd_validation(kw, expect):
+    assert _bwd_call(binding.library(), **kw) == expect
