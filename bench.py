@@ -382,6 +382,7 @@ def run_gpu(args):
     # ---- decode state update (rank 0's measurement)
     decode = run_decode(dev, S) if (rank == 0 and not args.no_decode) else None
     conv = run_conv(dev, S) if (rank == 0 and not args.no_decode) else None
+    bwd = run_bwd(dev, S) if (rank == 0 and not args.no_decode) else None
     euler = None
     if rank == 0 and not args.no_decode:
         # the same scan with the Euler input term (Bbar = dt B)
@@ -439,6 +440,8 @@ def run_gpu(args):
             line["conv1d"] = conv
         if euler:
             line["scan_euler"] = euler
+        if bwd:
+            line["scan_bwd"] = bwd
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -480,6 +483,62 @@ def run_conv(dev, S, iters=50):
             "ms_per_call": ms, "bytes_per_call": nbytes, "gpu_launches": iters,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "traffic": None, "peak_kind": kind}}
+
+
+def bwd_bytes(cfg) -> int:
+    """Algorithmic HBM bytes of one scan backward: u, delta, dy (and z) read, du,
+    ddelta (and dz) written per element; B, C read and dB, dC written per
+    position; fp32 A, D, bias read and dA, dD, bias gradient written."""
+    s = 2 if cfg.io == W.BF16 else 4
+    per_elem = (6 + (2 if cfg.gate else 0)) * s
+    per_pos = 4 * s * cfg.dstate
+    params = 2 * 4 * (cfg.dim * cfg.dstate + 2 * cfg.dim)
+    return cfg.elements * per_elem + cfg.batch * cfg.seqlen * per_pos + params
+
+
+def run_bwd(dev, S, iters=20):
+    """The scan's gradient on the bench workload (dy ~ N(0, 1)), through the C ABI."""
+    import torch
+    x = W.make_scan_inputs(CFG, seed=0)
+    gr = W.make_scan_grads(CFG, seed=0)
+    u, dl, z = to_dev_io(x["u"], dev), to_dev_io(x["delta"], dev), to_dev_io(x["z"], dev)
+    B, C = to_dev_io(x["B"], dev), to_dev_io(x["C"], dev)
+    dy = to_dev_io(gr["dy"], dev)
+    A = torch.from_numpy(x["A"]).to(dev)
+    Dv = torch.from_numpy(x["D"]).to(dev)
+    bias = torch.from_numpy(x["delta_bias"]).to(dev)
+
+    def call():
+        return S.scan_bwd(u, dl, A, B, C, dy, D=Dv, z=z, delta_bias=bias)
+
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    peaks, kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    ex2_peak = EX2_PER_CLK_SM * SM_COUNT * SM_MAX_MHZ * 1e6 / 1e12
+    texp = CFG.updates / (ms * 1e-3) / 1e12
+    nbytes = bwd_bytes(CFG)
+    return {"workload": f"gradient of the {CFG.name} scan (du, ddelta, dz, dA, dB, dC, dD, "
+                        "ddelta_bias, dh0)",
+            "ms_per_call": ms, "value": CFG.elements / (ms * 1e-3), "unit": "elements/s",
+            # the gradient kernel (bf16 io: one launch for the CTAs on the fast ZOH
+            # arithmetic, one for the rest) and the two fixed-order reductions
+            "gpu_launches": ((2 if CFG.io == W.BF16 else 1) + 2) * iters,
+            "roofline": {"bound": "alu", "achieved": texp, "peak": ex2_peak, "unit": "Texp/s",
+                         "frac": texp / ex2_peak, "traffic": None,
+                         "note": "one ex2 per state update, as the forward; the kernel also "
+                                 "recomputes the forward states (two more passes of ex2)"},
+            "hbm": {"bytes_per_call": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+                    "frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": kind}}
 
 
 def run_decode(dev, S):
@@ -572,6 +631,8 @@ def main():
                          "line is quoted on 2p8b)")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode loop and print its JSON (profiling)")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="run only the scan backward timing and print its JSON (profiling)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decode loop length (default 1024; fewer for ncu)")
     args = ap.parse_args()
@@ -591,6 +652,13 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps(run_decode(dev, S)), flush=True)
+        return 0
+    if args.bwd_only:
+        import torch
+        from selective_state_space_115_b300 import binding as S
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(run_bwd(dev, S, iters=max(1, min(args.steps, 20)))), flush=True)
         return 0
     return run_gpu(args)
 

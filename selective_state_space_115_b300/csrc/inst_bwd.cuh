@@ -6,10 +6,9 @@
 
 namespace ssm_host {
 
-template <typename IO, int N, bool GATE, bool EULER, bool VEC>
-static ssm_status bwd_main(const ssm::BwdParams& p, cudaStream_t s) {
-  using Cfg = ssm::BwdCfg<IO, N, GATE, EULER, VEC, kBwdThreads>;
-  auto kern = ssm::scan_bwd_kernel<Cfg>;
+template <typename Cfg, int MODE>
+static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s) {
+  auto kern = ssm::scan_bwd_kernel<Cfg, MODE>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
@@ -22,6 +21,18 @@ static ssm_status bwd_main(const ssm::BwdParams& p, cudaStream_t s) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "scan_bwd launch");
   return SSM_OK;
+}
+
+template <typename IO, int N, bool GATE, bool EULER, bool VEC>
+static ssm_status bwd_main(const ssm::BwdParams& p, cudaStream_t s) {
+  using Cfg = ssm::BwdCfg<IO, N, GATE, EULER, VEC, kBwdThreads>;
+  if constexpr (sizeof(IO) == 2 && !EULER) {
+    const ssm_status st = bwd_launch<Cfg, ssm::kBwdFastTiles>(p, s);
+    if (st != SSM_OK) return st;
+    return bwd_launch<Cfg, ssm::kBwdAccurateTiles>(p, s);
+  } else {
+    return bwd_launch<Cfg, ssm::kBwdAll>(p, s);
+  }
 }
 
 template <typename IO, int N>

@@ -20,10 +20,14 @@
 // Layout and schedule (one CTA = THREADS/4 channels of one batch row, four lanes
 // per channel, each lane owning N/4 states):
 //   phase 1  forward over the whole sequence, writing the state entering every
-//            block of 16 positions to a workspace checkpoint [block][row][N];
-//   phase 2  blocks in reverse: recompute the block's 16 states per lane into
-//            registers from its checkpoint, then run the adjoint backwards
-//            through the block.
+//            block of kBwdPos (8) positions to a workspace checkpoint
+//            [block][row][N];
+//   phase 2  blocks in reverse: recompute the block's states per lane into
+//            registers from its checkpoint (8 positions x N/4 states), then run
+//            the adjoint backwards through the block.
+// Eight-position blocks keep the trajectory at 32 registers, so four CTAs of 128
+// threads fit an SM (at 16 positions three did); the checkpoints take 4 bytes
+// per state every 8 positions, written once and read once.
 // u, delta, z, dy stream through a two-stage shared-memory ring filled by
 // cp.async; B and C are prefetched into registers one block ahead and parked in
 // shared memory as fp32 [position][state].  dB and dC are sums over the channels:
@@ -38,8 +42,9 @@
 
 namespace ssm {
 
-constexpr int kBwdPos = 16;  // positions per block = checkpoint stride
+constexpr int kBwdPos = 8;  // positions per block = checkpoint stride
 constexpr int kBwdLpc = 4;   // lanes per channel
+constexpr int kBwdPpl = kBwdPos / kBwdLpc;  // positions per lane in the per-position steps
 
 struct BwdParams {
   int64_t batch;
@@ -78,8 +83,9 @@ struct BwdCfg {
   static constexpr int CHB = CH * ROWB;      // one per-channel tile: [CH][16]
   static constexpr int STAGE = 4 * CHB;      // u, delta, z, dy
   static constexpr int BCS = N + 4;          // row of the fp32 B / C tile (padded)
-  static constexpr int BCB = 2 * kBwdPos * BCS * 4;
-  static constexpr int SCS = 20;             // per-channel row of S / SG / DY0 (padded)
+  // B and C are parked once per lane state order (NS orders, see bwd_perm)
+  static constexpr int BCB = 2 * NS * kBwdPos * BCS * 4;
+  static constexpr int SCS = kBwdPos + 4;    // per-channel row of S / SG / DY0 (padded)
   static constexpr int REDS = kBwdPos * 8 + 4;  // per-channel stride of RED (padded)
   static constexpr int WBS = kBwdPos + 1;       // position row of WB (padded)
   static constexpr int OFF_STAGE = 0;
@@ -96,6 +102,15 @@ struct BwdCfg {
   static_assert(OFF_BC % 16 == 0 && OFF_S % 16 == 0 && OFF_RED % 16 == 0 && OFF_OUT % 16 == 0,
                 "16-byte aligned regions");
 };
+
+// 2^x on the special-function unit, as an asm statement the compiler may not
+// merge with an identical one: the adjoint recomputes Abar rather than holding
+// the forward recompute's 16 x NS values in registers across the two passes
+__device__ __forceinline__ float ex2_fresh(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // d coef / d A of the ZOH coefficient coef = (e^{dt A} - 1) / A, with q = dt A
 // log2(e): the difference (dt Abar - coef) / A cancels for small |q|, where the
@@ -128,36 +143,39 @@ __device__ __forceinline__ float bwd_coef(float q, float dt, float a, float ra, 
   }
 }
 
-// Warp reduce-scatter over the 8 channels of a warp: v holds this lane's NS
-// states of one channel; returns the sum over the warp's channels of state
-// n0 + *n_off, which lanes with `bwd_rs_holder(lane)` hold without duplicates.
+// Lane state order.  Lane `part` of a channel owns states n0 .. n0+NS-1 (n0 =
+// part*NS), held in slot order: slot k is state n0 + (k ^ perm), with perm taken
+// from the lane bits that the channel reduction below pairs over (bits 4, 3 of
+// the lane).  The order makes that reduction's exchanges the same for every lane.
 template <int NS>
-__device__ __forceinline__ float bwd_rs(const float (&v)[NS], int lane, int* n_off) {
+__device__ __forceinline__ int bwd_perm(int lane) {
+  return NS == 4 ? (lane >> 3) & 3 : NS == 2 ? (lane >> 4) & 1 : 0;
+}
+
+// Warp reduce-scatter over the 8 channels of a warp (lane bits 2..4): v holds
+// this lane's NS slots of one channel; returns the sum over the warp's channels
+// of state n0 + bwd_perm(lane), which lanes with bwd_rs_holder(lane) hold once.
+// In slot order the partner of every exchange keeps the slots this lane sends,
+// so no lane-dependent selection is needed.
+template <int NS>
+__device__ __forceinline__ float bwd_rs(const float (&v)[NS]) {
   constexpr unsigned kAll = 0xffffffffu;
   if constexpr (NS == 4) {
-    const bool hi = (lane & 16) != 0;
-    float k0 = hi ? v[2] : v[0], k1 = hi ? v[3] : v[1];
-    const float s0 = hi ? v[0] : v[2], s1 = hi ? v[1] : v[3];
-    k0 += __shfl_xor_sync(kAll, s0, 16);
-    k1 += __shfl_xor_sync(kAll, s1, 16);
-    const bool h8 = (lane & 8) != 0;
-    float x = (h8 ? k1 : k0) + __shfl_xor_sync(kAll, h8 ? k0 : k1, 8);
+    const float k0 = v[0] + __shfl_xor_sync(kAll, v[2], 16);
+    const float k1 = v[1] + __shfl_xor_sync(kAll, v[3], 16);
+    float x = k0 + __shfl_xor_sync(kAll, k1, 8);
     x += __shfl_xor_sync(kAll, x, 4);
-    *n_off = (hi ? 2 : 0) + (h8 ? 1 : 0);
     return x;
   } else if constexpr (NS == 2) {
-    const bool hi = (lane & 16) != 0;
-    float x = (hi ? v[1] : v[0]) + __shfl_xor_sync(kAll, hi ? v[0] : v[1], 16);
+    float x = v[0] + __shfl_xor_sync(kAll, v[1], 16);
     x += __shfl_xor_sync(kAll, x, 8);
     x += __shfl_xor_sync(kAll, x, 4);
-    *n_off = hi ? 1 : 0;
     return x;
   } else {
     float x = v[0];
     x += __shfl_xor_sync(kAll, x, 16);
     x += __shfl_xor_sync(kAll, x, 8);
     x += __shfl_xor_sync(kAll, x, 4);
-    *n_off = 0;
     return x;
   }
 }
@@ -167,14 +185,16 @@ __device__ __forceinline__ bool bwd_rs_holder(int lane) {
 }
 
 // Stage the per-channel tiles (u, delta and, when `full`, z and dy) of positions
-// l0 .. l0+15 of the CTA's channels; positions past the end and channels past
+// l0 .. l0+kBwdPos-1 of the CTA's channels; positions past the end and channels past
 // dim read as zero.
 template <typename Cfg>
 __device__ __forceinline__ void bwd_stage(const BwdParams& p, unsigned char* st, int64_t rowbase,
                                           int d0, int l0, bool full) {
   using IO = typename Cfg::io_t;
-  const void* src[4] = {p.u, p.delta, p.z, p.dy};
   const int ntens = full ? 4 : 2;
+  auto src = [&](int t) -> const IO* {
+    return static_cast<const IO*>(t == 0 ? p.u : t == 1 ? p.delta : t == 2 ? p.z : p.dy);
+  };
   if constexpr (Cfg::VEC) {
     constexpr int CPR = Cfg::ROWB / 16;  // 16-byte chunks per row
     constexpr int PPC = 16 / Cfg::ES;    // positions per chunk
@@ -184,7 +204,7 @@ __device__ __forceinline__ void bwd_stage(const BwdParams& p, unsigned char* st,
       if (t == 2 && !Cfg::GATE) continue;
       const int d = d0 + ch, l = l0 + k * PPC;
       const bool ok = d < p.dim && l < p.seqlen;
-      const IO* g = static_cast<const IO*>(src[t]) +
+      const IO* g = src(t) +
                     (ok ? (rowbase + d) * static_cast<int64_t>(p.seqlen) + l : 0);
       cp_async16_zfill(st + t * Cfg::CHB + ch * Cfg::ROWB + k * 16, g, ok);
     }
@@ -196,15 +216,16 @@ __device__ __forceinline__ void bwd_stage(const BwdParams& p, unsigned char* st,
       const int d = d0 + ch, l = l0 + pp;
       IO v = IO(0);
       if (d < p.dim && l < p.seqlen)
-        v = static_cast<const IO*>(src[t])[(rowbase + d) * static_cast<int64_t>(p.seqlen) + l];
+        v = src(t)[(rowbase + d) * static_cast<int64_t>(p.seqlen) + l];
       reinterpret_cast<IO*>(st + t * Cfg::CHB + ch * Cfg::ROWB)[pp] = v;
     }
   }
 }
 
-// B (and C) of positions l0 .. l0+15 of batch row b: element e = t + i * THREADS
+// B (and C) of positions l0 .. l0+kBwdPos-1 of batch row b: element e = t + i * THREADS
 // (state e / 16, position e % 16) goes to thread t's register i as raw io bits;
-// bwd_bc_park converts and stores them as fp32 [position][state].
+// bwd_bc_park converts and stores them as fp32 [order][position][state], once in
+// each lane state order (B: orders 0 .. NS-1, then C).
 template <typename Cfg>
 __device__ __forceinline__ void bwd_bc_fetch(const BwdParams& p, int64_t b, int l0, bool withC,
                                              typename Cfg::io_t (&rb)[Cfg::BC_EPT],
@@ -234,9 +255,30 @@ __device__ __forceinline__ void bwd_bc_park(float* bc, const typename Cfg::io_t 
     const int e = threadIdx.x + i * Cfg::THREADS;
     if (e < Cfg::N * kBwdPos) {
       const int n = e / kBwdPos, pp = e % kBwdPos;
-      bc[pp * Cfg::BCS + n] = Io<IO>::load(&rb[i]);
-      bc[kBwdPos * Cfg::BCS + pp * Cfg::BCS + n] = Io<IO>::load(&rc[i]);
+      const float vb = Io<IO>::load(&rb[i]), vc = Io<IO>::load(&rc[i]);
+      constexpr int NS = Cfg::NS;
+#pragma unroll
+      for (int c = 0; c < NS; ++c) {  // order c: state n at slot (n ^ c) within its group
+        const int col = (n & ~(NS - 1)) | ((n & (NS - 1)) ^ c);
+        bc[(c * kBwdPos + pp) * Cfg::BCS + col] = vb;
+        bc[((NS + c) * kBwdPos + pp) * Cfg::BCS + col] = vc;
+      }
     }
+  }
+}
+
+// this lane's NS consecutive states of a [position][state] fp32 row (16-byte
+// aligned for NS = 4, 8-byte for NS = 2)
+template <int NS>
+__device__ __forceinline__ void ld_states(const float* q, float (&v)[NS]) {
+  if constexpr (NS == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(q);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else if constexpr (NS == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(q);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+    v[0] = q[0];
   }
 }
 
@@ -246,15 +288,15 @@ __device__ __forceinline__ float ld_io(const unsigned char* tile, int ch_rowb, i
 }
 
 // step size in log2 units, s = dt * log2(e), and sigmoid(delta + bias), for this
-// lane's four positions part*4 .. part*4+3 of its channel
+// lane's positions part*kBwdPpl .. (part+1)*kBwdPpl-1 of its channel
 template <typename Cfg>
 __device__ __forceinline__ void bwd_prologue(const BwdParams& p, const unsigned char* stage,
                                              int chl, int part, float bias, float* S, float* SG,
                                              bool want_sigmoid) {
   using IO = typename Cfg::io_t;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int pp = part * 4 + i;
+  for (int i = 0; i < kBwdPpl; ++i) {
+    const int pp = part * kBwdPpl + i;
     const float x = ld_io<IO>(stage + Cfg::CHB, chl * Cfg::ROWB, pp) + bias;
     const float x2 = x * kLog2e;
     float s = x2, sg = 1.0f;
@@ -275,7 +317,7 @@ __device__ __forceinline__ void bwd_prologue(const BwdParams& p, const unsigned 
 // phase 1 body for one block: advance this lane's states over the block
 template <typename Cfg, bool FAST>
 __device__ __forceinline__ void bwd_advance(const BwdParams& p, const unsigned char* stage,
-                                            const float* bc, const float* S, int chl, int n0,
+                                            const float* Bt, const float* S, int chl, int n0,
                                             int l0, const float (&a)[Cfg::NS],
                                             const float (&ra)[Cfg::NS], float (&h)[Cfg::NS]) {
   using IO = typename Cfg::io_t;
@@ -286,12 +328,14 @@ __device__ __forceinline__ void bwd_advance(const BwdParams& p, const unsigned c
       const float s = S[chl * Cfg::SCS + pp];
       const float dt = s * kLn2;
       const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
+      float Bv[NS];
+      ld_states<NS>(Bt + pp * Cfg::BCS + n0, Bv);
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         const float q = s * a[k];
         const float ab = ex2(q);
         const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
-        h[k] = fmaf(ab, h[k], coef * (bc[pp * Cfg::BCS + n0 + k] * uf));
+        h[k] = fmaf(ab, h[k], coef * (Bv[k] * uf));
       }
     }
   }
@@ -300,7 +344,8 @@ __device__ __forceinline__ void bwd_advance(const BwdParams& p, const unsigned c
 // phase 2 body for one block: recompute the states, then the adjoint backwards
 template <typename Cfg, bool FAST>
 __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned char* stage,
-                                          const float* bc, const float* S, float* DY0, float* RED,
+                                          const float* Bt, const float* Ct, const float* S,
+                                          float* DY0, float* RED,
                                           float* WB, unsigned char* OUT, int chl, int part,
                                           int lane, int warp, int n0, int l0, float Dd,
                                           const float (&a)[Cfg::NS], const float (&ra)[Cfg::NS],
@@ -309,11 +354,9 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
                                           float& dD_acc) {
   using IO = typename Cfg::io_t;
   constexpr int NS = Cfg::NS, N = Cfg::N;
-  constexpr unsigned kAll = 0xffffffffu;
-  const float* Bt = bc;
-  const float* Ct = bc + kBwdPos * Cfg::BCS;
 
-  // ---- forward recompute: traj[pp] = h after position pp
+  // ---- forward recompute: traj[pp] = h after position pp; this lane's part of
+  // the contraction sum_n C h goes to RED (the du slot, free until the adjoint)
   float traj[kBwdPos][NS];
   {
     float h[NS];
@@ -325,46 +368,58 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
         const float s = S[chl * Cfg::SCS + pp];
         const float dt = s * kLn2;
         const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
+        float Bv[NS], Cv[NS];
+        ld_states<NS>(Bt + pp * Cfg::BCS + n0, Bv);
+        ld_states<NS>(Ct + pp * Cfg::BCS + n0, Cv);
         float y = 0.0f;
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
           const float q = s * a[k];
           const float ab = ex2(q);
           const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
-          h[k] = fmaf(ab, h[k], coef * (Bt[pp * Cfg::BCS + n0 + k] * uf));
+          h[k] = fmaf(ab, h[k], coef * (Bv[k] * uf));
           traj[pp][k] = h[k];
-          y = fmaf(Ct[pp * Cfg::BCS + n0 + k], h[k], y);
+          y = fmaf(Cv[k], h[k], y);
         }
-        y += __shfl_xor_sync(kAll, y, 1);
-        y += __shfl_xor_sync(kAll, y, 2);
-        const float y0 = fmaf(Dd, uf, y);
-        const float dyf = ld_io<IO>(stage + 3 * Cfg::CHB, chl * Cfg::ROWB, pp);
-        float dy0 = dyf, dzv = 0.0f;
-        if constexpr (Cfg::GATE) {
-          const float zf = ld_io<IO>(stage + 2 * Cfg::CHB, chl * Cfg::ROWB, pp);
-          float sg;
-          if constexpr (sizeof(IO) == 2)
-            sg = rcp(1.0f + ex2(-zf * kLog2e));
-          else
-            sg = 1.0f / (1.0f + expf(-zf));
-          dy0 = dyf * zf * sg;
-          dzv = dyf * y0 * sg * fmaf(zf, 1.0f - sg, 1.0f);
-        }
-        if (part == (pp & 3)) {
-          DY0[chl * Cfg::SCS + pp] = dy0;
-          dD_acc = fmaf(dy0, uf, dD_acc);
-          if constexpr (Cfg::GATE)
-            Io<IO>::store(reinterpret_cast<IO*>(OUT + 2 * Cfg::CHB + chl * Cfg::ROWB) + pp, dzv);
-        }
+        RED[chl * Cfg::REDS + pp * 8 + part] = y;
       }
+    }
+  }
+  __syncwarp();
+  // ---- output before the gate, and the gate's gradients, for this lane's
+  // positions part*kBwdPpl ..: dy0 = dLoss/d(y before the gate), dz
+#pragma unroll
+  for (int i = 0; i < kBwdPpl; ++i) {
+    const int pp = part * kBwdPpl + i;
+    if (l0 + pp < p.seqlen) {
+      const float4 yp = lds128f(RED + chl * Cfg::REDS + pp * 8);
+      const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
+      const float y0 = fmaf(Dd, uf, (yp.x + yp.y) + (yp.z + yp.w));
+      const float dyf = ld_io<IO>(stage + 3 * Cfg::CHB, chl * Cfg::ROWB, pp);
+      float dy0 = dyf;
+      if constexpr (Cfg::GATE) {
+        const float zf = ld_io<IO>(stage + 2 * Cfg::CHB, chl * Cfg::ROWB, pp);
+        float sg;
+        if constexpr (sizeof(IO) == 2)
+          sg = rcp(1.0f + ex2(-zf * kLog2e));
+        else
+          sg = 1.0f / (1.0f + expf(-zf));
+        dy0 = dyf * zf * sg;
+        const float dzv = dyf * y0 * sg * fmaf(zf, 1.0f - sg, 1.0f);
+        Io<IO>::store(reinterpret_cast<IO*>(OUT + 2 * Cfg::CHB + chl * Cfg::ROWB) + pp, dzv);
+      }
+      DY0[chl * Cfg::SCS + pp] = dy0;
+      dD_acc = fmaf(dy0, uf, dD_acc);
     }
   }
   __syncwarp();
 
   // ---- adjoint, positions in reverse
-  float dAb[NS];
+  // dA accumulates per block as dA1 (the Abar term) and dA2 (the coefficient
+  // term; in FAST mode without its common factor 1/A, applied once per block)
+  float dA1[NS], dA2[NS];
 #pragma unroll
-  for (int k = 0; k < NS; ++k) dAb[k] = 0.0f;
+  for (int k = 0; k < NS; ++k) dA1[k] = dA2[k] = 0.0f;
 #pragma unroll
   for (int pp = kBwdPos - 1; pp >= 0; --pp) {
     if (l0 + pp < p.seqlen) {
@@ -373,50 +428,66 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
       const float uf = ld_io<IO>(stage, chl * Cfg::ROWB, pp);
       const float dy0 = DY0[chl * Cfg::SCS + pp];
       float du_p = 0.0f, ddt_p = 0.0f;
-      float dBv[NS], dCv[NS];
+      float dBv[NS], dCv[NS], Bs[NS], Cs[NS];
+      ld_states<NS>(Bt + pp * Cfg::BCS + n0, Bs);
+      ld_states<NS>(Ct + pp * Cfg::BCS + n0, Cs);
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         const float hp = (pp > 0) ? traj[pp > 0 ? pp - 1 : 0][k] : he[k];
-        const float Bv = Bt[pp * Cfg::BCS + n0 + k];
-        const float Cv = Ct[pp * Cfg::BCS + n0 + k];
         const float q = s * a[k];
-        const float ab = ex2(q);
+        const float ab = ex2_fresh(q);
         const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
-        const float gk = fmaf(g[k], an[k], Cv * dy0);
+        const float gk = fmaf(g[k], an[k], Cs[k] * dy0);  // dLoss/dh at this position
         dCv[k] = dy0 * traj[pp][k];
-        dBv[k] = coef * (gk * uf);
-        const float gB = gk * Bv;
-        du_p = fmaf(coef, gB, du_p);
-        const float bu = Bv * uf;
+        const float gc = gk * coef;
+        dBv[k] = gc * uf;
+        du_p = fmaf(gc, Bs[k], du_p);
+        const float bu = Bs[k] * uf;
         const float ga = gk * ab;
+        const float gdt = ga * dt;
+        dA1[k] = fmaf(gdt, hp, dA1[k]);
         if constexpr (Cfg::EULER) {
           ddt_p = fmaf(ga * a[k], hp, fmaf(gk, bu, ddt_p));
-          dAb[k] = fmaf(ga * dt, hp, dAb[k]);
         } else {
           ddt_p = fmaf(ga, fmaf(a[k], hp, bu), ddt_p);
-          const float dcda = dcoef_dA(dt, q, ra[k], ab, coef);
-          dAb[k] = fmaf(ga * dt, hp, fmaf(gk * dcda, bu, dAb[k]));
+          if constexpr (FAST) {
+            // gk dcoef/dA = (gk dt Abar - gk coef) / A; the difference cancels
+            // for small |q|, an absolute error ~ eps |gk B u| dt / |A| that stays
+            // below the terms of larger dt which dominate the sum over positions
+            dA2[k] = fmaf(gdt - gc, bu, dA2[k]);
+          } else {
+            dA2[k] = fmaf(gk * dcoef_dA(dt, q, ra[k], ab, coef), bu, dA2[k]);
+          }
         }
         g[k] = gk;
         an[k] = ab;
       }
       RED[chl * Cfg::REDS + pp * 8 + part] = du_p;
       RED[chl * Cfg::REDS + pp * 8 + 4 + part] = ddt_p;
-      int off;
-      const float sb = bwd_rs<NS>(dBv, lane, &off);
-      const float sc = bwd_rs<NS>(dCv, lane, &off);
+      const float sb = bwd_rs<NS>(dBv);
+      const float sc = bwd_rs<NS>(dCv);
       if (bwd_rs_holder<NS>(lane)) {
-        WB[((warp * 2 + 0) * N + n0 + off) * Cfg::WBS + pp] = sb;
-        WB[((warp * 2 + 1) * N + n0 + off) * Cfg::WBS + pp] = sc;
+        const int n = n0 + bwd_perm<NS>(lane);
+        WB[((warp * 2 + 0) * N + n) * Cfg::WBS + pp] = sb;
+        WB[((warp * 2 + 1) * N + n) * Cfg::WBS + pp] = sc;
       }
     }
   }
 #pragma unroll
-  for (int k = 0; k < NS; ++k) dA[k] += dAb[k];
+  for (int k = 0; k < NS; ++k) dA[k] += FAST ? fmaf(ra[k], dA2[k], dA1[k]) : dA1[k] + dA2[k];
 }
 
-template <typename Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams p) {
+// MODE 0: every CTA, accurate arithmetic (fp32 io, or the Euler term, which needs
+// no expm1).  For bf16 io with the ZOH term the work is split over two launches
+// compiled separately so that the common case is not held to the register
+// budget of the rare one: MODE 1 takes the CTAs whose channels all have
+// |A| >= 1/8 (coefficients from Abar - 1, as the forward's fast path), MODE 2
+// the others (the series near zero); each returns at once from the CTAs of the other.
+constexpr int kBwdAll = 0, kBwdFastTiles = 1, kBwdAccurateTiles = 2;
+
+template <typename Cfg, int MODE>
+__global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdParams p) {
+  constexpr bool FAST = MODE == kBwdFastTiles;
   using IO = typename Cfg::io_t;
   constexpr int NS = Cfg::NS, N = Cfg::N, CH = Cfg::CH;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -431,6 +502,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
   const int64_t row = rowbase + dc;
   const int64_t rows = p.batch * p.dim;
   const int n0 = part * NS;
+  const int perm = bwd_perm<NS>(lane);  // slot k holds state n0 + (k ^ perm)
 
   unsigned char* stage_base = smem + Cfg::OFF_STAGE;
   float* BC = reinterpret_cast<float*>(smem + Cfg::OFF_BC);
@@ -442,23 +514,28 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
   unsigned char* OUT = smem + Cfg::OFF_OUT;
   auto stage = [&](int i) { return stage_base + i * Cfg::STAGE; };
   auto bcbuf = [&](int i) { return BC + i * (Cfg::BCB / 4); };
+  // this lane's order of the parked B and C tiles
+  auto bt = [&](int i) { return bcbuf(i) + perm * kBwdPos * Cfg::BCS; };
+  auto ct = [&](int i) { return bcbuf(i) + (NS + perm) * kBwdPos * Cfg::BCS; };
 
   float a[NS], ra[NS];
   bool big = true;
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
-    a[k] = __ldg(p.A + static_cast<int64_t>(dc) * N + n0 + k);
+    a[k] = __ldg(p.A + static_cast<int64_t>(dc) * N + n0 + (k ^ perm));
     ra[k] = (a[k] != 0.0f) ? 1.0f / a[k] : 0.0f;
     big = big && fabsf(a[k]) >= kExpm1SeriesMaxQ;
   }
-  // bf16 io with every |A| of the warp >= 1/8: Abar - 1 as the ZOH coefficient
-  const bool fast = (sizeof(IO) == 2) && !Cfg::EULER && __all_sync(0xffffffffu, big);
+  if constexpr (MODE != kBwdAll) {
+    const bool cta_fast = __syncthreads_and(big) != 0;
+    if (cta_fast != FAST) return;
+  }
   const float bias = p.bias ? __ldg(p.bias + dc) : 0.0f;
   const float Dd = p.D ? __ldg(p.D + dc) : 0.0f;
 
   float h[NS];
 #pragma unroll
-  for (int k = 0; k < NS; ++k) h[k] = (chv && p.h0) ? p.h0[row * N + n0 + k] : 0.0f;
+  for (int k = 0; k < NS; ++k) h[k] = (chv && p.h0) ? p.h0[row * N + n0 + (k ^ perm)] : 0.0f;
 
   const int nblk = p.nblk;
   IO rb[Cfg::BC_EPT], rc[Cfg::BC_EPT];
@@ -486,14 +563,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
         p.ckpt[(static_cast<int64_t>(j) * rows + row) * N + n0 + k] = h[k];
     }
     __syncwarp();
-    if constexpr (sizeof(IO) == 2 && !Cfg::EULER) {
-      if (fast)
-        bwd_advance<Cfg, true>(p, stage(buf), bcbuf(buf), S, chl, n0, l0, a, ra, h);
-      else
-        bwd_advance<Cfg, false>(p, stage(buf), bcbuf(buf), S, chl, n0, l0, a, ra, h);
-    } else {
-      bwd_advance<Cfg, false>(p, stage(buf), bcbuf(buf), S, chl, n0, l0, a, ra, h);
-    }
+    bwd_advance<Cfg, FAST>(p, stage(buf), bt(buf), S, chl, n0, l0, a, ra, h);
     if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
   }
 
@@ -501,7 +571,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
   float g[NS], an[NS], dA[NS], he[NS], hn[NS];
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
-    g[k] = (chv && p.dh_last) ? p.dh_last[row * N + n0 + k] : 0.0f;
+    g[k] = (chv && p.dh_last) ? p.dh_last[row * N + n0 + (k ^ perm)] : 0.0f;
     an[k] = 1.0f;
     dA[k] = 0.0f;
     hn[k] = 0.0f;
@@ -539,23 +609,14 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
     }
     bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, p.softplus != 0);
     __syncwarp();
-    if constexpr (sizeof(IO) == 2 && !Cfg::EULER) {
-      if (fast)
-        bwd_block<Cfg, true>(p, stage(buf), bcbuf(buf), S, DY0, RED, WB, OUT, chl, part, lane,
-                             warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
-      else
-        bwd_block<Cfg, false>(p, stage(buf), bcbuf(buf), S, DY0, RED, WB, OUT, chl, part, lane,
-                              warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
-    } else {
-      bwd_block<Cfg, false>(p, stage(buf), bcbuf(buf), S, DY0, RED, WB, OUT, chl, part, lane,
-                            warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
-    }
+    bwd_block<Cfg, FAST>(p, stage(buf), bt(buf), ct(buf), S, DY0, RED, WB, OUT, chl, part,
+                         lane, warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
     __syncwarp();
     // per-position totals over the channel's four lanes: du (with the D skip) and
-    // ddelta (through the softplus) for this lane's positions part*4 .. +3
+    // ddelta (through the softplus) for this lane's positions part*kBwdPpl ..
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int pp = part * 4 + i;
+    for (int i = 0; i < kBwdPpl; ++i) {
+      const int pp = part * kBwdPpl + i;
       if (l0 + pp < p.seqlen) {
         const float4 r0 = lds128f(RED + chl * Cfg::REDS + pp * 8);
         const float4 r1 = lds128f(RED + chl * Cfg::REDS + pp * 8 + 4);
@@ -582,7 +643,9 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
     }
     // du, ddelta, dz tiles
     {
-      void* dst[3] = {p.du, p.ddelta, p.dz};
+      auto dst = [&](int t) -> IO* {
+        return static_cast<IO*>(t == 0 ? p.du : t == 1 ? p.ddelta : p.dz);
+      };
       const int ntens = Cfg::GATE ? 3 : 2;
       if constexpr (Cfg::VEC) {
         constexpr int CPR = Cfg::ROWB / 16, PPC = 16 / Cfg::ES;
@@ -590,7 +653,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
           const int k = c % CPR, ch = (c / CPR) % CH, t = c / (CPR * CH);
           const int dd = d0 + ch, l = l0 + k * PPC;
           if (dd < p.dim && l < p.seqlen)
-            *reinterpret_cast<uint4*>(static_cast<IO*>(dst[t]) +
+            *reinterpret_cast<uint4*>(dst(t) +
                                       (rowbase + dd) * static_cast<int64_t>(p.seqlen) + l) =
                 lds128(OUT + t * Cfg::CHB + ch * Cfg::ROWB + k * 16);
         }
@@ -599,7 +662,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
           const int pp = e % kBwdPos, ch = (e / kBwdPos) % CH, t = e / (kBwdPos * CH);
           const int dd = d0 + ch, l = l0 + pp;
           if (dd < p.dim && l < p.seqlen)
-            static_cast<IO*>(dst[t])[(rowbase + dd) * static_cast<int64_t>(p.seqlen) + l] =
+            dst(t)[(rowbase + dd) * static_cast<int64_t>(p.seqlen) + l] =
                 reinterpret_cast<const IO*>(OUT + t * Cfg::CHB + ch * Cfg::ROWB)[pp];
         }
       }
@@ -615,8 +678,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_bwd_kernel(const BwdParams 
   if (chv) {
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
-      p.part_a[row * N + n0 + k] = dA[k];
-      if (p.dh0) p.dh0[row * N + n0 + k] = an[k] * g[k];
+      p.part_a[row * N + n0 + (k ^ perm)] = dA[k];
+      if (p.dh0) p.dh0[row * N + n0 + (k ^ perm)] = an[k] * g[k];
     }
     if (part == 0) {
       p.part_dd[row * 2 + 0] = dD_acc;

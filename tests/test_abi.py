@@ -207,7 +207,7 @@ def test_read_status_rejects_null():
 
 def _bwd_bytes(batch, dim, n, seqlen):
     rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    nblk = (seqlen + 15) // 16
+    nblk = (seqlen + 7) // 8
     tiles = (dim + 31) // 32
     rows = batch * dim
     return (256 + rnd(nblk * rows * n * 4) + rnd(tiles * batch * 2 * n * seqlen * 4)
@@ -215,7 +215,7 @@ def _bwd_bytes(batch, dim, n, seqlen):
 
 
 def test_bwd_workspace_size():
-    """Checkpoints every 16 positions, one dB/dC partial per 32-channel CTA, the
+    """Checkpoints every 8 positions, one dB/dC partial per 32-channel CTA, the
     per-channel dA / dD / bias sums."""
     ws = binding.library().ssm_scan_bwd_workspace_size
     for shape in ((8, 5120, 16, 2048), (1, 1536, 16, 131072), (2, 37, 8, 69), (1, 1, 4, 1)):

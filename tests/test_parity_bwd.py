@@ -3,7 +3,7 @@ fp64 oracle's reverse-mode derivative.
 
 Every gradient is compared with the error metric of tests/helpers.py: 1e-4 for
 fp32 io, 2e-2 for bf16 io (fp32 state).  The shapes span several CTAs of
-channels with a ragged last one, sequences with a ragged last block of 16
+channels with a ragged last one, sequences with a ragged last block of 8
 positions, unaligned rows (element staging) and aligned ones (cp.async staging),
 every dstate, both discretisations, and the optional arguments present and absent.
 """
