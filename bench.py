@@ -490,7 +490,7 @@ def bwd_bytes(cfg) -> int:
     ddelta (and dz) written per element; B, C read and dB, dC written per
     position; fp32 A, D, bias read and dA, dD, bias gradient written."""
     s = 2 if cfg.io == W.BF16 else 4
-    per_elem = (6 + (2 if cfg.gate else 0)) * s
+    per_elem = (5 + (2 if cfg.gate else 0)) * s  # u, delta, dy, du, ddelta (+ z, dz)
     per_pos = 4 * s * cfg.dstate
     params = 2 * 4 * (cfg.dim * cfg.dstate + 2 * cfg.dim)
     return cfg.elements * per_elem + cfg.batch * cfg.seqlen * per_pos + params
