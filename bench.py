@@ -631,6 +631,8 @@ def main():
                          "line is quoted on 2p8b)")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode loop and print its JSON (profiling)")
+    ap.add_argument("--conv-only", action="store_true",
+                    help="run only the conv1d timing and print its JSON (profiling)")
     ap.add_argument("--bwd-only", action="store_true",
                     help="run only the scan backward timing and print its JSON (profiling)")
     ap.add_argument("--decode-steps", type=int, default=None,
@@ -652,6 +654,13 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps(run_decode(dev, S)), flush=True)
+        return 0
+    if args.conv_only:
+        import torch
+        from selective_state_space_115_b300 import binding as S
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(run_conv(dev, S, iters=max(1, min(args.steps, 50)))), flush=True)
         return 0
     if args.bwd_only:
         import torch

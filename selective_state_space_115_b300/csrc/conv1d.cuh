@@ -31,7 +31,38 @@ struct ConvParams {
   void* out;               // [rows, seqlen] (decode: [rows])
   void* state_out;         // [rows, width - 1] or null: the last width - 1 inputs
   void* state;             // decode: [rows, width - 1], updated in place
+  // aligned full-sequence kernel: vectors of this launch (< 2^31), the divisors
+  // vectors-per-row and dim, and row0 % dim
+  uint32_t nvec;
+  FastDivU32 div_vpr, div_dim;
+  uint32_t row0_mod;
 };
+
+// a 16-byte vector of io values to / from fp32
+template <typename IO>
+__device__ __forceinline__ void unpack16(const uint4 v, float* out) {
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (sizeof(IO) == 2) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      out[2 * k] = bf16lo(w4[k]);
+      out[2 * k + 1] = bf16hi(w4[k]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[k] = __uint_as_float(w4[k]);
+  }
+}
+template <typename IO>
+__device__ __forceinline__ uint4 pack16(const float* o) {
+  if constexpr (sizeof(IO) == 2) {
+    return make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                      pack_bf16x2(o[6], o[7]));
+  } else {
+    return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                      __float_as_uint(o[3]));
+  }
+}
 
 template <typename IO>
 __device__ __forceinline__ float conv_act(float v, int silu) {
@@ -133,6 +164,93 @@ __global__ void __launch_bounds__(128) conv1d_fwd_kernel(const ConvParams p) {
           if (t == idx) v = win[t];
         Io<IO>::store(so + k, v);
       }
+    }
+  }
+}
+
+// Aligned rows (seqlen * esize a multiple of 16, 16-byte aligned x and out): the
+// rows are cut into 16-byte vectors of TB positions, numbered row-major, and a
+// CTA of 128 threads takes the U * 128 consecutive vectors from base, thread t
+// vector base + u*128 + t.  All U loads are issued before any arithmetic (U
+// vectors in flight per thread) and parked in shared memory with the NPREV
+// vectors just before the CTA's, so the W - 1 inputs before each vector come from
+// shared memory; only vectors at the start of a row read the carried state (or
+// zero).  The filter width is a template argument: each output costs exactly W
+// multiply-adds.
+template <typename IO, int W>
+__global__ void __launch_bounds__(128) conv1d_fwd_vec_kernel(const ConvParams p) {
+  constexpr int TB = 16 / static_cast<int>(sizeof(IO));  // positions per vector
+  constexpr int NPREV = (W - 1 + TB - 1) / TB;            // previous vectors a window needs
+  constexpr int U = 4;
+  constexpr int WIN = (NPREV + 1) * TB;
+  __shared__ __align__(16) uint4 sv[NPREV + 128 * U];
+  const uint32_t tid = threadIdx.x;
+  const uint32_t vpr = p.div_vpr.d;  // vectors per row
+  const uint32_t cta0 = blockIdx.x * (128u * U);
+  const IO* x = static_cast<const IO*>(p.x) + p.row0 * p.seqlen;
+  // vectors of the launch are contiguous: vector e starts at element e * TB
+
+  uint4 cur[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t e = cta0 + u * 128 + tid;
+    cur[u] = (e < p.nvec) ? __ldg(reinterpret_cast<const uint4*>(x) + e)
+                          : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (NPREV > 0 && tid < NPREV) {
+    const int64_t e = static_cast<int64_t>(cta0) - NPREV + tid;
+    sv[tid] = (e >= 0 && e < p.nvec) ? __ldg(reinterpret_cast<const uint4*>(x) + e)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) sv[NPREV + u * 128 + tid] = cur[u];
+  __syncthreads();
+
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t e = cta0 + u * 128 + tid;
+    if (e >= p.nvec) break;
+    const uint32_t rl = p.div_vpr.div(e);  // row within the launch
+    const uint32_t v = e - rl * vpr;       // vector within the row
+    const int64_t row = p.row0 + rl;
+    const int l0 = static_cast<int>(v) * TB;
+    float win[WIN];
+#pragma unroll
+    for (int k = NPREV; k >= 1; --k) {
+      float* dst = win + (NPREV - k) * TB;
+      if (v >= static_cast<uint32_t>(k)) {
+        unpack16<IO>(sv[NPREV + u * 128 + tid - k], dst);
+      } else {
+        // before position 0: the carried-in inputs, or zero
+        const IO* sr = p.state_in ? static_cast<const IO*>(p.state_in) + row * (W - 1) : nullptr;
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+          const int pos = l0 - k * TB + j;
+          dst[j] = (sr && pos >= -(W - 1)) ? Io<IO>::ldg(sr + (W - 1) + pos) : 0.0f;
+        }
+      }
+    }
+    unpack16<IO>(cur[u], win + NPREV * TB);
+
+    const uint32_t rd = p.row0_mod + rl;
+    const uint32_t d = rd - p.div_dim.div(rd) * p.div_dim.d;  // row % dim
+    float wk[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) wk[k] = __ldg(p.w + d * W + k);
+    const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
+    float o[TB];
+#pragma unroll
+    for (int j = 0; j < TB; ++j) {
+      float acc = bias;
+#pragma unroll
+      for (int k = 0; k < W; ++k) acc = fmaf(wk[k], win[NPREV * TB + j - (W - 1) + k], acc);
+      o[j] = conv_act<IO>(acc, p.silu);
+    }
+    reinterpret_cast<uint4*>(static_cast<IO*>(p.out) + p.row0 * p.seqlen)[e] = pack16<IO>(o);
+    if (p.state_out && v == vpr - 1) {
+      IO* so = static_cast<IO*>(p.state_out) + row * (W - 1);
+#pragma unroll
+      for (int k = 0; k < W - 1; ++k) Io<IO>::store(so + k, win[NPREV * TB + TB - (W - 1) + k]);
     }
   }
 }

@@ -56,6 +56,32 @@ __device__ __forceinline__ float rcp(float x) {
 }
 
 // ---------------------------------------------------------------------------
+// division of 32-bit unsigned integers by an invariant divisor d >= 1 with one
+// multiply-high, an add and two shifts (Granlund and Montgomery, "Division by
+// Invariant Integers using Multiplication", PLDI 1994, the round-up method for
+// N = 32: l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+// q = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) with t = mulhi(m, n))
+// ---------------------------------------------------------------------------
+struct FastDivU32 {
+  uint32_t d, m;
+  int sh1, sh2;
+  __host__ __device__ static FastDivU32 make(uint32_t dv) {
+    FastDivU32 f;
+    f.d = dv;
+    int l = 0;
+    while (l < 32 && (uint64_t(1) << l) < dv) ++l;
+    f.m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - dv)) / dv + 1);
+    f.sh1 = l < 1 ? l : 1;
+    f.sh2 = l > 1 ? l - 1 : 0;
+    return f;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> sh1)) >> sh2;
+  }
+};
+
+// ---------------------------------------------------------------------------
 // packed f32x2 arithmetic (two lanes of fp32 per instruction)
 // ---------------------------------------------------------------------------
 struct f2 {

@@ -29,7 +29,13 @@ def _inputs(io, batch, dim, seqlen, width, seed, state):
 CASES = [
     # io, batch, dim, seqlen, width, state, silu
     (W.BF16, 2, 96, 2048, 4, False, True),    # the Mamba shape (d_conv = 4)
-    (W.BF16, 3, 40, 1000, 4, True, True),     # L not a multiple of 8: scalar tail
+    (W.BF16, 3, 40, 1000, 4, True, True),     # carried state, 125 vectors per row
+    (W.BF16, 2, 37, 64, 3, True, True),       # 8 vectors per row: row starts inside a warp
+    (W.F32, 3, 21, 24, 7, True, True),        # fp32, two previous vectors per window
+    (W.BF16, 1, 5, 8, 8, True, True),         # one vector per row: every window from the state
+    (W.F32, 2, 3, 4, 5, False, True),         # one vector per row, zero history
+    (W.BF16, 2, 64, 4096, 6, True, False),    # several CTAs per row
+    (W.BF16, 1, 8, 1002, 4, True, True),      # L not a multiple of 8: element path
     (W.F32, 2, 33, 517, 4, True, False),      # unaligned rows: element path
     (W.F32, 1, 16, 64, 2, False, True),
     (W.BF16, 1, 8, 3, 7, True, True),         # L < width - 1: history from the state
