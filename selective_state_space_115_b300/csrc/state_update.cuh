@@ -68,9 +68,12 @@ __device__ __forceinline__ void load4(const IO* p, float* out) {
 // states (in shared memory when staged, else in global memory); granule k of the
 // lane's registers holds states 4*((k + rot) % G) .. +3, so lanes that start
 // at different granules spread their 16-byte accesses over all bank groups.
-template <typename IO, typename Cfg>
+// The loads that do not depend on h (the channel's A row and token inputs) are
+// issued first; `wait` then waits for the staged states, so the two memory
+// latencies overlap instead of adding up.
+template <typename IO, typename Cfg, typename Wait>
 __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b, int d, float* hs,
-                                               int rot) {
+                                               int rot, Wait wait) {
   constexpr int N = Cfg::N, G = N / 4;
   const int64_t ch = b * p.dim + d;
   const float* __restrict__ Ap = p.A + static_cast<int64_t>(d) * N;
@@ -82,21 +85,28 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
   for (int k = 0; k < G; ++k) {
     const int g = ((k + rot) & (G - 1)) * 4;
     if constexpr (Cfg::VEC) {
-      const float4 h4 = *reinterpret_cast<const float4*>(hs + g);
       const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ap + g));
-      hv[4 * k] = h4.x; hv[4 * k + 1] = h4.y; hv[4 * k + 2] = h4.z; hv[4 * k + 3] = h4.w;
       Av[4 * k] = a4.x; Av[4 * k + 1] = a4.y; Av[4 * k + 2] = a4.z; Av[4 * k + 3] = a4.w;
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hv[4 * k + i] = hs[g + i];
-        Av[4 * k + i] = __ldg(Ap + g + i);
-      }
+      for (int i = 0; i < 4; ++i) Av[4 * k + i] = __ldg(Ap + g + i);
     }
   }
   const float uv = Io<IO>::ldg(static_cast<const IO*>(p.u) + ch);
   const float dv = Io<IO>::ldg(static_cast<const IO*>(p.delta) + ch);
   const float zv = Cfg::GATE ? Io<IO>::ldg(static_cast<const IO*>(p.z) + ch) : 0.0f;
+  wait();
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int g = ((k + rot) & (G - 1)) * 4;
+    if constexpr (Cfg::VEC) {
+      const float4 h4 = *reinterpret_cast<const float4*>(hs + g);
+      hv[4 * k] = h4.x; hv[4 * k + 1] = h4.y; hv[4 * k + 2] = h4.z; hv[4 * k + 3] = h4.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hv[4 * k + i] = hs[g + i];
+    }
+  }
   const float x2 = fmaf(dv, kLog2e, p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f);
   const float s = p.softplus ? softplus_log2_accurate(x2) : x2;  // dt * log2(e)
 
@@ -164,11 +174,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) state_update_kernel(const Upd
 #pragma unroll
       for (int k = 0; k < G; ++k) cp_async16(ws + (k * 32 + lane) * 4, hrow + (k * 32 + lane) * 4);
       cp_async_commit();
-      cp_async_wait_all();
-      __syncwarp();
       // start granule per lane: 8 consecutive lanes cover all 8 bank groups
       const int rot = (lane >> (G == 4 ? 1 : G == 2 ? 2 : 3)) & (G - 1);
-      update_channel<IO, Cfg>(p, b, d, ws + lane * N, rot);
+      update_channel<IO, Cfg>(p, b, d, ws + lane * N, rot, [] {
+        cp_async_wait_all();
+        __syncwarp();
+      });
       fence_proxy_async_smem();  // the lanes' stores -> visible to the bulk copy
       __syncwarp();
       if (lane == 0) {
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) state_update_kernel(const Upd
       return;
     }
   }
-  if (d < p.dim) update_channel<IO, Cfg>(p, b, d, p.h + (b * p.dim + d) * N, 0);
+  if (d < p.dim) update_channel<IO, Cfg>(p, b, d, p.h + (b * p.dim + d) * N, 0, [] {});
 }
 
 }  // namespace ssm
