@@ -76,6 +76,8 @@ KERNEL_SOURCES = {
     "scan_channel_2p8b": ("scan_channel.cuh", "ssm_device.cuh"),
     "scan_channel_long": ("scan_channel.cuh", "ssm_device.cuh"),
     "state_update_decode": ("state_update.cuh", "ssm_device.cuh"),
+    "scan_bwd_2p8b": ("scan_bwd.cuh", "ssm_device.cuh"),
+    "conv1d_2p8b": ("conv1d.cuh", "ssm_device.cuh"),
 }
 
 
@@ -482,7 +484,9 @@ def run_conv(dev, S, iters=50):
                         f"{'bf16' if CFG.io == W.BF16 else 'fp32'}",
             "ms_per_call": ms, "bytes_per_call": nbytes, "gpu_launches": iters,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "traffic": None, "peak_kind": kind}}
+                         "frac": gbs / hbm_peak,
+                         "traffic": profiled_traffic("conv1d_2p8b") if CFG.name == "2p8b"
+                         else None, "peak_kind": kind}}
 
 
 def bwd_bytes(cfg) -> int:
@@ -534,7 +538,9 @@ def run_bwd(dev, S, iters=20):
             # arithmetic, one for the rest) and the two fixed-order reductions
             "gpu_launches": ((2 if CFG.io == W.BF16 else 1) + 2) * iters,
             "roofline": {"bound": "alu", "achieved": texp, "peak": ex2_peak, "unit": "Texp/s",
-                         "frac": texp / ex2_peak, "traffic": None,
+                         "frac": texp / ex2_peak,
+                         "traffic": profiled_traffic("scan_bwd_2p8b") if CFG.name == "2p8b"
+                         else None,
                          "note": "one ex2 per state update, as the forward; the kernel also "
                                  "recomputes the forward states (two more passes of ex2)"},
             "hbm": {"bytes_per_call": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
