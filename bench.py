@@ -500,6 +500,12 @@ def bwd_bytes(cfg) -> int:
     return cfg.elements * per_elem + cfg.batch * cfg.seqlen * per_pos + params
 
 
+def bwd_split(cfg) -> bool:
+    """Whether the library splits this gradient's sequence into segments (fewer
+    than two 32-channel CTAs per SM, and room for two segments of 256 positions)."""
+    return (cfg.batch * ((cfg.dim + 31) // 32) < 2 * SM_COUNT) and cfg.seqlen >= 512
+
+
 def run_bwd(dev, S, iters=20):
     """The scan's gradient on the bench workload (dy ~ N(0, 1)), through the C ABI."""
     import torch
@@ -535,8 +541,10 @@ def run_bwd(dev, S, iters=20):
                         "ddelta_bias, dh0)",
             "ms_per_call": ms, "value": CFG.elements / (ms * 1e-3), "unit": "elements/s",
             # the gradient kernel (bf16 io: one launch for the CTAs on the fast ZOH
-            # arithmetic, one for the rest) and the two fixed-order reductions
-            "gpu_launches": ((2 if CFG.io == W.BF16 else 1) + 2) * iters,
+            # arithmetic, one for the rest), the segments' first pass when the
+            # sequence is split (as many again), and the two fixed-order reductions
+            "gpu_launches": ((2 if CFG.io == W.BF16 else 1) * (2 if bwd_split(CFG) else 1)
+                             + 2) * iters,
             "roofline": {"bound": "alu", "achieved": texp, "peak": ex2_peak, "unit": "Texp/s",
                          "frac": texp / ex2_peak,
                          "traffic": profiled_traffic("scan_bwd_2p8b") if CFG.name == "2p8b"

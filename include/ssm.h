@@ -269,6 +269,18 @@ SSM_API ssm_status ssm_state_update_ex(int64_t batch, int64_t dim, int64_t dstat
  */
 SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
                                            int64_t seqlen);
+/*
+ * ssm_scan_bwd with an explicit split of the sequence into `segments` pieces (0:
+ * the library's choice; the choice splits only when the (batch row, 32-channel)
+ * CTAs cannot fill the GPU, e.g. long sequences over few channels).  A split adds
+ * a first pass per segment (its end state from a zero state, its own adjoint from a
+ * zero adjoint, its step-size sum); the second pass combines them into each
+ * segment's entering state and end adjoint, as the segmented forward does.
+ * Results agree with the unsplit gradient up to rounding.  Negative `segments`
+ * is SSM_ERR_INVALID_ARG; more segments than 8-position blocks are capped.
+ */
+SSM_API size_t ssm_scan_bwd_ex_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                              int64_t seqlen, int segments);
 SSM_API ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                                 ssm_dtype io, const void* u, const void* delta,
                                 const float* delta_bias, int delta_softplus, const float* A,
@@ -278,6 +290,15 @@ SSM_API ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int6
                                 float* ddelta_bias, float* dh0, void* workspace,
                                 size_t workspace_bytes, ssm_discretization disc,
                                 ssm_stream_t stream);
+SSM_API ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                   ssm_dtype io, const void* u, const void* delta,
+                                   const float* delta_bias, int delta_softplus, const float* A,
+                                   const void* B, const void* C, const float* D, const void* z,
+                                   const float* h0, const void* dy, const float* dh_last,
+                                   void* du, void* ddelta, float* dA, void* dB, void* dC,
+                                   float* dD, void* dz, float* ddelta_bias, float* dh0,
+                                   void* workspace, size_t workspace_bytes,
+                                   ssm_discretization disc, int segments, ssm_stream_t stream);
 
 /*
  * Causal depthwise convolution over time, the step before the scan in the

@@ -48,6 +48,7 @@ _ALGOS.update({v: v for v in list(_ALGOS.values())})
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "ssm_scan_fwd",
             "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_conv1d_fwd",
             "ssm_conv1d_update", "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
+            "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -116,6 +117,11 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_bwd.restype = _int
         lib.ssm_scan_bwd.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
                                      + [_vp] * 18 + [ctypes.c_size_t, _int, _vp])
+        lib.ssm_scan_bwd_ex_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_bwd_ex_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _int]
+        lib.ssm_scan_bwd_ex.restype = _int
+        lib.ssm_scan_bwd_ex.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
+                                        + [_vp] * 18 + [ctypes.c_size_t, _int, _int, _vp])
         lib.ssm_read_device_status.restype = _int
         lib.ssm_read_device_status.argtypes = [_vp, _vp]
         lib.ssm_status_string.restype = ctypes.c_char_p
@@ -241,13 +247,15 @@ def scan_bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> i
 
 
 def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True,
-             h0=None, dh_last=None, want_dh0=True, discretization="zoh", workspace=None):
+             h0=None, dh_last=None, want_dh0=True, discretization="zoh", workspace=None,
+             segments=0):
     """Gradient of scan_fwd for the upstream gradient dy [batch, dim, seqlen] (and
     dh_last [batch, dim, dstate] float32 for the final state).  Takes the forward's
     inputs as passed to scan_fwd.  Returns a dict: du, ddelta, dz (io dtype,
     [batch, dim, seqlen]); dB, dC (io dtype, [batch, dstate, seqlen]); dA [dim, dstate],
     dD [dim] (when D), ddelta_bias [dim] (when delta_bias), dh0 [batch, dim, dstate]
-    (when want_dh0), all float32."""
+    (when want_dh0), all float32.  segments: split of the sequence (0: the
+    library's choice)."""
     if not isinstance(u, torch.Tensor) or not u.is_cuda:
         raise SsmError(SSM_ERR_INVALID_ARG, "u must be a CUDA tensor")
     if u.dim() != 3:
@@ -274,7 +282,9 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
          "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
          "dh0": torch.empty((batch, dim, dstate), **f32) if want_dh0 else None}
     lib = library()
-    nbytes = int(lib.ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen))
+    with torch.cuda.device(dev):
+        nbytes = int(lib.ssm_scan_bwd_ex_workspace_size(batch, dim, dstate, seqlen,
+                                                        int(segments)))
     if workspace is None:
         ws = _bwd_ws_cache.get(dev.index)
         if ws is None or ws.numel() < nbytes:
@@ -284,13 +294,13 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
         ws = workspace
     stream = torch.cuda.current_stream(dev).cuda_stream
     with torch.cuda.device(dev):
-        st = lib.ssm_scan_bwd(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
-                              _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
-                              _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(dy), _ptr(dh_last),
-                              _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
-                              _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]),
-                              _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), _ptr(ws), ws.numel(),
-                              _DISC[discretization], ctypes.c_void_p(stream))
+        st = lib.ssm_scan_bwd_ex(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                 _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
+                                 _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(dy), _ptr(dh_last),
+                                 _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                                 _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]),
+                                 _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), _ptr(ws), ws.numel(),
+                                 _DISC[discretization], int(segments), ctypes.c_void_p(stream))
     _check(st, "ssm_scan_bwd")
     return g
 

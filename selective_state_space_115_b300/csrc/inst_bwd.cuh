@@ -6,16 +6,16 @@
 
 namespace ssm_host {
 
-template <typename Cfg, int MODE>
+template <typename Cfg, int MODE, bool PRE>
 static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s) {
-  auto kern = ssm::scan_bwd_kernel<Cfg, MODE>;
+  auto kern = ssm::scan_bwd_kernel<Cfg, MODE, PRE>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   });
   if (attr != cudaSuccess) return cuda_fail(attr, "scan_bwd smem attribute");
-  const int64_t grid = p.batch * p.tiles;
+  const int64_t grid = static_cast<int64_t>(p.nseg) * p.batch * p.tiles;
   if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;
   kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM, s>>>(p);
   const cudaError_t e = cudaGetLastError();
@@ -23,16 +23,26 @@ static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s) {
   return SSM_OK;
 }
 
+// one pass (PRE: the segments' first pass) of every CTA
+template <typename Cfg, bool PRE>
+static ssm_status bwd_pass(const ssm::BwdParams& p, cudaStream_t s) {
+  if constexpr (sizeof(typename Cfg::io_t) == 2 && !Cfg::EULER) {
+    const ssm_status st = bwd_launch<Cfg, ssm::kBwdFastTiles, PRE>(p, s);
+    if (st != SSM_OK) return st;
+    return bwd_launch<Cfg, ssm::kBwdAccurateTiles, PRE>(p, s);
+  } else {
+    return bwd_launch<Cfg, ssm::kBwdAll, PRE>(p, s);
+  }
+}
+
 template <typename IO, int N, bool GATE, bool EULER, bool VEC>
 static ssm_status bwd_main(const ssm::BwdParams& p, cudaStream_t s) {
   using Cfg = ssm::BwdCfg<IO, N, GATE, EULER, VEC, kBwdThreads>;
-  if constexpr (sizeof(IO) == 2 && !EULER) {
-    const ssm_status st = bwd_launch<Cfg, ssm::kBwdFastTiles>(p, s);
+  if (p.nseg > 1) {
+    const ssm_status st = bwd_pass<Cfg, true>(p, s);
     if (st != SSM_OK) return st;
-    return bwd_launch<Cfg, ssm::kBwdAccurateTiles>(p, s);
-  } else {
-    return bwd_launch<Cfg, ssm::kBwdAll>(p, s);
   }
+  return bwd_pass<Cfg, false>(p, s);
 }
 
 template <typename IO, int N>
@@ -69,8 +79,9 @@ ssm_status launch_scan_bwd(const ssm::BwdParams& p, int dstate, bool gate, bool 
   }
   const int64_t npar = static_cast<int64_t>(p.dim) * dstate + p.dim;
   if (npar > 0) {
+    // the partials are [nseg][batch][dim]: sum over nseg * batch row blocks
     ssm::scan_bwd_reduce_param_kernel<><<<static_cast<unsigned>((npar + 255) / 256), 256, 0, s>>>(
-        p.part_a, p.part_dd, p.batch, p.dim, dstate, dA, dD, dbias);
+        p.part_a, p.part_dd, p.batch * p.nseg, p.dim, dstate, dA, dD, dbias);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "scan_bwd reduce launch");
   }

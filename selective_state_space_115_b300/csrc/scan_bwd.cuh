@@ -67,8 +67,14 @@ struct BwdParams {
   float* dh0;
   float* ckpt;     // [nblk][batch * dim][N]: state entering each block
   float* part_bc;  // [tiles][batch][2][N][seqlen]: per-CTA partial dB (0), dC (1)
-  float* part_a;   // [batch * dim][N]: per-channel dA
-  float* part_dd;  // [batch * dim][2]: per-channel dD, bias gradient
+  float* part_a;   // [nseg][batch * dim][N]: per-channel dA of each segment
+  float* part_dd;  // [nseg][batch * dim][2]: per-channel dD, bias gradient of each segment
+  // sequence split (nseg == 1: none; seg_len = seqlen), segments of seg_len
+  // positions (a multiple of kBwdPos); per (segment, channel) from the first pass:
+  int nseg, seg_len;
+  float* seg_E;    // [nseg][batch * dim][N]: state after the segment from a zero state
+  float* seg_R;    // [nseg][batch * dim][N]: the segment's own adjoint at the position before it
+  float* seg_sum;  // [nseg][batch * dim]: sum of the segment's step sizes (log2 units)
 };
 
 template <typename IO, int N_, bool GATE_, bool EULER_, bool VEC_, int THREADS_ = 128>
@@ -477,6 +483,128 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
   for (int k = 0; k < NS; ++k) dA[k] += FAST ? fmaf(ra[k], dA2[k], dA1[k]) : dA1[k] + dA2[k];
 }
 
+// First pass of the segmented gradient (nseg > 1), one CTA per (segment, batch
+// row, channel tile): the segment's end state from a zero entering state (E), its
+// step-size sum, and the adjoint that its own positions send to the position just
+// before it from a zero adjoint at its end (R = Abar_a g_a with g_l = Abar_{l+1}
+// g_{l+1} + C_l dy0_l).  dy0 does not depend on the states, so R needs no forward
+// pass; with E, R and the sums the second pass gives every segment its true
+// entering state and its true adjoint at the end (the recurrence and its adjoint
+// are linear, and a segment multiplies both by the product of its Abar factors).
+template <typename Cfg, bool FAST>
+__device__ __forceinline__ void bwd_segment_pass(
+    const BwdParams& p, unsigned char* smem, int seg, int64_t b, int d0, int chl, int part, int n0,
+    int perm, bool chv, int64_t row, int64_t rowbase, int64_t rows, int l_begin, int j_begin,
+    int j_end, float bias, const float (&a)[Cfg::NS], const float (&ra)[Cfg::NS]) {
+  using IO = typename Cfg::io_t;
+  constexpr int NS = Cfg::NS, N = Cfg::N;
+  unsigned char* stage_base = smem + Cfg::OFF_STAGE;
+  float* BC = reinterpret_cast<float*>(smem + Cfg::OFF_BC);
+  float* S = reinterpret_cast<float*>(smem + Cfg::OFF_S);
+  float* SG = reinterpret_cast<float*>(smem + Cfg::OFF_SG);
+  auto stage = [&](int i) { return stage_base + i * Cfg::STAGE; };
+  auto bcbuf = [&](int i) { return BC + i * (Cfg::BCB / 4); };
+  auto bt = [&](int i) { return bcbuf(i) + perm * kBwdPos * Cfg::BCS; };
+  auto ct = [&](int i) { return bcbuf(i) + (NS + perm) * kBwdPos * Cfg::BCS; };
+  const int nblk = j_end - j_begin;
+  IO rb[Cfg::BC_EPT], rc[Cfg::BC_EPT];
+  float ssum = 0.0f;
+
+  // forward from a zero state (every segment but the last)
+  if (seg < p.nseg - 1) {
+    float h[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) h[k] = 0.0f;
+    bwd_stage<Cfg>(p, stage(0), rowbase, d0, l_begin, false);
+    cp_async_commit();
+    bwd_bc_fetch<Cfg>(p, b, l_begin, false, rb, rc);
+    bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
+    for (int jj = 0; jj < nblk; ++jj) {
+      const int l0 = (j_begin + jj) * kBwdPos, buf = jj & 1;
+      cp_async_wait_all();
+      __syncthreads();
+      const bool more = jj + 1 < nblk;
+      if (more) {
+        bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 + kBwdPos, false);
+        cp_async_commit();
+        bwd_bc_fetch<Cfg>(p, b, l0 + kBwdPos, false, rb, rc);
+      }
+      bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, false);
+      __syncwarp();
+#pragma unroll
+      for (int pp = 0; pp < kBwdPos; ++pp)
+        if (l0 + pp < p.seqlen) ssum += S[chl * Cfg::SCS + pp];
+      bwd_advance<Cfg, FAST>(p, stage(buf), bt(buf), S, chl, n0, l0, a, ra, h);
+      if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
+    }
+    if (chv) {
+#pragma unroll
+      for (int k = 0; k < NS; ++k) p.seg_E[(seg * rows + row) * N + n0 + (k ^ perm)] = h[k];
+    }
+    __syncthreads();  // the stages are reused below
+  }
+
+  // adjoint from a zero adjoint at the segment's end (every segment but the first)
+  if (seg > 0) {
+    float g[NS], an[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      g[k] = 0.0f;
+      an[k] = 1.0f;
+    }
+    const int l_last = (j_end - 1) * kBwdPos;
+    bwd_stage<Cfg>(p, stage(0), rowbase, d0, l_last, true);
+    cp_async_commit();
+    bwd_bc_fetch<Cfg>(p, b, l_last, true, rb, rc);
+    bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
+    for (int it = 0; it < nblk; ++it) {
+      const int j = j_end - 1 - it, l0 = j * kBwdPos, buf = it & 1;
+      cp_async_wait_all();
+      __syncthreads();
+      const bool more = j > j_begin;
+      if (more) {
+        bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 - kBwdPos, true);
+        cp_async_commit();
+        bwd_bc_fetch<Cfg>(p, b, l0 - kBwdPos, true, rb, rc);
+      }
+      bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, false);
+      __syncwarp();
+      const float* Ct = ct(buf);
+#pragma unroll
+      for (int pp = kBwdPos - 1; pp >= 0; --pp) {
+        if (l0 + pp < p.seqlen) {
+          const float s = S[chl * Cfg::SCS + pp];
+          if (seg == p.nseg - 1) ssum += s;
+          float dy0 = ld_io<IO>(stage(buf) + 3 * Cfg::CHB, chl * Cfg::ROWB, pp);
+          if constexpr (Cfg::GATE) {
+            const float zf = ld_io<IO>(stage(buf) + 2 * Cfg::CHB, chl * Cfg::ROWB, pp);
+            float sg;
+            if constexpr (sizeof(IO) == 2)
+              sg = rcp(1.0f + ex2(-zf * kLog2e));
+            else
+              sg = 1.0f / (1.0f + expf(-zf));
+            dy0 = dy0 * zf * sg;
+          }
+          float Cs[NS];
+          ld_states<NS>(Ct + pp * Cfg::BCS + n0, Cs);
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            g[k] = fmaf(g[k], an[k], Cs[k] * dy0);
+            an[k] = ex2(s * a[k]);
+          }
+        }
+      }
+      if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
+    }
+    if (chv) {
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+        p.seg_R[(seg * rows + row) * N + n0 + (k ^ perm)] = an[k] * g[k];
+    }
+  }
+  if (chv && part == 0) p.seg_sum[seg * rows + row] = ssum;
+}
+
 // MODE 0: every CTA, accurate arithmetic (fp32 io, or the Euler term, which needs
 // no expm1).  For bf16 io with the ZOH term the work is split over two launches
 // compiled separately so that the common case is not held to the register
@@ -485,7 +613,7 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
 // the others (the series near zero); each returns at once from the CTAs of the other.
 constexpr int kBwdAll = 0, kBwdFastTiles = 1, kBwdAccurateTiles = 2;
 
-template <typename Cfg, int MODE>
+template <typename Cfg, int MODE, bool PRE>
 __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdParams p) {
   constexpr bool FAST = MODE == kBwdFastTiles;
   using IO = typename Cfg::io_t;
@@ -493,8 +621,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, part = lane & 3;
   const int chl = tid >> 2;  // channel within the CTA
-  const int64_t b = blockIdx.x / p.tiles;
-  const int d0 = static_cast<int>(blockIdx.x % p.tiles) * CH;
+  // CTA = (segment, batch row, channel tile)
+  const int64_t per_seg = p.batch * p.tiles;
+  const int seg = static_cast<int>(blockIdx.x / per_seg);
+  const int64_t b = (blockIdx.x % per_seg) / p.tiles;
+  const int tile = static_cast<int>(blockIdx.x % p.tiles);
+  const int d0 = tile * CH;
+  const int l_begin = seg * p.seg_len;
+  const int l_end = (p.seqlen - l_begin < p.seg_len) ? p.seqlen : l_begin + p.seg_len;
+  const int j_begin = l_begin / kBwdPos, j_end = (l_end + kBwdPos - 1) / kBwdPos;
   const int d = d0 + chl;
   const bool chv = d < p.dim;
   const int dc = chv ? d : p.dim - 1;  // clamped for parameter reads
@@ -533,157 +668,186 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
   const float bias = p.bias ? __ldg(p.bias + dc) : 0.0f;
   const float Dd = p.D ? __ldg(p.D + dc) : 0.0f;
 
-  float h[NS];
-#pragma unroll
-  for (int k = 0; k < NS; ++k) h[k] = (chv && p.h0) ? p.h0[row * N + n0 + (k ^ perm)] : 0.0f;
-
-  const int nblk = p.nblk;
   IO rb[Cfg::BC_EPT], rc[Cfg::BC_EPT];
-  // ---------------- phase 1: forward, checkpoint entering each block
-  if (nblk > 0) {
-    bwd_stage<Cfg>(p, stage(0), rowbase, d0, 0, false);
-    cp_async_commit();
-    bwd_bc_fetch<Cfg>(p, b, 0, false, rb, rc);
-    bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
-  }
-  for (int j = 0; j < nblk; ++j) {
-    const int l0 = j * kBwdPos, buf = j & 1;
-    cp_async_wait_all();
-    __syncthreads();  // stage j and B of block j visible; block j-1 fully consumed
-    const bool more = j + 1 < nblk;
-    if (more) {
-      bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 + kBwdPos, false);
-      cp_async_commit();
-      bwd_bc_fetch<Cfg>(p, b, l0 + kBwdPos, false, rb, rc);
-    }
-    bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, false);
-    if (chv) {
+  if constexpr (PRE) {
+    bwd_segment_pass<Cfg, FAST>(p, smem, seg, b, d0, chl, part, n0, perm, chv, row, rowbase,
+                                rows, l_begin, j_begin, j_end, bias, a, ra);
+  } else {
+    // state entering the segment: h0, then each earlier segment i folded in as
+    // h <- 2^(A sum_i) h + E_i (the recurrence is linear in h; 2^(A sum_i) is the
+    // product of segment i's Abar factors)
+    float h[NS];
 #pragma unroll
-      for (int k = 0; k < NS; ++k)
-        p.ckpt[(static_cast<int64_t>(j) * rows + row) * N + n0 + k] = h[k];
+    for (int k = 0; k < NS; ++k) h[k] = (chv && p.h0) ? p.h0[row * N + n0 + (k ^ perm)] : 0.0f;
+    if (chv) {
+#pragma unroll 1
+      for (int i = 0; i < seg; ++i) {
+        const float sum = p.seg_sum[i * rows + row];
+        const float* E = p.seg_E + (i * rows + row) * N + n0;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) h[k] = fmaf(ex2(a[k] * sum), h[k], E[k ^ perm]);
+      }
     }
-    __syncwarp();
-    bwd_advance<Cfg, FAST>(p, stage(buf), bt(buf), S, chl, n0, l0, a, ra, h);
-    if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
-  }
 
-  // ---------------- phase 2: blocks in reverse
-  float g[NS], an[NS], dA[NS], he[NS], hn[NS];
-#pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    g[k] = (chv && p.dh_last) ? p.dh_last[row * N + n0 + (k ^ perm)] : 0.0f;
-    an[k] = 1.0f;
-    dA[k] = 0.0f;
-    hn[k] = 0.0f;
-  }
-  float dD_acc = 0.0f, db_acc = 0.0f;
-  __syncthreads();  // phase 1's last block consumed
-  if (nblk > 0) {
-    const int l0 = (nblk - 1) * kBwdPos;
-    bwd_stage<Cfg>(p, stage(0), rowbase, d0, l0, true);
-    cp_async_commit();
-    bwd_bc_fetch<Cfg>(p, b, l0, true, rb, rc);
-    bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
-    if (chv) {
-#pragma unroll
-      for (int k = 0; k < NS; ++k)
-        hn[k] = p.ckpt[(static_cast<int64_t>(nblk - 1) * rows + row) * N + n0 + k];
-    }
-  }
-  for (int it = 0; it < nblk; ++it) {
-    const int j = nblk - 1 - it, l0 = j * kBwdPos, buf = it & 1;
-    cp_async_wait_all();
-    __syncthreads();  // stage of block j visible; the previous block fully consumed
-#pragma unroll
-    for (int k = 0; k < NS; ++k) he[k] = hn[k];
-    const bool more = j > 0;
-    if (more) {
-      bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 - kBwdPos, true);
+    const int nblk = j_end - j_begin;  // blocks of this segment
+    // ---------------- phase 1: forward, checkpoint entering each block
+    if (nblk > 0) {
+      bwd_stage<Cfg>(p, stage(0), rowbase, d0, l_begin, false);
       cp_async_commit();
-      bwd_bc_fetch<Cfg>(p, b, l0 - kBwdPos, true, rb, rc);
+      bwd_bc_fetch<Cfg>(p, b, l_begin, false, rb, rc);
+      bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
+    }
+    for (int jj = 0; jj < nblk; ++jj) {
+      const int j = j_begin + jj, l0 = j * kBwdPos, buf = jj & 1;
+      cp_async_wait_all();
+      __syncthreads();  // stage j and B of block j visible; block j-1 fully consumed
+      const bool more = jj + 1 < nblk;
+      if (more) {
+        bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 + kBwdPos, false);
+        cp_async_commit();
+        bwd_bc_fetch<Cfg>(p, b, l0 + kBwdPos, false, rb, rc);
+      }
+      bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, false);
       if (chv) {
 #pragma unroll
         for (int k = 0; k < NS; ++k)
-          hn[k] = p.ckpt[(static_cast<int64_t>(j - 1) * rows + row) * N + n0 + k];
+          p.ckpt[(static_cast<int64_t>(j) * rows + row) * N + n0 + k] = h[k];
       }
+      __syncwarp();
+      bwd_advance<Cfg, FAST>(p, stage(buf), bt(buf), S, chl, n0, l0, a, ra, h);
+      if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
     }
-    bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, p.softplus != 0);
-    __syncwarp();
-    bwd_block<Cfg, FAST>(p, stage(buf), bt(buf), ct(buf), S, DY0, RED, WB, OUT, chl, part,
-                         lane, warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
-    __syncwarp();
-    // per-position totals over the channel's four lanes: du (with the D skip) and
-    // ddelta (through the softplus) for this lane's positions part*kBwdPpl ..
-#pragma unroll
-    for (int i = 0; i < kBwdPpl; ++i) {
-      const int pp = part * kBwdPpl + i;
-      if (l0 + pp < p.seqlen) {
-        const float4 r0 = lds128f(RED + chl * Cfg::REDS + pp * 8);
-        const float4 r1 = lds128f(RED + chl * Cfg::REDS + pp * 8 + 4);
-        const float du = fmaf(Dd, DY0[chl * Cfg::SCS + pp], (r0.x + r0.y) + (r0.z + r0.w));
-        float dx = (r1.x + r1.y) + (r1.z + r1.w);
-        if (p.softplus) dx *= SG[chl * Cfg::SCS + pp];
-        db_acc += dx;
-        Io<IO>::store(reinterpret_cast<IO*>(OUT + chl * Cfg::ROWB) + pp, du);
-        Io<IO>::store(reinterpret_cast<IO*>(OUT + Cfg::CHB + chl * Cfg::ROWB) + pp, dx);
-      }
-    }
-    __syncthreads();  // WB and OUT complete
-    // dB / dC partials of this CTA: sum the warps
-    for (int v = tid; v < 2 * N * kBwdPos; v += Cfg::THREADS) {
-      const int pp = v % kBwdPos, n = (v / kBwdPos) % N, t = v / (kBwdPos * N);
-      float sum = 0.0f;
-#pragma unroll
-      for (int w = 0; w < Cfg::WARPS; ++w) sum += WB[((w * 2 + t) * N + n) * Cfg::WBS + pp];
-      const int l = l0 + pp;
-      if (l < p.seqlen)
-        p.part_bc[((static_cast<int64_t>(blockIdx.x % p.tiles) * p.batch + b) * 2 + t) * N *
-                      static_cast<int64_t>(p.seqlen) +
-                  static_cast<int64_t>(n) * p.seqlen + l] = sum;
-    }
-    // du, ddelta, dz tiles
-    {
-      auto dst = [&](int t) -> IO* {
-        return static_cast<IO*>(t == 0 ? p.du : t == 1 ? p.ddelta : p.dz);
-      };
-      const int ntens = Cfg::GATE ? 3 : 2;
-      if constexpr (Cfg::VEC) {
-        constexpr int CPR = Cfg::ROWB / 16, PPC = 16 / Cfg::ES;
-        for (int c = tid; c < ntens * CH * CPR; c += Cfg::THREADS) {
-          const int k = c % CPR, ch = (c / CPR) % CH, t = c / (CPR * CH);
-          const int dd = d0 + ch, l = l0 + k * PPC;
-          if (dd < p.dim && l < p.seqlen)
-            *reinterpret_cast<uint4*>(dst(t) +
-                                      (rowbase + dd) * static_cast<int64_t>(p.seqlen) + l) =
-                lds128(OUT + t * Cfg::CHB + ch * Cfg::ROWB + k * 16);
-        }
-      } else {
-        for (int e = tid; e < ntens * CH * kBwdPos; e += Cfg::THREADS) {
-          const int pp = e % kBwdPos, ch = (e / kBwdPos) % CH, t = e / (kBwdPos * CH);
-          const int dd = d0 + ch, l = l0 + pp;
-          if (dd < p.dim && l < p.seqlen)
-            dst(t)[(rowbase + dd) * static_cast<int64_t>(p.seqlen) + l] =
-                reinterpret_cast<const IO*>(OUT + t * Cfg::CHB + ch * Cfg::ROWB)[pp];
-        }
-      }
-    }
-    if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
-  }
 
-  // ---------------- per-channel results
-  dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
-  dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 2);
-  db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 1);
-  db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 2);
-  if (chv) {
+    // ---------------- phase 2: blocks in reverse
+    float g[NS], an[NS], dA[NS], he[NS], hn[NS];
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
-      p.part_a[row * N + n0 + (k ^ perm)] = dA[k];
-      if (p.dh0) p.dh0[row * N + n0 + (k ^ perm)] = an[k] * g[k];
+      g[k] = (chv && p.dh_last) ? p.dh_last[row * N + n0 + (k ^ perm)] : 0.0f;
+      an[k] = 1.0f;
+      dA[k] = 0.0f;
+      hn[k] = 0.0f;
     }
-    if (part == 0) {
-      p.part_dd[row * 2 + 0] = dD_acc;
-      p.part_dd[row * 2 + 1] = db_acc;
+    // adjoint entering the segment from its end: dh_last, then each later segment i
+    // folded in as g <- 2^(A sum_i) g + R_i (the adjoint is linear in g and passes
+    // through segment i's Abar factors)
+    if (chv) {
+#pragma unroll 1
+      for (int i = p.nseg - 1; i > seg; --i) {
+        const float sum = p.seg_sum[i * rows + row];
+        const float* R = p.seg_R + (i * rows + row) * N + n0;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) g[k] = fmaf(ex2(a[k] * sum), g[k], R[k ^ perm]);
+      }
+    }
+    float dD_acc = 0.0f, db_acc = 0.0f;
+    __syncthreads();  // phase 1's last block consumed
+    if (nblk > 0) {
+      const int l0 = (j_end - 1) * kBwdPos;
+      bwd_stage<Cfg>(p, stage(0), rowbase, d0, l0, true);
+      cp_async_commit();
+      bwd_bc_fetch<Cfg>(p, b, l0, true, rb, rc);
+      bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
+      if (chv) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+          hn[k] = p.ckpt[(static_cast<int64_t>(j_end - 1) * rows + row) * N + n0 + k];
+      }
+    }
+    for (int it = 0; it < nblk; ++it) {
+      const int j = j_end - 1 - it, l0 = j * kBwdPos, buf = it & 1;
+      cp_async_wait_all();
+      __syncthreads();  // stage of block j visible; the previous block fully consumed
+#pragma unroll
+      for (int k = 0; k < NS; ++k) he[k] = hn[k];
+      const bool more = j > j_begin;
+      if (more) {
+        bwd_stage<Cfg>(p, stage(buf ^ 1), rowbase, d0, l0 - kBwdPos, true);
+        cp_async_commit();
+        bwd_bc_fetch<Cfg>(p, b, l0 - kBwdPos, true, rb, rc);
+        if (chv) {
+#pragma unroll
+          for (int k = 0; k < NS; ++k)
+            hn[k] = p.ckpt[(static_cast<int64_t>(j - 1) * rows + row) * N + n0 + k];
+        }
+      }
+      bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, p.softplus != 0);
+      __syncwarp();
+      bwd_block<Cfg, FAST>(p, stage(buf), bt(buf), ct(buf), S, DY0, RED, WB, OUT, chl, part,
+                           lane, warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
+      __syncwarp();
+      // per-position totals over the channel's four lanes: du (with the D skip) and
+      // ddelta (through the softplus) for this lane's positions part*kBwdPpl ..
+#pragma unroll
+      for (int i = 0; i < kBwdPpl; ++i) {
+        const int pp = part * kBwdPpl + i;
+        if (l0 + pp < p.seqlen) {
+          const float4 r0 = lds128f(RED + chl * Cfg::REDS + pp * 8);
+          const float4 r1 = lds128f(RED + chl * Cfg::REDS + pp * 8 + 4);
+          const float du = fmaf(Dd, DY0[chl * Cfg::SCS + pp], (r0.x + r0.y) + (r0.z + r0.w));
+          float dx = (r1.x + r1.y) + (r1.z + r1.w);
+          if (p.softplus) dx *= SG[chl * Cfg::SCS + pp];
+          db_acc += dx;
+          Io<IO>::store(reinterpret_cast<IO*>(OUT + chl * Cfg::ROWB) + pp, du);
+          Io<IO>::store(reinterpret_cast<IO*>(OUT + Cfg::CHB + chl * Cfg::ROWB) + pp, dx);
+        }
+      }
+      __syncthreads();  // WB and OUT complete
+      // dB / dC partials of this CTA: sum the warps
+      for (int v = tid; v < 2 * N * kBwdPos; v += Cfg::THREADS) {
+        const int pp = v % kBwdPos, n = (v / kBwdPos) % N, t = v / (kBwdPos * N);
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < Cfg::WARPS; ++w) sum += WB[((w * 2 + t) * N + n) * Cfg::WBS + pp];
+        const int l = l0 + pp;
+        if (l < p.seqlen)
+          p.part_bc[((static_cast<int64_t>(tile) * p.batch + b) * 2 + t) * N *
+                        static_cast<int64_t>(p.seqlen) +
+                    static_cast<int64_t>(n) * p.seqlen + l] = sum;
+      }
+      // du, ddelta, dz tiles
+      {
+        auto dst = [&](int t) -> IO* {
+          return static_cast<IO*>(t == 0 ? p.du : t == 1 ? p.ddelta : p.dz);
+        };
+        const int ntens = Cfg::GATE ? 3 : 2;
+        if constexpr (Cfg::VEC) {
+          constexpr int CPR = Cfg::ROWB / 16, PPC = 16 / Cfg::ES;
+          for (int c = tid; c < ntens * CH * CPR; c += Cfg::THREADS) {
+            const int k = c % CPR, ch = (c / CPR) % CH, t = c / (CPR * CH);
+            const int dd = d0 + ch, l = l0 + k * PPC;
+            if (dd < p.dim && l < p.seqlen)
+              *reinterpret_cast<uint4*>(dst(t) +
+                                        (rowbase + dd) * static_cast<int64_t>(p.seqlen) + l) =
+                  lds128(OUT + t * Cfg::CHB + ch * Cfg::ROWB + k * 16);
+          }
+        } else {
+          for (int e = tid; e < ntens * CH * kBwdPos; e += Cfg::THREADS) {
+            const int pp = e % kBwdPos, ch = (e / kBwdPos) % CH, t = e / (kBwdPos * CH);
+            const int dd = d0 + ch, l = l0 + pp;
+            if (dd < p.dim && l < p.seqlen)
+              dst(t)[(rowbase + dd) * static_cast<int64_t>(p.seqlen) + l] =
+                  reinterpret_cast<const IO*>(OUT + t * Cfg::CHB + ch * Cfg::ROWB)[pp];
+          }
+        }
+      }
+      if (more) bwd_bc_park<Cfg>(bcbuf(buf ^ 1), rb, rc);
+    }
+
+    // ---------------- per-channel results
+    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
+    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 2);
+    db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 1);
+    db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 2);
+    if (chv) {
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        p.part_a[(seg * rows + row) * N + n0 + (k ^ perm)] = dA[k];
+        if (p.dh0 && seg == 0) p.dh0[row * N + n0 + (k ^ perm)] = an[k] * g[k];
+      }
+      if (part == 0) {
+        p.part_dd[(seg * rows + row) * 2 + 0] = dD_acc;
+        p.part_dd[(seg * rows + row) * 2 + 1] = db_acc;
+      }
     }
   }
 }

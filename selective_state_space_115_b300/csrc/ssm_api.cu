@@ -302,8 +302,13 @@ ssm_status ssm_state_update(int64_t batch, int64_t dim, int64_t dstate, ssm_dtyp
 }
 
 size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
-  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1) return kStatusBytes;
-  return bwd_layout(batch, dim, dstate, seqlen).total;
+  return ssm_scan_bwd_ex_workspace_size(batch, dim, dstate, seqlen, 0);
+}
+
+size_t ssm_scan_bwd_ex_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                      int segments) {
+  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1 || segments < 0) return kStatusBytes;
+  return bwd_layout(batch, dim, dstate, seqlen, segments).total;
 }
 
 ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ssm_dtype io,
@@ -314,6 +319,20 @@ ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seql
                         void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
                         void* workspace, size_t workspace_bytes, ssm_discretization disc,
                         ssm_stream_t stream) {
+  return ssm_scan_bwd_ex(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A,
+                         B, C, D, z, h0, dy, dh_last, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+                         dh0, workspace, workspace_bytes, disc, 0, stream);
+}
+
+ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                           ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
+                           int delta_softplus, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* h0, const void* dy,
+                           const float* dh_last, void* du, void* ddelta, float* dA, void* dB,
+                           void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                           void* workspace, size_t workspace_bytes, ssm_discretization disc,
+                           int segments, ssm_stream_t stream) {
+  if (segments < 0) return SSM_ERR_INVALID_ARG;
   ssm_status st = validate_common(batch, dim, dstate, io);
   if (st != SSM_OK) return st;
   if (seqlen < 1 || seqlen > INT32_MAX - 4096) return SSM_ERR_INVALID_ARG;
@@ -324,7 +343,7 @@ ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seql
   if ((z != nullptr) != (dz != nullptr)) return SSM_ERR_INVALID_ARG;
   if (D && !dD) return SSM_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256)) return SSM_ERR_INVALID_ARG;
-  const BwdLayout w = bwd_layout(batch, dim, dstate, seqlen);
+  const BwdLayout w = bwd_layout(batch, dim, dstate, seqlen, segments);
   if (workspace_bytes < w.total) return SSM_ERR_INVALID_ARG;
   const size_t esz = (io == SSM_DTYPE_BF16) ? 2 : 4;
   const void* io_ptrs[12] = {u, delta, B, C, z, dy, du, ddelta, dB, dC, dz, nullptr};
@@ -367,6 +386,11 @@ ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seql
   p.part_bc = reinterpret_cast<float*>(ws + w.off_bc);
   p.part_a = reinterpret_cast<float*>(ws + w.off_a);
   p.part_dd = reinterpret_cast<float*>(ws + w.off_dd);
+  p.nseg = w.nseg;
+  p.seg_len = w.seg_len;
+  p.seg_E = reinterpret_cast<float*>(ws + w.off_E);
+  p.seg_R = reinterpret_cast<float*>(ws + w.off_R);
+  p.seg_sum = reinterpret_cast<float*>(ws + w.off_sum);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool euler = disc == SSM_DISC_EULER;
   float* dD_out = D ? dD : nullptr;

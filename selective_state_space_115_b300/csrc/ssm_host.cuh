@@ -240,27 +240,64 @@ inline size_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, co
 // ---------------------------------------------------------------------------
 // scan gradient workspace: [0, 256) status words; the block checkpoints
 // [nblk][batch * dim][N]; the per-CTA dB / dC partials [tiles][batch][2][N][L];
-// the per-channel dA [batch * dim][N]; dD and the bias gradient [batch * dim][2]
+// the per-(segment, channel) dA [nseg][batch * dim][N], dD and bias gradient
+// [nseg][batch * dim][2]; with segments, their end states and own adjoints
+// [nseg][batch * dim][N] each and step-size sums [nseg][batch * dim]
 // ---------------------------------------------------------------------------
 constexpr int kBwdThreads = 128;
 constexpr int kBwdChannels = kBwdThreads / ssm::kBwdLpc;
+// split sequences until about this many (segment, tile) CTAs per SM: four waves of
+// the four resident CTAs (measured on the long-sequence gradient, B1 D1536 L131072:
+// 13 segments 12.8 ms, 26 10.8 ms, 52 9.9 ms, 78 9.7 ms; unsplit 48.8 ms)
+constexpr int kBwdSegCtasPerSm = 16;
+constexpr int64_t kBwdMinSegLen = 256;   // positions: shorter segments cost more than they gain
 
 struct BwdLayout {
   int64_t nblk = 0, tiles = 0;
-  size_t off_ckpt = 0, off_bc = 0, off_a = 0, off_dd = 0, total = 0;
+  int nseg = 1, seg_len = 0;
+  size_t off_ckpt = 0, off_bc = 0, off_a = 0, off_dd = 0, off_E = 0, off_R = 0, off_sum = 0,
+         total = 0;
 };
 
-inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+// Segments for the gradient: when the (batch row, channel tile) CTAs cannot fill
+// the SMs (fewer than two per SM), split the sequence into about
+// kBwdSegCtasPerSm CTAs per SM, each segment at least kBwdMinSegLen positions, a
+// multiple of the 8-position block.  `segments` > 0 asks for that many (tests).
+inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                            int64_t segments = 0) {
   BwdLayout w;
   w.nblk = (seqlen + ssm::kBwdPos - 1) / ssm::kBwdPos;
   w.tiles = (dim + kBwdChannels - 1) / kBwdChannels;
+  const int64_t ctas = batch * w.tiles;
+  int64_t nseg = 1;
+  if (segments > 0) {
+    nseg = segments;
+  } else if (ctas < 2 * static_cast<int64_t>(sm_count())) {
+    nseg = (static_cast<int64_t>(sm_count()) * kBwdSegCtasPerSm + ctas - 1) / ctas;
+    if (nseg > seqlen / kBwdMinSegLen) nseg = seqlen / kBwdMinSegLen;
+  }
+  if (nseg > w.nblk) nseg = w.nblk;
+  if (nseg < 1) nseg = 1;
+  int64_t len = (seqlen + nseg - 1) / nseg;
+  len = (len + ssm::kBwdPos - 1) / ssm::kBwdPos * ssm::kBwdPos;
+  w.nseg = static_cast<int>((seqlen + len - 1) / len);
+  w.seg_len = static_cast<int>(w.nseg == 1 ? seqlen : len);
   const size_t rows = static_cast<size_t>(batch) * static_cast<size_t>(dim);
+  const size_t ns = static_cast<size_t>(w.nseg);
   w.off_ckpt = kStatusBytes;
   w.off_bc = w.off_ckpt + round_up(static_cast<size_t>(w.nblk) * rows * dstate * 4, 256);
   w.off_a = w.off_bc + round_up(static_cast<size_t>(w.tiles) * batch * 2 * dstate *
                                     static_cast<size_t>(seqlen) * 4, 256);
-  w.off_dd = w.off_a + round_up(rows * dstate * 4, 256);
-  w.total = w.off_dd + round_up(rows * 2 * 4, 256);
+  w.off_dd = w.off_a + round_up(ns * rows * dstate * 4, 256);
+  w.off_E = w.off_dd + round_up(ns * rows * 2 * 4, 256);
+  if (w.nseg > 1) {
+    w.off_R = w.off_E + round_up(ns * rows * dstate * 4, 256);
+    w.off_sum = w.off_R + round_up(ns * rows * dstate * 4, 256);
+    w.total = w.off_sum + round_up(ns * rows * 4, 256);
+  } else {
+    w.off_R = w.off_sum = w.off_E;
+    w.total = w.off_E;
+  }
   return w;
 }
 

@@ -205,21 +205,51 @@ def test_read_status_rejects_null():
     assert lib.ssm_read_device_status(None, None) == binding.SSM_ERR_INVALID_ARG
 
 
-def _bwd_bytes(batch, dim, n, seqlen):
+def _bwd_nseg(batch, dim, seqlen, segments=0, sms=148):
+    """The gradient's sequence split: only when the (batch row, 32-channel) CTAs are
+    fewer than two per SM, about 16 CTAs per SM, segments of >= 256 positions, a
+    multiple of 8 long."""
+    nblk = (seqlen + 7) // 8
+    ctas = batch * ((dim + 31) // 32)
+    nseg = segments
+    if segments == 0:
+        nseg = 1
+        if ctas < 2 * sms:
+            nseg = min((sms * 16 + ctas - 1) // ctas, seqlen // 256)
+    nseg = max(1, min(nseg, nblk))
+    seg_len = -(-seqlen // nseg)
+    seg_len = -(-seg_len // 8) * 8
+    return -(-seqlen // seg_len)
+
+
+def _bwd_bytes(batch, dim, n, seqlen, segments=0):
     rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
     nblk = (seqlen + 7) // 8
     tiles = (dim + 31) // 32
     rows = batch * dim
-    return (256 + rnd(nblk * rows * n * 4) + rnd(tiles * batch * 2 * n * seqlen * 4)
-            + rnd(rows * n * 4) + rnd(rows * 2 * 4))
+    nseg = _bwd_nseg(batch, dim, seqlen, segments)
+    total = (256 + rnd(nblk * rows * n * 4) + rnd(tiles * batch * 2 * n * seqlen * 4)
+             + rnd(nseg * rows * n * 4) + rnd(nseg * rows * 2 * 4))
+    if nseg > 1:
+        total += 2 * rnd(nseg * rows * n * 4) + rnd(nseg * rows * 4)
+    return total
 
 
 def test_bwd_workspace_size():
     """Checkpoints every 8 positions, one dB/dC partial per 32-channel CTA, the
-    per-channel dA / dD / bias sums."""
-    ws = binding.library().ssm_scan_bwd_workspace_size
-    for shape in ((8, 5120, 16, 2048), (1, 1536, 16, 131072), (2, 37, 8, 69), (1, 1, 4, 1)):
+    per-(segment, channel) dA / dD / bias sums, and with a split each segment's end
+    state, own adjoint and step-size sum (without a device the library assumes
+    148 SMs)."""
+    lib = binding.library()
+    ws, wsx = lib.ssm_scan_bwd_workspace_size, lib.ssm_scan_bwd_ex_workspace_size
+    for shape in ((8, 5120, 16, 2048), (1, 1536, 16, 131072), (2, 37, 8, 69), (1, 1, 4, 1),
+                  (1, 64, 4, 4096)):
         assert ws(*shape) == _bwd_bytes(*shape), shape
+        assert wsx(*shape, 0) == ws(*shape)
+    assert _bwd_nseg(8, 5120, 2048) == 1 and _bwd_nseg(1, 1536, 131072) == 50
+    for segs in (1, 2, 3, 7, 1000):
+        assert wsx(2, 37, 8, 517, segs) == _bwd_bytes(2, 37, 8, 517, segs), segs
+    assert wsx(2, 37, 8, 517, -1) == 256
 
 
 def _bwd_call(lib, **kw):
@@ -258,3 +288,13 @@ def _bwd_call(lib, **kw):
 ])
 def test_bwd_validation(kw, expect):
     assert _bwd_call(binding.library(), **kw) == expect
+
+
+def test_bwd_rejects_negative_segments():
+    lib = binding.library()
+    v = lambda q: None if q is None else ctypes.c_void_p(q)  # noqa: E731
+    st = lib.ssm_scan_bwd_ex(2, 8, 16, 64, 1, v(P), v(P), None, 1, v(P), v(P), v(P), None, None,
+                             None, v(P), None, v(P + 4096), v(P + 8192), v(P + 12288),
+                             v(P + 16384), v(P + 20480), None, None, None, None, v(WS), 1 << 30,
+                             0, -2, None)
+    assert st == binding.SSM_ERR_INVALID_ARG

@@ -30,7 +30,7 @@ def f64(x, io):
     return None if x is None else W.to_f64(x, io)
 
 
-def gpu_bwd(x, gr, io, softplus=True, disc="zoh", with_dh_last=True):
+def gpu_bwd(x, gr, io, softplus=True, disc="zoh", with_dh_last=True, segments=0):
     import torch
     g = S().scan_bwd(torch_io(x["u"], io), torch_io(x["delta"], io), torch_f32(x["A"]),
                      torch_io(x["B"], io), torch_io(x["C"], io), torch_io(gr["dy"], io),
@@ -38,7 +38,7 @@ def gpu_bwd(x, gr, io, softplus=True, disc="zoh", with_dh_last=True):
                      delta_bias=torch_f32(x.get("delta_bias")), delta_softplus=softplus,
                      h0=torch_f32(x.get("h0")),
                      dh_last=torch_f32(gr["dh_last"]) if with_dh_last else None,
-                     discretization=disc)
+                     discretization=disc, segments=segments)
     torch.cuda.synchronize()
     return {k: (None if v is None else from_torch(v)) for k, v in g.items()}
 
@@ -131,6 +131,68 @@ def test_bwd_zero_and_small_A(io):
     x["A"] = A
     gr = W.make_scan_grads(cfg, seed=11)
     check(gpu_bwd(x, gr, io), oracle_bwd(x, gr, io), io, what=f"small A {io}")
+
+
+SEGMENT_CASES = [
+    # io, batch, dim, dstate, seqlen, gate, h0, segments, disc
+    (W.BF16, 2, 40, 16, 1000, True, True, 4, "zoh"),     # 125 blocks in 4 segments
+    (W.F32, 1, 37, 16, 517, True, True, 3, "zoh"),       # ragged last segment, element staging
+    (W.BF16, 1, 70, 8, 2048, False, False, 7, "euler"),
+    (W.F32, 2, 33, 4, 96, True, True, 1000, "zoh"),      # capped at one block per segment
+    (W.BF16, 3, 64, 16, 256, True, True, 2, "zoh"),
+]
+
+
+@pytest.mark.parametrize("io,batch,dim,dstate,seqlen,gate,h0,segments,disc", SEGMENT_CASES)
+def test_bwd_segments(io, batch, dim, dstate, seqlen, gate, h0, segments, disc):
+    """The sequence split into segments (first pass: each segment's end state, own
+    adjoint and step-size sum; second pass: the segment with its combined entering
+    state and end adjoint) against the oracle."""
+    cfg = W.ScanConfig("t", batch, dim, dstate, seqlen, io, gate=gate, dt_bias=True,
+                       d_skip="normal", description="")
+    x = W.make_scan_inputs(cfg, seed=seqlen + segments, with_h0=h0)
+    gr = W.make_scan_grads(cfg, seed=seqlen + segments)
+    check(gpu_bwd(x, gr, io, disc=disc, segments=segments),
+          oracle_bwd(x, gr, io, disc=disc), io, what=f"{segments} segments {io} L{seqlen}")
+
+
+def test_bwd_segments_match_unsplit():
+    """A forced split and no split agree to rounding on the same inputs."""
+    io = W.F32
+    cfg = W.ScanConfig("t", 1, 64, 16, 2048, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=8, with_h0=True)
+    gr = W.make_scan_grads(cfg, seed=8)
+    a = gpu_bwd(x, gr, io, segments=1)
+    b = gpu_bwd(x, gr, io, segments=6)
+    for k in GRAD_KEYS:
+        assert rel_err(b[k], a[k]) <= 1e-5, k
+
+
+def test_bwd_long_sampled():
+    """The long-sequence workload (bf16, B1 D1536 N16 L131072, no gate), which the
+    library splits into segments: channel-local gradients, dA, dD, the bias gradient
+    and dh0 on sampled channels against the oracle over those channels."""
+    cfg = W.SCAN_CONFIGS["long"]
+    io = cfg.io
+    x = W.make_scan_inputs(cfg, seed=0)
+    gr = W.make_scan_grads(cfg, seed=0)
+    got = gpu_bwd(x, gr, io)
+    ds = np.array([0, 31, 32, 777, 1535], dtype=np.int64)
+    sub = dict(x)
+    for k in ("u", "delta"):
+        sub[k] = np.ascontiguousarray(x[k][:, ds, :])
+    sub["A"] = np.ascontiguousarray(x["A"][ds])
+    sub["D"] = np.ascontiguousarray(x["D"][ds])
+    sub["delta_bias"] = np.ascontiguousarray(x["delta_bias"][ds])
+    sgr = {"dy": np.ascontiguousarray(gr["dy"][:, ds, :]),
+           "dh_last": np.ascontiguousarray(gr["dh_last"][:, ds, :])}
+    ref = oracle_bwd(sub, sgr, io)
+    gsub = {k: got[k][:, ds] for k in ("du", "ddelta", "dh0")}
+    gsub.update({k: got[k][ds] for k in ("dA", "dD", "ddelta_bias")})
+    check(gsub, ref, io, what="long sampled channels",
+          keys=("du", "ddelta", "dh0", "dA", "dD", "ddelta_bias"))
+    assert np.isfinite(got["dB"]).all() and np.isfinite(got["dC"]).all()
 
 
 def test_bwd_is_deterministic():
