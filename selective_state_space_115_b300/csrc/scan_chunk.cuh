@@ -13,9 +13,12 @@
 // and the state after the last lane is carried (in shared memory) to the next chunk.
 // The 4-D (position, state) tensor exists only as T pairs per lane per state.
 //
-// Loads are plain coalesced global loads (16-byte vectors when the row pitch
-// and the pointers allow, element loads with bounds checks otherwise), so this
-// kernel accepts every shape and alignment.
+// A CTA holds WARPS channels of one batch row, which share B and C: each chunk's B
+// and C tiles ([N][32*T] each) are staged once per CTA in shared memory (cp.async,
+// one chunk ahead, when rows are 16-byte aligned; element loads otherwise), so the
+// per-state loop reads them from shared memory instead of waiting on global loads.
+// u, delta and z are plain coalesced global loads, so this kernel accepts every
+// shape and alignment.
 #pragma once
 
 #include "scan_channel.cuh"
@@ -35,6 +38,7 @@ struct ChunkCfg {
   static constexpr int T = 32 / ESZ;        // positions per lane: 16 bf16 / 8 fp32 (32 bytes)
   static constexpr int TB = 16 / ESZ;       // positions per 16-byte vector
   static constexpr int LCH = 32 * T;        // positions per chunk
+  static constexpr int SMEM = 2 * 2 * N * LCH * ESZ;  // two buffers of the B and C tiles
 };
 
 // T io values starting at position l of a row (row_base points at position 0)
@@ -95,9 +99,63 @@ __device__ __forceinline__ void store_run(IO* row_base, int64_t l, int seqlen, c
   }
 }
 
+// T io values of a staged [position] run in shared memory into fp32
+template <typename IO, int T>
+__device__ __forceinline__ void lds_run(const IO* q, float* out) {
+#pragma unroll
+  for (int v = 0; v < T * static_cast<int>(sizeof(IO)) / 16; ++v) {
+    const uint4 w = *reinterpret_cast<const uint4*>(q + v * (16 / sizeof(IO)));
+    if constexpr (sizeof(IO) == 2) {
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        out[v * 8 + 2 * k] = bf16lo(ws[k]);
+        out[v * 8 + 2 * k + 1] = bf16hi(ws[k]);
+      }
+    } else {
+      out[v * 4 + 0] = __uint_as_float(w.x);
+      out[v * 4 + 1] = __uint_as_float(w.y);
+      out[v * 4 + 2] = __uint_as_float(w.z);
+      out[v * 4 + 3] = __uint_as_float(w.w);
+    }
+  }
+}
+
+// Stage B and C of chunk k of batch row b: tile[t][n][i] = (t ? C : B)[b][n][k*LCH + i],
+// zero past the end of the sequence.
+template <typename IO, typename Cfg>
+__device__ __forceinline__ void chunk_stage_bc(const ScanParams& p, int b, int k, IO* tile) {
+  constexpr int N = Cfg::N, LCH = Cfg::LCH;
+  const IO* src[2] = {static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * N * p.seqlen,
+                      static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * N * p.seqlen};
+  const int64_t l0 = static_cast<int64_t>(k) * LCH;
+  if constexpr (Cfg::VEC) {
+    constexpr int PPV = 16 / static_cast<int>(sizeof(IO));  // positions per 16 bytes
+    constexpr int VPR = LCH / PPV;                          // vectors per state row
+    for (int c = threadIdx.x; c < 2 * N * VPR; c += Cfg::THREADS) {
+      const int v = c % VPR, n = (c / VPR) % N, t = c / (VPR * N);
+      const int64_t l = l0 + static_cast<int64_t>(v) * PPV;
+      const bool ok = l < p.seqlen;
+      const IO* g = (t ? src[1] : src[0]) + (ok ? static_cast<int64_t>(n) * p.seqlen + l : 0);
+      cp_async16_zfill(tile + (t * N + n) * LCH + v * PPV, g, ok);
+    }
+  } else {
+    for (int e = threadIdx.x; e < 2 * N * LCH; e += Cfg::THREADS) {
+      const int i = e % LCH, n = (e / LCH) % N, t = e / (LCH * N);
+      const int64_t l = l0 + i;
+      IO v = IO(0);
+      if (l < p.seqlen) v = (t ? src[1] : src[0])[static_cast<int64_t>(n) * p.seqlen + l];
+      tile[(t * N + n) * LCH + i] = v;
+    }
+  }
+}
+
+// One chunk of one channel for the warp that owns it; `carry` ([N], this warp's,
+// in shared memory) holds the state entering the chunk and receives the state after
+// it; `tile` holds the chunk's B and C.
 template <typename IO, typename Cfg, bool ACC>
-__device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d, int lane,
-                                              float* carry /* [N], this warp's, in shared memory */) {
+__device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d, int lane, int k,
+                                              const IO* tile, float* carry) {
   constexpr int N = Cfg::N, T = Cfg::T, LCH = Cfg::LCH;
   const unsigned FULL = 0xffffffffu;
   const int64_t row = static_cast<int64_t>(b) * p.dim + d;
@@ -105,118 +163,135 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
   const IO* drow = static_cast<const IO*>(p.delta) + row * p.seqlen;
   const IO* zrow = Cfg::GATE ? static_cast<const IO*>(p.z) + row * p.seqlen : nullptr;
   IO* yrow = static_cast<IO*>(p.y) + row * p.seqlen;
-  const IO* Bb = static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * N * p.seqlen;
-  const IO* Cb = static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * N * p.seqlen;
   const float* Arow = p.A + static_cast<int64_t>(d) * N;
-
-  if (lane < N) carry[lane] = p.h0 ? __ldg(p.h0 + row * N + lane) : 0.0f;
-  __syncwarp();
   const float Dd = p.D ? __ldg(p.D + d) : 0.0f;
   const float bias2 = p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f;
 
-  const int nch = (p.seqlen + LCH - 1) / LCH;
-#pragma unroll 1
-  for (int k = 0; k < nch; ++k) {
-    const int64_t l = static_cast<int64_t>(k) * LCH + lane * T;  // this lane's first position
-    float s[T], u[T], y[T];
-    load_run<IO, Cfg>(urow, l, p.seqlen, u);
-    load_run<IO, Cfg>(drow, l, p.seqlen, s);
+  const int64_t l = static_cast<int64_t>(k) * LCH + lane * T;  // this lane's first position
+  float s[T], u[T], y[T];
+  load_run<IO, Cfg>(urow, l, p.seqlen, u);
+  load_run<IO, Cfg>(drow, l, p.seqlen, s);
 #pragma unroll
-    for (int i = 0; i < T; ++i) {
-      const float x2 = fmaf(s[i], kLog2e, bias2);
-      const float sv =
-          p.softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
-      s[i] = (l + i < p.seqlen) ? sv : 0.0f;  // past the end: identity pair (1, 0)
-      y[i] = 0.0f;
-    }
-#pragma unroll 1
-    for (int n = 0; n < N; ++n) {
-      const float An = __ldg(Arow + n);
-      const float IAn = (An == 0.0f) ? 0.0f : 1.0f / An;
-      const float isZn = (An == 0.0f) ? 1.0f : 0.0f;
-      float Bv[T], Cv[T], a[T], bb[T];
-      load_run<IO, Cfg>(Bb + static_cast<int64_t>(n) * p.seqlen, l, p.seqlen, Bv);
-      load_run<IO, Cfg>(Cb + static_cast<int64_t>(n) * p.seqlen, l, p.seqlen, Cv);
-      float P = 1.0f, H = 0.0f;
-#pragma unroll
-      for (int i = 0; i < T; ++i) {
-        const float q = s[i] * An;
-        const float ahw = ex2(q);
-        const float X = Bv[i] * u[i];
-        if constexpr (Cfg::EULER) {
-          a[i] = ACC ? ((fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + exp2m1_accurate(q, ahw) : ahw)
-                     : ahw;
-          bb[i] = (s[i] * kLn2) * X;         // dt B u
-        } else if constexpr (!ACC) {
-          const float nK = X * (-IAn);       // -B u / A
-          a[i] = ahw;
-          bb[i] = fmaf(-ahw, nK, nK);        // (Abar - 1) B u / A
-        } else {
-          const float em1 = exp2m1_accurate(q, ahw);
-          a[i] = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
-          const float coef = fmaf(isZn, s[i] * kLn2, em1 * IAn);
-          bb[i] = coef * X;
-        }
-        H = fmaf(a[i], H, bb[i]);
-        P *= a[i];
-      }
-      // inclusive warp scan of (P, H) over lanes (lane order = position order)
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float Pu = __shfl_up_sync(FULL, P, o);
-        const float Hu = __shfl_up_sync(FULL, H, o);
-        if (lane >= o) {
-          H = fmaf(P, Hu, H);
-          P *= Pu;
-        }
-      }
-      const float Pe = __shfl_up_sync(FULL, P, 1);
-      const float He = __shfl_up_sync(FULL, H, 1);
-      const float P31 = __shfl_sync(FULL, P, 31);
-      const float H31 = __shfl_sync(FULL, H, 31);
-      const float cin = carry[n];
-      float hs = (lane == 0) ? cin : fmaf(Pe, cin, He);
-      __syncwarp();
-      if (lane == 0) carry[n] = fmaf(P31, cin, H31);
-#pragma unroll
-      for (int i = 0; i < T; ++i) {
-        hs = fmaf(a[i], hs, bb[i]);
-        y[i] = fmaf(Cv[i], hs, y[i]);
-      }
-    }
-    float z[T];
-    if constexpr (Cfg::GATE) load_run<IO, Cfg>(zrow, l, p.seqlen, z);
-#pragma unroll
-    for (int i = 0; i < T; ++i) {
-      float v = fmaf(Dd, u[i], y[i]);
-      if constexpr (Cfg::GATE) v *= (ACC ? silu_accurate(z[i]) : silu_fast(z[i]));
-      y[i] = v;
-    }
-    store_run<IO, Cfg>(yrow, l, p.seqlen, y);
-    __syncwarp();
+  for (int i = 0; i < T; ++i) {
+    const float x2 = fmaf(s[i], kLog2e, bias2);
+    const float sv = p.softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
+    s[i] = (l + i < p.seqlen) ? sv : 0.0f;  // past the end: identity pair (1, 0)
+    y[i] = 0.0f;
   }
-  if (p.h_last && lane < N) p.h_last[row * N + lane] = carry[lane];
+#pragma unroll 1
+  for (int n = 0; n < N; ++n) {
+    const float An = __ldg(Arow + n);
+    const float IAn = (An == 0.0f) ? 0.0f : 1.0f / An;
+    const float isZn = (An == 0.0f) ? 1.0f : 0.0f;
+    float Bv[T], Cv[T], a[T], bb[T];
+    lds_run<IO, T>(tile + n * LCH + lane * T, Bv);
+    lds_run<IO, T>(tile + (N + n) * LCH + lane * T, Cv);
+    float P = 1.0f, H = 0.0f;
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+      const float q = s[i] * An;
+      const float ahw = ex2(q);
+      const float X = Bv[i] * u[i];
+      if constexpr (Cfg::EULER) {
+        a[i] = ACC ? ((fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + exp2m1_accurate(q, ahw) : ahw)
+                   : ahw;
+        bb[i] = (s[i] * kLn2) * X;         // dt B u
+      } else if constexpr (!ACC) {
+        const float nK = X * (-IAn);       // -B u / A
+        a[i] = ahw;
+        bb[i] = fmaf(-ahw, nK, nK);        // (Abar - 1) B u / A
+      } else {
+        const float em1 = exp2m1_accurate(q, ahw);
+        a[i] = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
+        const float coef = fmaf(isZn, s[i] * kLn2, em1 * IAn);
+        bb[i] = coef * X;
+      }
+      H = fmaf(a[i], H, bb[i]);
+      P *= a[i];
+    }
+    // inclusive warp scan of (P, H) over lanes (lane order = position order)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float Pu = __shfl_up_sync(FULL, P, o);
+      const float Hu = __shfl_up_sync(FULL, H, o);
+      if (lane >= o) {
+        H = fmaf(P, Hu, H);
+        P *= Pu;
+      }
+    }
+    const float Pe = __shfl_up_sync(FULL, P, 1);
+    const float He = __shfl_up_sync(FULL, H, 1);
+    const float P31 = __shfl_sync(FULL, P, 31);
+    const float H31 = __shfl_sync(FULL, H, 31);
+    const float cin = carry[n];
+    float hs = (lane == 0) ? cin : fmaf(Pe, cin, He);
+    __syncwarp();
+    if (lane == 0) carry[n] = fmaf(P31, cin, H31);
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+      hs = fmaf(a[i], hs, bb[i]);
+      y[i] = fmaf(Cv[i], hs, y[i]);
+    }
+  }
+  float z[T];
+  if constexpr (Cfg::GATE) load_run<IO, Cfg>(zrow, l, p.seqlen, z);
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    float v = fmaf(Dd, u[i], y[i]);
+    if constexpr (Cfg::GATE) v *= (ACC ? silu_accurate(z[i]) : silu_fast(z[i]));
+    y[i] = v;
+  }
+  store_run<IO, Cfg>(yrow, l, p.seqlen, y);
+  __syncwarp();
 }
 
+// Grid: x = batch row * ceil(dim / WARPS) + channel group; warp w of a CTA owns
+// channel group * WARPS + w of that batch row (warps past dim only stage).
 template <typename IO, typename Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS) scan_chunk_kernel(const ScanParams p) {
+  extern __shared__ __align__(16) unsigned char chunk_smem[];
   __shared__ float carry_smem[Cfg::WARPS][Cfg::N];
+  constexpr int N = Cfg::N, LCH = Cfg::LCH;
+  IO* tiles = reinterpret_cast<IO*>(chunk_smem);  // 2 buffers of [2][N][LCH]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* carry = carry_smem[warp];
-  const int64_t ch = static_cast<int64_t>(blockIdx.x) * Cfg::WARPS + warp;
-  if (ch >= static_cast<int64_t>(p.batch) * p.dim) return;  // whole warp leaves together
-  const int b = static_cast<int>(ch / p.dim), d = static_cast<int>(ch % p.dim);
-  bool small_a = false;
+  const int groups = (p.dim + Cfg::WARPS - 1) / Cfg::WARPS;
+  const int b = static_cast<int>(blockIdx.x / groups);
+  const int d = static_cast<int>(blockIdx.x % groups) * Cfg::WARPS + warp;
+  const bool active = d < p.dim;
+  const int64_t row = static_cast<int64_t>(b) * p.dim + d;
+
+  // fast or accurate arithmetic per warp (bf16 io with every |A| >= the fast-path bound)
+  bool acc = true;
   if constexpr (sizeof(IO) == 2) {
-    for (int n = lane; n < Cfg::N; n += 32)
-      small_a |= !(fabsf(__ldg(p.A + static_cast<int64_t>(d) * Cfg::N + n)) >= kFastPathMinAbsA);
-    small_a = __any_sync(0xffffffffu, small_a);
-    if (!small_a) {
-      chunk_channel<IO, Cfg, false>(p, b, d, lane, carry);
-      return;
+    bool small_a = false;
+    if (active)
+      for (int n = lane; n < N; n += 32)
+        small_a |= !(fabsf(__ldg(p.A + static_cast<int64_t>(d) * N + n)) >= kFastPathMinAbsA);
+    acc = __any_sync(0xffffffffu, small_a);
+  }
+  if (active && lane < N) carry[lane] = p.h0 ? __ldg(p.h0 + row * N + lane) : 0.0f;
+
+  const int nch = (p.seqlen + LCH - 1) / LCH;
+  chunk_stage_bc<IO, Cfg>(p, b, 0, tiles);
+  cp_async_commit();
+#pragma unroll 1
+  for (int k = 0; k < nch; ++k) {
+    IO* cur = tiles + (k & 1) * 2 * N * LCH;
+    cp_async_wait_all();
+    __syncthreads();  // chunk k's B and C visible; chunk k - 1's buffer free
+    if (k + 1 < nch) {
+      chunk_stage_bc<IO, Cfg>(p, b, k + 1, tiles + ((k + 1) & 1) * 2 * N * LCH);
+      cp_async_commit();
+    }
+    if (active) {
+      if (acc)
+        chunk_channel<IO, Cfg, true>(p, b, d, lane, k, cur, carry);
+      else
+        chunk_channel<IO, Cfg, false>(p, b, d, lane, k, cur, carry);
     }
   }
-  chunk_channel<IO, Cfg, true>(p, b, d, lane, carry);
+  if (active && p.h_last && lane < N) p.h_last[row * N + lane] = carry[lane];
 }
 
 }  // namespace ssm

@@ -121,9 +121,17 @@ template <typename IO, int N, bool GATE, bool VEC, bool EULER>
 ssm_status launch_chunk(const ScanCall& c, void* workspace, cudaStream_t stream) {
   using Cfg = ChunkCfg<IO, N, GATE, VEC, EULER>;
   ScanParams p = make_params(c, workspace);
-  const int64_t channels = c.batch * c.dim;
-  const unsigned grid = static_cast<unsigned>((channels + Cfg::WARPS - 1) / Cfg::WARPS);
-  ssm::scan_chunk_kernel<IO, Cfg><<<grid, Cfg::THREADS, 0, stream>>>(p);
+  // one CTA per (batch row, group of WARPS channels)
+  const int64_t grid64 = c.batch * ((c.dim + Cfg::WARPS - 1) / Cfg::WARPS);
+  if (grid64 > INT32_MAX) return SSM_ERR_INVALID_ARG;
+  auto kern = ssm::scan_chunk_kernel<IO, Cfg>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  });
+  if (attr != cudaSuccess) return cuda_fail(attr, "scan_chunk smem attribute");
+  kern<<<static_cast<unsigned>(grid64), Cfg::THREADS, Cfg::SMEM, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "scan_chunk launch");
   return SSM_OK;
