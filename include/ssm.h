@@ -344,6 +344,18 @@ SSM_API ssm_status ssm_conv1d_update(int64_t batch, int64_t dim, int64_t width, 
  */
 SSM_API ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t stream);
 
+/*
+ * Check of the device-side timeout path: one CTA waits, with the library's
+ * bounded wait and a limit of `limit_ns` nanoseconds (1e3 .. 1e10), for an
+ * mbarrier phase that only completes when `arrive` is nonzero.  Without the
+ * arrival the wait gives up and the kernel records the timeout in the status words
+ * at the start of `workspace` (>= 16 bytes, 16-byte aligned, zeroed by the caller
+ * beforehand); ssm_read_device_status then returns SSM_ERR_DEVICE_TIMEOUT.  The
+ * kernel always returns normally and the context stays usable.
+ */
+SSM_API ssm_status ssm_selftest_wait(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                     int arrive, ssm_stream_t stream);
+
 /* Static description of a status code. */
 SSM_API const char* ssm_status_string(ssm_status status);
 

@@ -48,7 +48,7 @@ _ALGOS.update({v: v for v in list(_ALGOS.values())})
 EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "ssm_scan_fwd",
             "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_conv1d_fwd",
             "ssm_conv1d_update", "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
-            "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex",
+            "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex", "ssm_selftest_wait",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -122,6 +122,8 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_bwd_ex.restype = _int
         lib.ssm_scan_bwd_ex.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
                                         + [_vp] * 18 + [ctypes.c_size_t, _int, _int, _vp])
+        lib.ssm_selftest_wait.restype = _int
+        lib.ssm_selftest_wait.argtypes = [_vp, ctypes.c_size_t, _i64, _int, _vp]
         lib.ssm_read_device_status.restype = _int
         lib.ssm_read_device_status.argtypes = [_vp, _vp]
         lib.ssm_status_string.restype = ctypes.c_char_p
@@ -303,6 +305,19 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
                                  _DISC[discretization], int(segments), ctypes.c_void_p(stream))
     _check(st, "ssm_scan_bwd")
     return g
+
+
+def selftest_wait(limit_ns: int, arrive: bool, device=None) -> int:
+    """Run the device-side timeout check on a fresh status buffer of its own and
+    return its status: SSM_OK when `arrive`, SSM_ERR_DEVICE_TIMEOUT otherwise."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    lib = library()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib.ssm_selftest_wait(_ptr(ws), ws.numel(), int(limit_ns), int(bool(arrive)),
+                                     ctypes.c_void_p(stream)), "ssm_selftest_wait")
+        return int(lib.ssm_read_device_status(_ptr(ws), ctypes.c_void_p(stream)))
 
 
 def read_device_status(workspace: Optional[torch.Tensor] = None, device=None) -> int:

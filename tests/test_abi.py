@@ -298,3 +298,16 @@ def test_bwd_rejects_negative_segments():
                              v(P + 16384), v(P + 20480), None, None, None, None, v(WS), 1 << 30,
                              0, -2, None)
     assert st == binding.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("ws,nbytes,limit", [
+    (None, 256, 10_000_000),          # no status buffer
+    (WS, 8, 10_000_000),              # too small for the status words
+    (WS + 4, 256, 10_000_000),        # misaligned
+    (WS, 256, 10),                    # limit below 1 us
+    (WS, 256, 20_000_000_000),        # limit above 10 s
+])
+def test_selftest_wait_validation(ws, nbytes, limit):
+    lib = binding.library()
+    v = None if ws is None else ctypes.c_void_p(ws)
+    assert lib.ssm_selftest_wait(v, nbytes, limit, 0, None) == binding.SSM_ERR_INVALID_ARG
