@@ -345,6 +345,31 @@ SSM_API ssm_status ssm_conv1d_update(int64_t batch, int64_t dim, int64_t width, 
 SSM_API ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t stream);
 
 /*
+ * The scan with HOST buffers: u, delta, z, B, C, y, A, D, delta_bias, h0, h_last
+ * as in ssm_scan_fwd_ex but in host memory (page-locked memory lets the copies
+ * overlap; pageable memory works, without overlap).  The batch is cut into pieces
+ * (a batch row, or a range of a row's channels when there are few rows) that
+ * stream through three device staging slots in `workspace`: each piece is copied
+ * in while the previous one is scanned and the one before it copied out, on
+ * streams of the call's own, so the call costs about its host-to-device bytes over
+ * the link.  Blocks until y (and h_last) hold the results.  Returns
+ * SSM_ERR_DEVICE_TIMEOUT if any piece's scan recorded a timeout.
+ *  workspace  device memory, ssm_scan_fwd_host_workspace_size(...) bytes, 256-byte
+ *             aligned; `has_z`, `has_h0`, `has_h_last` say whether those are given
+ */
+SSM_API size_t ssm_scan_fwd_host_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                                int64_t seqlen, ssm_dtype io, int has_z,
+                                                int has_h0, int has_h_last, ssm_algo algo);
+SSM_API ssm_status ssm_scan_fwd_host(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                     ssm_dtype io, const void* u, const void* delta,
+                                     const float* delta_bias, int delta_softplus,
+                                     const float* A, const void* B, const void* C,
+                                     const float* D, const void* z, const float* h0,
+                                     float* h_last, void* y, void* workspace,
+                                     size_t workspace_bytes, ssm_discretization disc,
+                                     ssm_algo algo);
+
+/*
  * Check of the device-side timeout path: one CTA waits, with the library's
  * bounded wait and a limit of `limit_ns` nanoseconds (1e3 .. 1e10), for an
  * mbarrier phase that only completes when `arrive` is nonzero.  Without the

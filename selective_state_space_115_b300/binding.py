@@ -49,6 +49,7 @@ EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "
             "ssm_scan_fwd_algo", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_conv1d_fwd",
             "ssm_conv1d_update", "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
             "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex", "ssm_selftest_wait",
+            "ssm_scan_fwd_host_workspace_size", "ssm_scan_fwd_host",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
             "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
 
@@ -122,6 +123,12 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_bwd_ex.restype = _int
         lib.ssm_scan_bwd_ex.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
                                         + [_vp] * 18 + [ctypes.c_size_t, _int, _int, _vp])
+        lib.ssm_scan_fwd_host_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_fwd_host_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _int, _int,
+                                                         _int, _int, _int]
+        lib.ssm_scan_fwd_host.restype = _int
+        lib.ssm_scan_fwd_host.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
+                                          + [_vp] * 9 + [ctypes.c_size_t, _int, _int])
         lib.ssm_selftest_wait.restype = _int
         lib.ssm_selftest_wait.argtypes = [_vp, ctypes.c_size_t, _i64, _int, _vp]
         lib.ssm_read_device_status.restype = _int
@@ -305,6 +312,53 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
                                  _DISC[discretization], int(segments), ctypes.c_void_p(stream))
     _check(st, "ssm_scan_bwd")
     return g
+
+
+_host_ws_cache = {}
+
+
+def scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                  h0=None, return_last_state=False, out=None, algo="auto",
+                  discretization="zoh", device=None):
+    """The scan on HOST tensors (CPU, ideally pinned): the library streams the batch
+    through device staging buffers in pieces, overlapping copy-in, scan and
+    copy-out, and returns once the outputs are in host memory.  Shapes and dtypes as
+    scan_fwd; A, D, delta_bias, h0 float32 host tensors too.  Returns y (host; `out`
+    if given) and h_last (host) when asked."""
+    for name, t in (("u", u), ("delta", delta), ("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise SsmError(SSM_ERR_INVALID_ARG, f"{name} must be a host (CPU) tensor")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    io = _io_dtype(u)
+    cpu = torch.device("cpu")
+    _need(delta, "delta", (batch, dim, seqlen), u.dtype, cpu)
+    _need(z, "z", (batch, dim, seqlen), u.dtype, cpu, optional=True)
+    _need(B, "B", (batch, dstate, seqlen), u.dtype, cpu)
+    _need(C, "C", (batch, dstate, seqlen), u.dtype, cpu)
+    _need(A, "A", (dim, dstate), torch.float32, cpu)
+    _need(D, "D", (dim,), torch.float32, cpu, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, cpu, optional=True)
+    _need(h0, "h0", (batch, dim, dstate), torch.float32, cpu, optional=True)
+    y = torch.empty_like(u) if out is None else out
+    _need(y, "out", (batch, dim, seqlen), u.dtype, cpu)
+    h_last = torch.empty((batch, dim, dstate), dtype=torch.float32) if return_last_state else None
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    lib = library()
+    with torch.cuda.device(dev):
+        nbytes = int(lib.ssm_scan_fwd_host_workspace_size(
+            batch, dim, dstate, seqlen, io, int(z is not None), int(h0 is not None),
+            int(return_last_state), _ALGOS[algo]))
+        ws = _host_ws_cache.get(dev.index)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+            _host_ws_cache[dev.index] = ws
+        st = lib.ssm_scan_fwd_host(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                   _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
+                                   _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(h_last), _ptr(y),
+                                   _ptr(ws), ws.numel(), _DISC[discretization], _ALGOS[algo])
+    _check(st, "ssm_scan_fwd_host")
+    return (y, h_last) if return_last_state else y
 
 
 def selftest_wait(limit_ns: int, arrive: bool, device=None) -> int:

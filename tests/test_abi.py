@@ -311,3 +311,22 @@ def test_selftest_wait_validation(ws, nbytes, limit):
     lib = binding.library()
     v = None if ws is None else ctypes.c_void_p(ws)
     assert lib.ssm_selftest_wait(v, nbytes, limit, 0, None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_host_scan_workspace_size_and_validation():
+    lib = binding.library()
+    wsz = lib.ssm_scan_fwd_host_workspace_size
+    small = wsz(8, 5120, 16, 2048, 1, 1, 0, 0, 0)
+    # three staging slots of one batch row (u, delta, z, y + B, C) at least
+    assert small >= 3 * (4 * 5120 * 2048 * 2 + 2 * 16 * 2048 * 2)
+    assert wsz(8, 5120, 16, 2048, 1, 1, 1, 1, 0) > small  # room for h0 / h_last slices
+    v = lambda q: None if q is None else ctypes.c_void_p(q)  # noqa: E731
+    args = [8, 64, 16, 256, 1, v(P), v(P), None, 1, v(P), v(P), v(P), None, None, None, None,
+            v(P)]
+    assert lib.ssm_scan_fwd_host(*args, None, 1 << 30, 0, 0) == binding.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_fwd_host(*args, v(WS), 256, 0, 0) == binding.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_fwd_host(*args, v(WS + 16), 1 << 30, 0, 0) == \
+        binding.SSM_ERR_INVALID_ARG
+    bad = list(args)
+    bad[5] = None  # no u
+    assert lib.ssm_scan_fwd_host(*bad, v(WS), 1 << 30, 0, 0) == binding.SSM_ERR_INVALID_ARG
