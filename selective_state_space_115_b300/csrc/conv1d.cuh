@@ -184,6 +184,10 @@ __global__ void __launch_bounds__(128) conv1d_fwd_vec_kernel(const ConvParams p)
   constexpr int U = 4;
   constexpr int WIN = (NPREV + 1) * TB;
   __shared__ __align__(16) uint4 sv[NPREV + 128 * U];
+  // launched with programmatic stream serialisation: wait for the previous kernel
+  // on the stream (and its writes) before reading x, then let the next one launch
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tid = threadIdx.x;
   const uint32_t vpr = p.div_vpr.d;  // vectors per row
   const uint32_t cta0 = blockIdx.x * (128u * U);

@@ -37,8 +37,19 @@ static ssm_status conv_fwd_vec(const ssm::ConvParams& p0, cudaStream_t s) {
     p.nvec = static_cast<uint32_t>(n * vpr);
     p.row0_mod = static_cast<uint32_t>(r0 % p0.dim);
     const int64_t grid = (static_cast<int64_t>(p.nvec) + 128 * 4 - 1) / (128 * 4);
-    ssm::conv1d_fwd_vec_kernel<IO, W><<<static_cast<unsigned>(grid), 128, 0, s>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    // programmatic stream serialisation: this launch overlaps the previous kernel's
+    // last wave; the kernel waits for it before reading x
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, ssm::conv1d_fwd_vec_kernel<IO, W>, p);
     if (e != cudaSuccess) return cuda_fail(e, "conv1d_fwd launch");
   }
   return SSM_OK;

@@ -189,8 +189,20 @@ ssm_status launch_update(const UpdateParams& p0, cudaStream_t stream) {
     const int64_t rows = (p0.batch - b0 < kRowsPerLaunch) ? p0.batch - b0 : kRowsPerLaunch;
     const dim3 grid(static_cast<unsigned>((p.dim + Cfg::THREADS - 1) / Cfg::THREADS),
                     static_cast<unsigned>(rows));
-    ssm::state_update_kernel<IO, Cfg><<<grid, Cfg::THREADS, 0, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    // programmatic stream serialisation: consecutive decode steps overlap the next
+    // step's launch with this one's last wave (the kernel waits for its
+    // predecessor before reading anything)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, ssm::state_update_kernel<IO, Cfg>, p);
     if (e != cudaSuccess) return cuda_fail(e, "state_update launch");
   }
   return SSM_OK;

@@ -161,6 +161,11 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
 template <typename IO, typename Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 4) state_update_kernel(const UpdateParams p) {
   constexpr int N = Cfg::N, G = N / 4;
+  // Launched with programmatic stream serialisation, a step's CTAs may be
+  // scheduled while the previous kernel on the stream is finishing: wait for it
+  // (and its writes) before touching any input, then let the next step do the same.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // grid: x over channel blocks of one batch row, y over batch rows b0 + y
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = p.b0 + blockIdx.y;
