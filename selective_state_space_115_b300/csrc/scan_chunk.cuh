@@ -178,7 +178,7 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
     s[i] = (l + i < p.seqlen) ? sv : 0.0f;  // past the end: identity pair (1, 0)
     y[i] = 0.0f;
   }
-#pragma unroll 1
+#pragma unroll 2
   for (int n = 0; n < N; ++n) {
     const float An = __ldg(Arow + n);
     const float IAn = (An == 0.0f) ? 0.0f : 1.0f / An;
