@@ -9,11 +9,9 @@ namespace ssm_host {
 template <typename Cfg, int MODE, bool PRE>
 static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s) {
   auto kern = ssm::scan_bwd_kernel<Cfg, MODE, PRE>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-  });
+  // per call: the attribute belongs to the current device's context
+  const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (attr != cudaSuccess) return cuda_fail(attr, "scan_bwd smem attribute");
   const int64_t grid = static_cast<int64_t>(p.nseg) * p.batch * p.tiles;
   if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;

@@ -125,11 +125,9 @@ ssm_status launch_chunk(const ScanCall& c, void* workspace, cudaStream_t stream)
   const int64_t grid64 = c.batch * ((c.dim + Cfg::WARPS - 1) / Cfg::WARPS);
   if (grid64 > INT32_MAX) return SSM_ERR_INVALID_ARG;
   auto kern = ssm::scan_chunk_kernel<IO, Cfg>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-  });
+  // per call: the attribute belongs to the current device's context
+  const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (attr != cudaSuccess) return cuda_fail(attr, "scan_chunk smem attribute");
   kern<<<static_cast<unsigned>(grid64), Cfg::THREADS, Cfg::SMEM, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
