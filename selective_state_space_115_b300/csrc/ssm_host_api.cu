@@ -91,7 +91,12 @@ struct Streams {
            cudaEventCreateWithFlags(&comp_done[s], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&out_done[s], cudaEventDisableTiming) == cudaSuccess;
   }
+  // On every return path: no copy of this call may still be writing the caller's
+  // host buffers (or reading them) once the call has returned.
   ~Streams() {
+    if (in) cudaStreamSynchronize(in);
+    if (comp) cudaStreamSynchronize(comp);
+    if (out) cudaStreamSynchronize(out);
     for (int s = 0; s < kSlots; ++s) {
       if (in_done[s]) cudaEventDestroy(in_done[s]);
       if (comp_done[s]) cudaEventDestroy(comp_done[s]);
