@@ -37,6 +37,7 @@ from selective_state_space_115_b300 import workloads as W  # noqa: E402
 
 METRIC = "selective-scan elements/s (B·D·L) and achieved HBM GB/s vs B300 roofline"
 CFG = W.SCAN_CONFIGS["2p8b"]
+FLUSH_L2 = False
 DEC = W.DECODE_CONFIGS["decode"]
 DECODE_STEPS = DEC.steps
 SM_COUNT = 148
@@ -272,8 +273,11 @@ def bench_config(impl_note: str):
             f"{CFG.batch}, dim {CFG.dim}, dstate {CFG.dstate}, seqlen {CFG.seqlen}, {gate}, "
             f"dt bias = inverse softplus of log-uniform dt, A[d,n] = -(n+1), D ~ N(0,1)")
     mb = scan_bytes(CFG) / 1e6
-    l2 = (f"inputs larger than L2 ({mb:.0f} MB per step vs 126 MB L2); no flush" if mb > 126
-          else f"inputs ({mb:.0f} MB) fit in the 126 MB L2: unflushed, L2-warm")
+    if FLUSH_L2:
+        l2 = f"L2 flushed before every step (256 MB write, untimed); {mb:.0f} MB per step"
+    else:
+        l2 = (f"inputs larger than L2 ({mb:.0f} MB per step vs 126 MB L2); no flush"
+              if mb > 126 else f"inputs ({mb:.0f} MB) fit in the 126 MB L2: unflushed, L2-warm")
     return {"workload": desc, "batch": CFG.batch, "dim": CFG.dim, "dstate": CFG.dstate,
             "seqlen": CFG.seqlen, "io": io, "impl": impl_note, "l2": l2,
             "parallelism": "one independent problem per GPU (weak scaling)"}
@@ -332,16 +336,30 @@ def run_gpu(args):
     if sampler:
         sampler.mark()
     t0 = time.perf_counter()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    if args.flush_l2:
+        # every step starts from a cold L2: a 256 MB write (twice the L2) before it,
+        # outside the step's own pair of events
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        dev_ms = sum(a.elapsed_time(b) for a, b in evs)
+    else:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        dev_ms = ev0.elapsed_time(ev1)
     wall = time.perf_counter() - t0
     if sampler:
         sampler.mark()
     barrier(world)
-    dev_ms = ev0.elapsed_time(ev1)
     clocks = sampler.stop() if sampler else None
     assert S.read_device_status() == 0, "device-side wait timed out in the timed region"
     ms_step = max_over_ranks(dev_ms / args.steps, world, dev)
@@ -646,6 +664,9 @@ def main():
                          "line is quoted on 2p8b)")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode loop and print its JSON (profiling)")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write 256 MB between timed steps (each step timed alone from a cold "
+                         "L2; for workloads whose inputs fit in L2)")
     ap.add_argument("--conv-only", action="store_true",
                     help="run only the conv1d timing and print its JSON (profiling)")
     ap.add_argument("--bwd-only", action="store_true",
@@ -653,8 +674,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decode loop length (default 1024; fewer for ncu)")
     args = ap.parse_args()
-    global CFG, DECODE_STEPS
+    global CFG, DECODE_STEPS, FLUSH_L2
     CFG = W.SCAN_CONFIGS[args.workload]
+    FLUSH_L2 = args.flush_l2
     if args.batch:
         CFG = dataclasses.replace(CFG, batch=args.batch)
     if args.decode_steps:
