@@ -85,7 +85,7 @@ class Oracle:
         lib.oracle_state_update.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [_i64, _i64, _i64, _dp, _dp, _dp, _dp,
                                             ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp,
-                                            ctypes.c_int]
+                                            ctypes.c_int, ctypes.c_int]
         lib.oracle_scan_bwd.restype = ctypes.c_int
         lib.oracle_scan_bwd.argtypes = [_i64, _i64, _i64, _i64, _dp, _dp, _dp, ctypes.c_int,
                                         _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
@@ -147,7 +147,7 @@ class Oracle:
         return (y, h_last) if return_last_state else y
 
     def state_update(self, h, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                     delta_softplus=True, discretization: str = "zoh"):
+                     delta_softplus=True, discretization: str = "zoh", nthreads: int = 1):
         """One decode step in fp64.  h [b,d,n] (copied, not modified); u, delta, z [b,d];
         B, C [b,n].  Returns (y [b,d], h_new [b,d,n])."""
         h = np.array(h, dtype=np.float64, copy=True, order="C")
@@ -160,7 +160,7 @@ class Oracle:
         rc = self.lib.oracle_state_update(batch, dim, dstate, _ptr(h), _ptr(u), _ptr(delta),
                                           _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
                                           _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
-                                          _euler(discretization))
+                                          _euler(discretization), int(nthreads))
         if rc != 0:
             raise RuntimeError("oracle_state_update failed")
         return y, h

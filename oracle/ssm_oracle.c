@@ -206,23 +206,30 @@ int oracle_scan_rows(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
 }
 
 /* Single-token state update, h updated in place.
- * h [batch, dim, dstate]; u, delta, z, y [batch, dim]; B, C [batch, dstate]. */
+ * h [batch, dim, dstate]; u, delta, z, y [batch, dim]; B, C [batch, dstate].
+ * Channels are independent; `nthreads` > 1 only spreads whole channels over
+ * threads and does not change any arithmetic. */
 int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double* h,
                         const double* u, const double* delta, const double* delta_bias,
                         int delta_softplus, const double* A, const double* B, const double* C,
-                        const double* D, const double* z, double* y, int euler)
+                        const double* D, const double* z, double* y, int euler, int nthreads)
 {
     if (batch < 0 || dim < 0 || dstate <= 0)
         return -1;
-    for (int64_t b = 0; b < batch; ++b) {
-        for (int64_t d = 0; d < dim; ++d) {
-            const int64_t i = b * dim + d;
-            y[i] = oracle_step(dstate, h + i * dstate, u[i], delta[i],
-                               delta_bias ? delta_bias[d] : 0.0, delta_softplus,
-                               A + d * dstate, B + b * dstate, C + b * dstate, 1,
-                               D ? D[d] : 0.0, z ? z + i : NULL, euler);
-        }
+    const int64_t rows = batch * dim;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+#endif
+    for (int64_t i = 0; i < rows; ++i) {
+        const int64_t b = i / dim, d = i % dim;
+        y[i] = oracle_step(dstate, h + i * dstate, u[i], delta[i],
+                           delta_bias ? delta_bias[d] : 0.0, delta_softplus,
+                           A + d * dstate, B + b * dstate, C + b * dstate, 1,
+                           D ? D[d] : 0.0, z ? z + i : NULL, euler);
     }
+    (void)nthreads;
     return 0;
 }
 
