@@ -6,8 +6,10 @@
 
 namespace ssm_host {
 
+// `overlap`: launched with programmatic stream serialisation, so that it may start
+// while the previous launch (the accurate CTAs) still runs
 template <typename Cfg, int MODE, bool PRE>
-static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s) {
+static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s, bool overlap = false) {
   auto kern = ssm::scan_bwd_kernel<Cfg, MODE, PRE>;
   // per call: the attribute belongs to the current device's context
   const cudaError_t attr =
@@ -15,19 +17,33 @@ static ssm_status bwd_launch(const ssm::BwdParams& p, cudaStream_t s) {
   if (attr != cudaSuccess) return cuda_fail(attr, "scan_bwd smem attribute");
   const int64_t grid = static_cast<int64_t>(p.nseg) * p.batch * p.tiles;
   if (grid > INT32_MAX) return SSM_ERR_INVALID_ARG;
-  kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM, s>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = overlap ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return cuda_fail(e, "scan_bwd launch");
   return SSM_OK;
 }
 
-// one pass (PRE: the segments' first pass) of every CTA
+// one pass (PRE: the segments' first pass) of every CTA.  bf16 ZOH: the CTAs that
+// need the series coefficients (small |A| or vanishing steps, per the classify
+// kernel's flags) run in the first launch, which lets the second (the fast
+// coefficients, compiled apart for its lower register count) start at once; the
+// second's block 0 waits for the first before it exits, so whatever follows on the
+// stream sees both.
 template <typename Cfg, bool PRE>
 static ssm_status bwd_pass(const ssm::BwdParams& p, cudaStream_t s) {
   if constexpr (sizeof(typename Cfg::io_t) == 2 && !Cfg::EULER) {
-    const ssm_status st = bwd_launch<Cfg, ssm::kBwdFastTiles, PRE>(p, s);
+    const ssm_status st = bwd_launch<Cfg, ssm::kBwdAccurateTiles, PRE>(p, s);
     if (st != SSM_OK) return st;
-    return bwd_launch<Cfg, ssm::kBwdAccurateTiles, PRE>(p, s);
+    return bwd_launch<Cfg, ssm::kBwdFastTiles, PRE>(p, s, true);
   } else {
     return bwd_launch<Cfg, ssm::kBwdAll, PRE>(p, s);
   }
@@ -36,6 +52,13 @@ static ssm_status bwd_pass(const ssm::BwdParams& p, cudaStream_t s) {
 template <typename IO, int N, bool GATE, bool EULER, bool VEC>
 static ssm_status bwd_main(const ssm::BwdParams& p, cudaStream_t s) {
   using Cfg = ssm::BwdCfg<IO, N, GATE, EULER, VEC, kBwdThreads>;
+  if constexpr (sizeof(IO) == 2 && !EULER) {
+    const int64_t grid = static_cast<int64_t>(p.nseg) * p.batch * p.tiles;
+    ssm::scan_bwd_classify_kernel<N><<<static_cast<unsigned>(grid), 128, 0, s>>>(
+        p, VEC, const_cast<unsigned char*>(p.cta_fast));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "scan_bwd classify launch");
+  }
   if (p.nseg > 1) {
     const ssm_status st = bwd_pass<Cfg, true>(p, s);
     if (st != SSM_OK) return st;

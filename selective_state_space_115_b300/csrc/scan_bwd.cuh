@@ -75,6 +75,8 @@ struct BwdParams {
   float* seg_E;    // [nseg][batch * dim][N]: state after the segment from a zero state
   float* seg_R;    // [nseg][batch * dim][N]: the segment's own adjoint at the position before it
   float* seg_sum;  // [nseg][batch * dim]: sum of the segment's step sizes (log2 units)
+  // [nseg * batch * tiles] (bf16 ZOH): 1 where the CTA takes the fast coefficients
+  const unsigned char* cta_fast;
 };
 
 template <typename IO, int N_, bool GATE_, bool EULER_, bool VEC_, int THREADS_ = 128>
@@ -421,8 +423,7 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
   __syncwarp();
 
   // ---- adjoint, positions in reverse
-  // dA accumulates per block as dA1 (the Abar term) and dA2 (the coefficient
-  // term; in FAST mode without its common factor 1/A, applied once per block)
+  // dA accumulates per block as dA1 (the Abar term) and dA2 (the coefficient term)
   float dA1[NS], dA2[NS];
 #pragma unroll
   for (int k = 0; k < NS; ++k) dA1[k] = dA2[k] = 0.0f;
@@ -456,14 +457,11 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
           ddt_p = fmaf(ga * a[k], hp, fmaf(gk, bu, ddt_p));
         } else {
           ddt_p = fmaf(ga, fmaf(a[k], hp, bu), ddt_p);
-          if constexpr (FAST) {
-            // gk dcoef/dA = (gk dt Abar - gk coef) / A; the difference cancels
-            // for small |q|, an absolute error ~ eps |gk B u| dt / |A| that stays
-            // below the terms of larger dt which dominate the sum over positions
-            dA2[k] = fmaf(gdt - gc, bu, dA2[k]);
-          } else {
-            dA2[k] = fmaf(gk * dcoef_dA(dt, q, ra[k], ab, coef), bu, dA2[k]);
-          }
+          // dcoef/dA from its series near zero on the fast path too: the difference
+          // (dt Abar - coef) / A cancels like dt^2 while its rounding and the
+          // hardware ex2's error stay ~2^-24 |B u / A|, so at small |dt A| it would be
+          // lost (its relative error grows like 2^-23 / (dt A)^2)
+          dA2[k] = fmaf(gk * dcoef_dA(dt, q, ra[k], ab, coef), bu, dA2[k]);
         }
         g[k] = gk;
         an[k] = ab;
@@ -480,7 +478,7 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
     }
   }
 #pragma unroll
-  for (int k = 0; k < NS; ++k) dA[k] += FAST ? fmaf(ra[k], dA2[k], dA1[k]) : dA1[k] + dA2[k];
+  for (int k = 0; k < NS; ++k) dA[k] += dA1[k] + dA2[k];
 }
 
 // First pass of the segmented gradient (nseg > 1), one CTA per (segment, batch
@@ -653,17 +651,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
   auto bt = [&](int i) { return bcbuf(i) + perm * kBwdPos * Cfg::BCS; };
   auto ct = [&](int i) { return bcbuf(i) + (NS + perm) * kBwdPos * Cfg::BCS; };
 
+  if constexpr (MODE != kBwdAll) {
+    // the accurate launch runs first and lets the fast launch start at once (they write
+    // disjoint CTAs' outputs); the fast launch's block 0 waits for it before exiting
+    if constexpr (MODE == kBwdAccurateTiles) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if ((p.cta_fast[blockIdx.x] != 0) != FAST) {
+      if (MODE == kBwdFastTiles && blockIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      return;
+    }
+  }
   float a[NS], ra[NS];
-  bool big = true;
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
     a[k] = __ldg(p.A + static_cast<int64_t>(dc) * N + n0 + (k ^ perm));
     ra[k] = (a[k] != 0.0f) ? 1.0f / a[k] : 0.0f;
-    big = big && fabsf(a[k]) >= kExpm1SeriesMaxQ;
-  }
-  if constexpr (MODE != kBwdAll) {
-    const bool cta_fast = __syncthreads_and(big) != 0;
-    if (cta_fast != FAST) return;
   }
   const float bias = p.bias ? __ldg(p.bias + dc) : 0.0f;
   const float Dd = p.D ? __ldg(p.D + dc) : 0.0f;
@@ -850,6 +851,63 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
       }
     }
   }
+  if constexpr (MODE == kBwdFastTiles) {
+    if (blockIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+}
+
+// Per CTA of the gradient (segment, batch row, tile of 32 channels), whether the fast
+// coefficients (Abar - 1) / A hold (bf16 io, ZOH): every |A| of its channels at least
+// kFastPathMinAbsA, and every step of its positions with |q| = s |A| at least
+// kBwdFastPathMinQ (s = dt log2 e; softplus is monotone, so the smallest raw step
+// decides).  With Abar = ex2(q) the coefficient (Abar - 1) / A carries an error of
+// about 2^-24 / |q ln 2| of itself (measured near the limit: below 0.5 %), so a tile
+// whose steps vanish needs the series.
+constexpr float kBwdFastPathMinQ = 1.52587890625e-05f;  // 2^-16
+
+template <int N>
+__global__ void __launch_bounds__(128) scan_bwd_classify_kernel(const BwdParams p, bool vec,
+                                                                unsigned char* flags) {
+  const int tid = threadIdx.x, chl = tid >> 2, part = tid & 3;
+  const int64_t per_seg = p.batch * p.tiles;
+  const int seg = static_cast<int>(blockIdx.x / per_seg);
+  const int64_t b = (blockIdx.x % per_seg) / p.tiles;
+  const int tile = static_cast<int>(blockIdx.x % p.tiles);
+  const int d = tile * (128 / kBwdLpc) + chl;
+  const int l_begin = seg * p.seg_len;
+  const int l_end = (p.seqlen - l_begin < p.seg_len) ? p.seqlen : l_begin + p.seg_len;
+  bool ok = true;
+  if (d < p.dim) {
+    float amin = fabsf(__ldg(p.A + static_cast<int64_t>(d) * N));
+#pragma unroll
+    for (int n = 1; n < N; ++n) amin = fminf(amin, fabsf(__ldg(p.A + static_cast<int64_t>(d) * N + n)));
+    ok = amin >= kFastPathMinAbsA;
+    if (ok) {
+      const uint16_t* row = static_cast<const uint16_t*>(p.delta) +
+                            (b * p.dim + d) * static_cast<int64_t>(p.seqlen);
+      float xmin = 3.0e38f;
+      if (vec) {
+        // 16-byte rows: segment starts are multiples of 8 positions, and a vector
+        // reaching past l_end stays inside the row (its length is a multiple of 8)
+        for (int l = l_begin + part * 8; l < l_end; l += 32) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + l));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (l + 2 * k < l_end) xmin = fminf(xmin, bf16lo(ws[k]));
+            if (l + 2 * k + 1 < l_end) xmin = fminf(xmin, bf16hi(ws[k]));
+          }
+        }
+      } else {
+        for (int l = l_begin + part; l < l_end; l += 4) xmin = fminf(xmin, bf16_to_f32(row[l]));
+      }
+      const float x2 = (xmin + (p.bias ? __ldg(p.bias + d) : 0.0f)) * kLog2e;
+      const float s = p.softplus ? softplus_log2_accurate(x2) : x2;
+      ok = s * amin >= kBwdFastPathMinQ;
+    }
+  }
+  ok = __syncthreads_and(ok) != 0;
+  if (tid == 0) flags[blockIdx.x] = ok ? 1 : 0;
 }
 
 // dB, dC [batch][N][seqlen] = sum over a batch row's CTAs of the partials, in

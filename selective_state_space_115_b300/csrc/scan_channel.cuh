@@ -73,10 +73,6 @@ struct ScanParams {
 //                segment with outputs
 constexpr int kModeFull = 0, kModeStates = 1, kModeCarry = 2;
 
-// |A| below this (or A == 0) sends a bf16 channel group to the accurate path: the fast
-// path forms (Abar - 1) w as Abar (h + w) - w, whose absolute error grows like
-// 2^-22 |B u / A|.
-constexpr float kFastPathMinAbsA = 0.125f;
 
 template <typename IO, int N_, bool GATE_, int LPC_, int S_, int RB_, bool EULER_ = false>
 struct ChanCfg {
@@ -275,18 +271,108 @@ __device__ __forceinline__ void reduce_scatter(const float* v, float* out, float
 }
 
 // ---------------------------------------------------------------------------
-// one chunk of positions for one lane (its channel's row `row` of the tiles,
-// its states part*NS .. part*NS + NS - 1)
+// the state updates and partial contractions of one 16-byte block of positions
+// for one lane (its states part*NS .. part*NS + NS - 1).  AR selects the update
+// arithmetic: kArFast the fast form Abar (h + w) - w; kArNeg (every A of the channel
+// group negative) h + coef (A h + B u) with coef = (2^q - 1) / A from the branch-free
+// estimate; kArGen the expm1 series near zero and the dt limit at A == 0.
 // ---------------------------------------------------------------------------
-template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL>
+template <typename Cfg, bool OUT, int AR>
+__device__ __forceinline__ void chan_positions(const float* bcfB, const float* bcfC, int blk,
+                                               int part, const float* uj, const float* sj,
+                                               const float* Areg, const float* nIA, float* h,
+                                               float* acc) {
+  constexpr int N = Cfg::N, NS = Cfg::NS, TB = Cfg::TB;
+  constexpr bool UACC = AR != kArFast;
+#pragma unroll
+  for (int j = 0; j < TB; ++j) {
+    const int lc = blk * TB + j;  // position within the chunk
+    const float dtj = sj[j] * kLn2;  // dt (Euler input term)
+    (void)dtj;
+    const float* Bp = bcfB + lc * N + part * NS;
+    const float* Cp = bcfC + lc * N + part * NS;
+    // contraction in a fixed order for every lane split: a packed pair sum per
+    // group of 4 states, then a tree over the groups (and over lanes in
+    // reduce_scatter), so 1, 2 and 4 lanes per channel give identical bits
+    float pg[NS / 4];
+#pragma unroll
+    for (int m = 0; m < NS; m += 4) {
+      f2 a2 = mk2(0.0f, 0.0f);
+      const float4 Bv = lds128f(Bp + m);
+      const float4 Cv = OUT ? lds128f(Cp + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+      const float cv[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
+#pragma unroll
+      for (int pp = 0; pp < 4; pp += 2) {
+        const int i = m + pp;
+        if constexpr (!UACC) {
+          const f2 q = mul2(mk2(sj[j], sj[j]), mk2(Areg[i], Areg[i + 1]));
+          const f2 a = mk2(ex2(q.x), ex2(q.y));
+          const f2 X = mul2(mk2(bv[pp], bv[pp + 1]), mk2(uj[j], uj[j]));
+          f2 hn;
+          if constexpr (Cfg::EULER) {
+            const f2 W = mul2(X, mk2(dtj, dtj));                // dt B u
+            hn = fma2(a, mk2(h[i], h[i + 1]), W);               // Abar h + dt B u
+          } else {
+            const f2 nw = mul2(X, mk2(nIA[i], nIA[i + 1]));     // -w = -B u / A
+            const f2 t = sub2(mk2(h[i], h[i + 1]), nw);         // h + w
+            hn = fma2(a, t, nw);                                // Abar (h + w) - w
+          }
+          h[i] = hn.x;
+          h[i + 1] = hn.y;
+        } else if constexpr (AR == kArNeg && !Cfg::EULER) {
+          // h + (2^q - 1) / A (A h + B u) = Abar h + coef B u; with nq = -q and
+          // 1 - 2^q from its branch-free estimate, coef = (1 - 2^q) (-1 / A)
+          const f2 nq = mul2(mk2(-sj[j], -sj[j]), mk2(Areg[i], Areg[i + 1]));
+          const f2 a = mk2(ex2(-nq.x), ex2(-nq.y));
+          const f2 coef = mul2(one_minus_exp2_neg2(nq, a), mk2(nIA[i], nIA[i + 1]));
+          const f2 bu = mul2(mk2(bv[pp], bv[pp + 1]), mk2(uj[j], uj[j]));
+          const f2 hh = mk2(h[i], h[i + 1]);
+          const f2 hn = fma2(coef, fma2(mk2(Areg[i], Areg[i + 1]), hh, bu), hh);
+          h[i] = hn.x;
+          h[i + 1] = hn.y;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float A0 = Areg[i + e];
+            const float q = sj[j] * A0;
+            const float ahw = ex2(q);
+            const float em1 = exp2m1_accurate(q, ahw);
+            const float a = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
+            // (Abar - 1) / A, or dt at A == 0
+            const float coef =
+                (Cfg::EULER || A0 == 0.0f) ? sj[j] * kLn2 : em1 * -nIA[i + e];
+            h[i + e] = fmaf(a, h[i + e], coef * (bv[pp + e] * uj[j]));
+          }
+        }
+        if constexpr (OUT) a2 = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), a2);
+      }
+      pg[m / 4] = a2.x + a2.y;
+    }
+    if constexpr (NS == 16)
+      acc[j] = (pg[0] + pg[1]) + (pg[2] + pg[3]);
+    else if constexpr (NS == 8)
+      acc[j] = pg[0] + pg[1];
+    else
+      acc[j] = pg[0];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// one chunk of positions for one lane (its channel's row `row` of the tiles,
+// its states part*NS .. part*NS + NS - 1).  ACC: accurate arithmetic for the
+// whole chunk (fp32 io, or a channel group with small |A|); otherwise each block
+// whose step sizes reach below `s_min` (a state update with |dt A log2 e| under
+// kFastPathMinQ) takes the accurate update, the rest the fast one.
+// ---------------------------------------------------------------------------
+template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG>
 __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile, const float* bcfB,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
                                            const float* nIA, float Dd, float bias2, int softplus,
-                                           float* h, float& ssum) {
+                                           float s_min, float* h, float& ssum) {
   constexpr bool OUT = MODE != kModeStates;  // this pass writes y
-  constexpr int N = Cfg::N, NS = Cfg::NS, LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB,
-                RB = Cfg::RB;
+  constexpr int LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB, RB = Cfg::RB;
   const uint8_t* tu = stage;
   const uint8_t* td = stage + Cfg::TILE;
   const uint8_t* tz = stage + 2 * Cfg::TILE;
@@ -315,66 +401,22 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
       for (int j = 0; j < TB; ++j) ssum += sj[j];
     }
     float acc[TB];
+    constexpr int AR_ACC = NEG ? kArNeg : kArGen;
+    if constexpr (ACC || Cfg::EULER) {
+      // the Euler input term dt B u has no cancellation: the fast form holds for any dt
+      chan_positions<Cfg, OUT, ACC ? AR_ACC : kArFast>(bcfB, bcfC, blk, part, uj, sj, Areg, nIA,
+                                                       h, acc);
+    } else {
+      // a step too small for Abar (h + w) - w (its error relative to the update grows
+      // like 2^-22 / |q|): this block takes the accurate update.  The decision depends
+      // only on the channel's own step sizes and A row, so every lane split takes it alike.
+      float smallest = sj[0];
 #pragma unroll
-    for (int j = 0; j < TB; ++j) {
-      const int lc = blk * TB + j;  // position within the chunk
-      const float dtj = sj[j] * kLn2;  // dt (Euler input term)
-      (void)dtj;
-      const float* Bp = bcfB + lc * N + part * NS;
-      const float* Cp = bcfC + lc * N + part * NS;
-      // contraction in a fixed order for every lane split: a packed pair sum per
-      // group of 4 states, then a tree over the groups (and over lanes in
-      // reduce_scatter), so 1, 2 and 4 lanes per channel give identical bits
-      float pg[NS / 4];
-#pragma unroll
-      for (int m = 0; m < NS; m += 4) {
-        f2 a2 = mk2(0.0f, 0.0f);
-        const float4 Bv = lds128f(Bp + m);
-        const float4 Cv = OUT ? lds128f(Cp + m) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
-        const float cv[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
-#pragma unroll
-        for (int pp = 0; pp < 4; pp += 2) {
-          const int i = m + pp;
-          if constexpr (!ACC) {
-            const f2 q = mul2(mk2(sj[j], sj[j]), mk2(Areg[i], Areg[i + 1]));
-            const f2 a = mk2(ex2(q.x), ex2(q.y));
-            const f2 X = mul2(mk2(bv[pp], bv[pp + 1]), mk2(uj[j], uj[j]));
-            f2 hn;
-            if constexpr (Cfg::EULER) {
-              const f2 W = mul2(X, mk2(dtj, dtj));                // dt B u
-              hn = fma2(a, mk2(h[i], h[i + 1]), W);               // Abar h + dt B u
-            } else {
-              const f2 nw = mul2(X, mk2(nIA[i], nIA[i + 1]));     // -w = -B u / A
-              const f2 t = sub2(mk2(h[i], h[i + 1]), nw);         // h + w
-              hn = fma2(a, t, nw);                                // Abar (h + w) - w
-            }
-            h[i] = hn.x;
-            h[i + 1] = hn.y;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float A0 = Areg[i + e];
-              const float q = sj[j] * A0;
-              const float ahw = ex2(q);
-              const float em1 = exp2m1_accurate(q, ahw);
-              const float a = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
-              // (Abar - 1) / A, or dt at A == 0
-              const float coef =
-                  (Cfg::EULER || A0 == 0.0f) ? sj[j] * kLn2 : em1 * -nIA[i + e];
-              h[i + e] = fmaf(a, h[i + e], coef * (bv[pp + e] * uj[j]));
-            }
-          }
-          if constexpr (OUT) a2 = fma2(mk2(cv[pp], cv[pp + 1]), mk2(h[i], h[i + 1]), a2);
-        }
-        pg[m / 4] = a2.x + a2.y;
-      }
-      if constexpr (NS == 16)
-        acc[j] = (pg[0] + pg[1]) + (pg[2] + pg[3]);
-      else if constexpr (NS == 8)
-        acc[j] = pg[0] + pg[1];
+      for (int j = 1; j < TB; ++j) smallest = fminf(smallest, sj[j]);
+      if (!(smallest >= s_min))
+        chan_positions<Cfg, OUT, AR_ACC>(bcfB, bcfC, blk, part, uj, sj, Areg, nIA, h, acc);
       else
-        acc[j] = pg[0];
+        chan_positions<Cfg, OUT, kArFast>(bcfB, bcfC, blk, part, uj, sj, Areg, nIA, h, acc);
     }
     if constexpr (!OUT) continue;
     // full contraction of this lane's positions, then D skip, gate, rounding
@@ -459,17 +501,31 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
   const float bias2 = (valid && p.bias) ? __ldg(p.bias + d) * kLog2e : 0.0f;
   // fast or accurate arithmetic, decided per aligned group of 32 channels (every
   // warp of every lane split lies inside one group, so a channel's arithmetic does
-  // not depend on the split): accurate when any |A| of the group is below 1/8
-  bool accurate = true;
-  if constexpr (sizeof(IO) == 2) {
+  // not depend on the split): accurate when any |A| of the group is below 1/8; the
+  // accurate update without branches when every A of the group is negative
+  bool accurate = true, neg = true;
+  {
     const int dg = (d0 + (tid >> 5) * (32 / Cfg::LPC)) / 32 * 32 + lane;  // lane's channel
-    bool small_a = false;
+    bool small_a = false, nonneg = false;
     if (dg < p.dim) {
 #pragma unroll
-      for (int i = 0; i < N; ++i)
-        small_a |= !(fabsf(__ldg(p.A + static_cast<int64_t>(dg) * N + i)) >= kFastPathMinAbsA);
+      for (int i = 0; i < N; ++i) {
+        const float a = __ldg(p.A + static_cast<int64_t>(dg) * N + i);
+        small_a |= !(fabsf(a) >= kFastPathMinAbsA);
+        nonneg |= !(a < 0.0f);
+      }
     }
-    accurate = __any_sync(0xffffffffu, small_a);
+    if constexpr (sizeof(IO) == 2) accurate = __any_sync(0xffffffffu, small_a);
+    neg = !__any_sync(0xffffffffu, nonneg);
+  }
+  // smallest step size (log2 units) the fast update takes for this channel: every
+  // state's |q| = s |A| must reach kFastPathMinQ
+  float s_min = 0.0f;
+  if (sizeof(IO) == 2 && !accurate && valid) {
+    float amin = fabsf(__ldg(p.A + static_cast<int64_t>(d) * N));
+#pragma unroll
+    for (int i = 1; i < N; ++i) amin = fminf(amin, fabsf(__ldg(p.A + static_cast<int64_t>(d) * N + i)));
+    s_min = kFastPathMinQ / amin;
   }
 
   if (tid == 0) {
@@ -546,24 +602,25 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
     uint8_t* ytile = smem + Cfg::OFF_Y + (k & 1) * Cfg::TILE;
     const int l0 = l_begin + k * LC;
     const bool tail = l0 + LC > p.seqlen;
-    if constexpr (sizeof(IO) == 2) {
-      if (!accurate) {
-        if (!tail)
-          chan_chunk<Cfg, IO, MODE, false, false>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
-                                                  p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h,
-                                                  ssum);
-        else
-          chan_chunk<Cfg, IO, MODE, false, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
-                                                 p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h,
-                                                 ssum);
-      } else {
-        chan_chunk<Cfg, IO, MODE, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
-                                              p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h, ssum);
+    // (the group flags are warp-uniform: every lane of a warp takes the same branch)
+#define SSM_CHAN_CHUNK(ACC, TAIL, NEG)                                                        \
+  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,   \
+                                            p.seqlen, Areg, nIA, Dd, bias2, p.softplus, s_min, \
+                                            h, ssum)
+    bool fast_chunk = false;
+    if constexpr (sizeof(IO) == 2) fast_chunk = !accurate;
+    if (fast_chunk) {
+      if constexpr (sizeof(IO) == 2) {
+        if (neg) {
+          if (!tail) SSM_CHAN_CHUNK(false, false, true); else SSM_CHAN_CHUNK(false, true, true);
+        } else {
+          if (!tail) SSM_CHAN_CHUNK(false, false, false); else SSM_CHAN_CHUNK(false, true, false);
+        }
       }
     } else {
-      chan_chunk<Cfg, IO, MODE, true, true>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,
-                                            p.seqlen, Areg, nIA, Dd, bias2, p.softplus, h, ssum);
+      if (neg) SSM_CHAN_CHUNK(true, true, true); else SSM_CHAN_CHUNK(true, true, false);
     }
+#undef SSM_CHAN_CHUNK
     fence_proxy_async_smem();  // y tile writes -> visible to the TMA store
   }
   __syncthreads();

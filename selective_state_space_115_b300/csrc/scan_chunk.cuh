@@ -150,34 +150,16 @@ __device__ __forceinline__ void chunk_stage_bc(const ScanParams& p, int b, int k
   }
 }
 
-// One chunk of one channel for the warp that owns it; `carry` ([N], this warp's,
-// in shared memory) holds the state entering the chunk and receives the state after
-// it; `tile` holds the chunk's B and C.
-template <typename IO, typename Cfg, bool ACC>
-__device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d, int lane, int k,
-                                              const IO* tile, float* carry) {
+// The per-state loop of one chunk for the warp that owns the channel: pairs, warp
+// scan, carry and replay with y += C h.  AR: kArFast (1 - Abar) B u / -A, kArNeg the
+// accurate coefficient for negative A, kArGen the accurate one for any A.
+template <typename IO, typename Cfg, int AR>
+__device__ __forceinline__ void chunk_states(const float* Arow, int lane, const IO* tile,
+                                             const float* s, const float* u, float* y,
+                                             float* carry) {
+  constexpr bool UACC = AR != kArFast;
   constexpr int N = Cfg::N, T = Cfg::T, LCH = Cfg::LCH;
   const unsigned FULL = 0xffffffffu;
-  const int64_t row = static_cast<int64_t>(b) * p.dim + d;
-  const IO* urow = static_cast<const IO*>(p.u) + row * p.seqlen;
-  const IO* drow = static_cast<const IO*>(p.delta) + row * p.seqlen;
-  const IO* zrow = Cfg::GATE ? static_cast<const IO*>(p.z) + row * p.seqlen : nullptr;
-  IO* yrow = static_cast<IO*>(p.y) + row * p.seqlen;
-  const float* Arow = p.A + static_cast<int64_t>(d) * N;
-  const float Dd = p.D ? __ldg(p.D + d) : 0.0f;
-  const float bias2 = p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f;
-
-  const int64_t l = static_cast<int64_t>(k) * LCH + lane * T;  // this lane's first position
-  float s[T], u[T], y[T];
-  load_run<IO, Cfg>(urow, l, p.seqlen, u);
-  load_run<IO, Cfg>(drow, l, p.seqlen, s);
-#pragma unroll
-  for (int i = 0; i < T; ++i) {
-    const float x2 = fmaf(s[i], kLog2e, bias2);
-    const float sv = p.softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
-    s[i] = (l + i < p.seqlen) ? sv : 0.0f;  // past the end: identity pair (1, 0)
-    y[i] = 0.0f;
-  }
 #pragma unroll 2
   for (int n = 0; n < N; ++n) {
     const float An = __ldg(Arow + n);
@@ -193,13 +175,17 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
       const float ahw = ex2(q);
       const float X = Bv[i] * u[i];
       if constexpr (Cfg::EULER) {
-        a[i] = ACC ? ((fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + exp2m1_accurate(q, ahw) : ahw)
-                   : ahw;
+        a[i] = UACC ? ((fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + exp2m1_accurate(q, ahw) : ahw)
+                    : ahw;
         bb[i] = (s[i] * kLn2) * X;         // dt B u
-      } else if constexpr (!ACC) {
+      } else if constexpr (!UACC) {
         const float nK = X * (-IAn);       // -B u / A
         a[i] = ahw;
         bb[i] = fmaf(-ahw, nK, nK);        // (Abar - 1) B u / A
+      } else if constexpr (AR == kArNeg) {
+        const float em1 = exp2m1_neg(q, ahw);
+        a[i] = 1.0f + em1;
+        bb[i] = (em1 * IAn) * X;           // (Abar - 1) / A B u
       } else {
         const float em1 = exp2m1_accurate(q, ahw);
         a[i] = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
@@ -232,6 +218,52 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
       hs = fmaf(a[i], hs, bb[i]);
       y[i] = fmaf(Cv[i], hs, y[i]);
     }
+  }
+}
+
+// One chunk of one channel for the warp that owns it; `carry` ([N], this warp's,
+// in shared memory) holds the state entering the chunk and receives the state after
+// it; `tile` holds the chunk's B and C.  ACC: accurate arithmetic throughout (fp32
+// io, or small |A|); otherwise a chunk holding a step with |q| = s |A| below
+// kFastPathMinQ (s_min = kFastPathMinQ / min |A|) takes the accurate update.
+template <typename IO, typename Cfg, bool ACC>
+__device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d, int lane, int k,
+                                              const IO* tile, float* carry, float s_min,
+                                              bool neg) {
+  constexpr int T = Cfg::T, LCH = Cfg::LCH;
+  const int64_t row = static_cast<int64_t>(b) * p.dim + d;
+  const IO* urow = static_cast<const IO*>(p.u) + row * p.seqlen;
+  const IO* drow = static_cast<const IO*>(p.delta) + row * p.seqlen;
+  const IO* zrow = Cfg::GATE ? static_cast<const IO*>(p.z) + row * p.seqlen : nullptr;
+  IO* yrow = static_cast<IO*>(p.y) + row * p.seqlen;
+  const float* Arow = p.A + static_cast<int64_t>(d) * Cfg::N;
+  const float Dd = p.D ? __ldg(p.D + d) : 0.0f;
+  const float bias2 = p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f;
+
+  const int64_t l = static_cast<int64_t>(k) * LCH + lane * T;  // this lane's first position
+  float s[T], u[T], y[T];
+  load_run<IO, Cfg>(urow, l, p.seqlen, u);
+  load_run<IO, Cfg>(drow, l, p.seqlen, s);
+  bool slow = false;
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    const float x2 = fmaf(s[i], kLog2e, bias2);
+    const float sv = p.softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
+    const bool in = l + i < p.seqlen;
+    s[i] = in ? sv : 0.0f;  // past the end: identity pair (1, 0)
+    slow |= in && !(sv >= s_min);
+    y[i] = 0.0f;
+  }
+  if constexpr (Cfg::EULER) {
+    // (the Euler input term dt B u has no cancellation at small steps)
+    chunk_states<IO, Cfg, ACC ? kArGen : kArFast>(Arow, lane, tile, s, u, y, carry);
+  } else {
+    if (!ACC && !__any_sync(0xffffffffu, slow))
+      chunk_states<IO, Cfg, kArFast>(Arow, lane, tile, s, u, y, carry);
+    else if (neg)
+      chunk_states<IO, Cfg, kArNeg>(Arow, lane, tile, s, u, y, carry);
+    else
+      chunk_states<IO, Cfg, kArGen>(Arow, lane, tile, s, u, y, carry);
   }
   float z[T];
   if constexpr (Cfg::GATE) load_run<IO, Cfg>(zrow, l, p.seqlen, z);
@@ -270,6 +302,18 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_chunk_kernel(const ScanPara
         small_a |= !(fabsf(__ldg(p.A + static_cast<int64_t>(d) * N + n)) >= kFastPathMinAbsA);
     acc = __any_sync(0xffffffffu, small_a);
   }
+  // every A of the channel negative: the accurate update needs no branch
+  bool neg = true;
+  if (active)
+    for (int n = lane; n < N; n += 32) neg = neg && __ldg(p.A + static_cast<int64_t>(d) * N + n) < 0.0f;
+  neg = __all_sync(0xffffffffu, neg);
+  // smallest step size (log2 units) the fast update takes for this channel
+  float s_min = 0.0f;
+  if (sizeof(IO) == 2 && !acc && active) {
+    float amin = fabsf(__ldg(p.A + static_cast<int64_t>(d) * N));
+    for (int n = 1; n < N; ++n) amin = fminf(amin, fabsf(__ldg(p.A + static_cast<int64_t>(d) * N + n)));
+    s_min = kFastPathMinQ / amin;
+  }
   if (active && lane < N) carry[lane] = p.h0 ? __ldg(p.h0 + row * N + lane) : 0.0f;
 
   const int nch = (p.seqlen + LCH - 1) / LCH;
@@ -286,9 +330,9 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_chunk_kernel(const ScanPara
     }
     if (active) {
       if (acc)
-        chunk_channel<IO, Cfg, true>(p, b, d, lane, k, cur, carry);
+        chunk_channel<IO, Cfg, true>(p, b, d, lane, k, cur, carry, s_min, neg);
       else
-        chunk_channel<IO, Cfg, false>(p, b, d, lane, k, cur, carry);
+        chunk_channel<IO, Cfg, false>(p, b, d, lane, k, cur, carry, s_min, neg);
     }
   }
   if (active && p.h_last && lane < N) p.h_last[row * N + lane] = carry[lane];

@@ -174,16 +174,82 @@ __device__ __forceinline__ float exp2m1_accurate(float q, float a /* = ex2(q) */
   return (fabsf(q) < kExpm1SeriesMaxQ) ? p : (a - 1.0f);
 }
 
-// softplus in log2 units: returns log2(1 + 2^x2) (= softplus(x) * log2 e for x2 = x log2 e)
+// |A| below this (or A == 0) sends a bf16 channel group to the accurate path: the fast
+// path forms (Abar - 1) w as Abar (h + w) - w, whose absolute error grows like
+// 2^-22 |B u / A|.
+constexpr float kFastPathMinAbsA = 0.125f;
+// A block of positions with a state update |q| = |dt A| log2(e) below this takes the
+// accurate update even on the fast path: Abar (h + w) - w with Abar = ex2(q) carries an
+// error of about 2^-22 |h + w| per step, which matters once it is not small against the
+// exact increment (Abar - 1)(h + w) ~ q ln2 |h + w| -- a state built only from tiny steps
+// (dt -> 0, the "keep the state" regime of the selection mechanism) would be lost to it.
+// At 2^-15 the fast update's error stays below 2^-6.5 of each increment.
+constexpr float kFastPathMinQ = 3.0517578125e-05f;  // 2^-15
+
+// Arithmetic of a state update: the fast form Abar (h + w) - w (bf16 io), the accurate
+// form for a channel whose A are all negative (2^q - 1 from exp2m1_neg, no branch), and
+// the general accurate form (expm1 series near zero, the dt limit at A == 0, any sign).
+constexpr int kArFast = 0, kArNeg = 1, kArGen = 2;
+
+// softplus in log2 units: returns log2(1 + 2^x2) (= softplus(x) * log2 e for x2 = x log2 e).
+// With t = 2^x2: the hardware lg2 of 1 + t while that sum keeps enough of t's bits
+// (x2 >= -12: rounding 1 + t costs at most 2^-24 / t = 2^-12 relative); below, the
+// series' leading term t log2(e) (log2(1 + t) = log2(e) (t - t^2/2 + ...), so its
+// relative error is below t / 2 <= 2^-13) -- a vanishing step stays positive instead
+// of rounding 1 + t to 1 (for x2 < -24 that would make dt exactly 0).  x itself beyond
+// x2 = 20 (the rest is below 2^-20 relative).
 __device__ __forceinline__ float softplus_log2_fast(float x2) {
-  const float s = lg2(1.0f + ex2(x2));
-  return (x2 > 20.0f) ? x2 : s;
+  const float t = ex2(x2);
+  const float big = lg2(1.0f + t);
+  return (x2 > 20.0f) ? x2 : ((x2 < -12.0f) ? t * kLog2e : big);
 }
-// accurate variant for the fp32 path (library log1pf / expf)
-__device__ __forceinline__ float softplus_log2_accurate(float x2) {
+// to about 1 ulp from the library log1pf / expf, for memory-bound kernels (decode),
+// where the arithmetic costs nothing
+__device__ __forceinline__ float softplus_log2_precise(float x2) {
   const float x = x2 * kLn2;
   const float sp = (x > 15.0f) ? x : log1pf(expf(x));
   return sp * kLog2e;
+}
+
+// accurate variant (fp32 io; about 3e-6 relative): max(x2, 0) + log2(1 + t) with
+// t = 2^-|x2| in (0, 1]; log2(1 + t) from the hardware lg2 for t >= 1/16 (its absolute
+// error, about 2^-22, is then below 3e-6 of the result) and below that from the series
+// log2(e) (t - t^2/2 + t^3/3 - t^4/4) (truncation under t^4 / 5 < 3.1e-6 relative)
+__device__ __forceinline__ float softplus_log2_accurate(float x2) {
+  const float t = ex2(-fabsf(x2));
+  const float ser = t * kLog2e * fmaf(fmaf(fmaf(-0.25f, t, 1.0f / 3.0f), t, -0.5f), t, 1.0f);
+  const float l = (t < 0.0625f) ? ser : lg2(1.0f + t);
+  return fmaxf(x2, 0.0f) + l;
+}
+
+// 2^q - 1 for q <= 0 without cancellation and without a branch.  Two estimates, both
+// never below the true value: the degree-4 Taylor series of e^x - 1 (x = q ln 2), whose
+// remainder e^xi x^5 / 120 is negative for x < 0 (accurate near zero, too large far
+// from it), and the hardware 2^q minus 1 raised by 2^-22, more than that ex2's error
+// (accurate away from zero).  The smaller one is the accurate one: within about 4e-8
+// relative for |q| <= 1/8 and 2^-21 absolute beyond.
+__device__ __forceinline__ float exp2m1_neg(float q, float a /* = ex2(q) */) {
+  // coefficients ln2^k / k!, k = 1..4
+  const float c1 = 0.69314718055994531f, c2 = 0.24022650695910071f,
+              c3 = 0.05550410866482158f, c4 = 0.00961812910762848f;
+  float p = fmaf(c4, q, c3);
+  p = fmaf(p, q, c2);
+  p = fmaf(p, q, c1);
+  return fminf(p * q, a - 0.99999976158142089844f /* 1 - 2^-22 */);
+}
+// 1 - 2^q for two values q = -nq <= 0 (packed f32x2 arithmetic), from nq = -q and
+// a = 2^q: the same two estimates with signs flipped, so the larger is the accurate one
+__device__ __forceinline__ f2 one_minus_exp2_neg2(f2 nq, f2 a) {
+  const f2 c1 = mk2(0.69314718055994531f, 0.69314718055994531f);
+  const f2 c2 = mk2(-0.24022650695910071f, -0.24022650695910071f);
+  const f2 c3 = mk2(0.05550410866482158f, 0.05550410866482158f);
+  const f2 c4 = mk2(-0.00961812910762848f, -0.00961812910762848f);
+  f2 p = fma2(c4, nq, c3);  // the series of e^x - 1 at x = -nq ln 2, in powers of nq
+  p = fma2(p, nq, c2);
+  p = fma2(p, nq, c1);
+  p = mul2(p, nq);
+  const f2 d = sub2(mk2(0.99999976158142089844f, 0.99999976158142089844f), a);
+  return mk2(fmaxf(p.x, d.x), fmaxf(p.y, d.y));
 }
 
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -197,7 +263,11 @@ __device__ __forceinline__ float tanh_hw(float x) {
 __device__ __forceinline__ float silu_fast(float z) {
   return z * fmaf(0.5f, tanh_hw(0.5f * z), 0.5f);
 }
-__device__ __forceinline__ float silu_accurate(float z) { return z / (1.0f + expf(-z)); }
+// z * sigmoid(z) to about 5e-7 relative: hardware ex2 and reciprocal (for z < -88 the
+// exponential overflows to inf and the result is -0, the limit)
+__device__ __forceinline__ float silu_accurate(float z) {
+  return z * rcp(1.0f + ex2(-z * kLog2e));
+}
 
 // ---------------------------------------------------------------------------
 // mbarrier (shared::cta) with bounded waits

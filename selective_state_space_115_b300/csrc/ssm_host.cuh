@@ -36,6 +36,7 @@ constexpr size_t kWorkspaceBytes = 256;
 constexpr int64_t kChannelKernelMinChannels = 8192;
 
 inline thread_local std::string g_last_cuda_error;
+inline thread_local std::string g_last_plan;
 
 inline ssm_status cuda_fail(cudaError_t e, const char* what) {
   g_last_cuda_error = std::string(what) + ": " + cudaGetErrorString(e);
@@ -242,7 +243,8 @@ inline size_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, co
 // [nblk][batch * dim][N]; the per-CTA dB / dC partials [tiles][batch][2][N][L];
 // the per-(segment, channel) dA [nseg][batch * dim][N], dD and bias gradient
 // [nseg][batch * dim][2]; with segments, their end states and own adjoints
-// [nseg][batch * dim][N] each and step-size sums [nseg][batch * dim]
+// [nseg][batch * dim][N] each and step-size sums [nseg][batch * dim]; one byte per
+// CTA [nseg][batch][tiles] saying whether it takes the fast coefficients
 // ---------------------------------------------------------------------------
 constexpr int kBwdThreads = 128;
 constexpr int kBwdChannels = kBwdThreads / ssm::kBwdLpc;
@@ -256,7 +258,7 @@ struct BwdLayout {
   int64_t nblk = 0, tiles = 0;
   int nseg = 1, seg_len = 0;
   size_t off_ckpt = 0, off_bc = 0, off_a = 0, off_dd = 0, off_E = 0, off_R = 0, off_sum = 0,
-         total = 0;
+         off_flags = 0, total = 0;
 };
 
 // Segments for the gradient: when the (batch row, channel tile) CTAs cannot fill
@@ -293,11 +295,13 @@ inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t 
   if (w.nseg > 1) {
     w.off_R = w.off_E + round_up(ns * rows * dstate * 4, 256);
     w.off_sum = w.off_R + round_up(ns * rows * dstate * 4, 256);
-    w.total = w.off_sum + round_up(ns * rows * 4, 256);
+    w.off_flags = w.off_sum + round_up(ns * rows * 4, 256);
   } else {
     w.off_R = w.off_sum = w.off_E;
-    w.total = w.off_E;
+    w.off_flags = w.off_E;
   }
+  // one byte per CTA: fast or accurate coefficients
+  w.total = w.off_flags + round_up(ns * static_cast<size_t>(batch) * w.tiles, 256);
   return w;
 }
 

@@ -108,7 +108,7 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
     }
   }
   const float x2 = fmaf(dv, kLog2e, p.bias ? __ldg(p.bias + d) * kLog2e : 0.0f);
-  const float s = p.softplus ? softplus_log2_accurate(x2) : x2;  // dt * log2(e)
+  const float s = p.softplus ? softplus_log2_precise(x2) : x2;  // dt * log2(e)
 
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
