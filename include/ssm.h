@@ -26,7 +26,9 @@
  *
  * Conventions shared by every entry point:
  *  - All tensor pointers are DEVICE pointers, owned by the caller.  The library
- *    allocates no device memory and keeps no per-call state.
+ *    allocates no device memory and keeps no per-call state -- except
+ *    ssm_scan_fwd_noalloc, whose statically reserved scratch keeps the last call's
+ *    contents (see its comment).
  *  - Tensors are contiguous, row-major, last index fastest:
  *      u, delta, z, y : [batch, dim, seqlen]      (scan)  /  [batch, dim]  (update)
  *      B, C           : [batch, dstate, seqlen]   (scan)  /  [batch, dstate] (update)
@@ -191,13 +193,15 @@ SSM_API ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, i
  * GPU that loads the library keeps until the process exits.  The caller still
  * passes all inputs and outputs, exactly as for ssm_scan_fwd (kernel chosen as
  * by SSM_ALGO_AUTO).
- *  - The first call on a device looks up that device's scratch address
- *    (cudaGetSymbolAddress) with the caller's current device, which must be the
- *    device of the tensors and of `stream`; make that first call before any
- *    stream capture.
+ *  - The first call on a device (and the first after that device's context was
+ *    reset or created again) looks up the scratch address (cudaGetSymbolAddress)
+ *    with the caller's current device, which must be the device of the tensors
+ *    and of `stream`; make that first call before any stream capture.
  *  - The kernel is chosen as by SSM_ALGO_AUTO among the plans whose scratch fits
- *    the reserved 4096 bytes (the segmented long-sequence plan does not, so long
- *    sequences over few channels take the lanes-over-positions kernel here).
+ *    the reserved 4096 bytes: the channel kernels always fit; the segmented
+ *    long-sequence plan is taken when its segment states fit (e.g. one channel of
+ *    8192+ positions), and otherwise the lanes-over-positions kernel takes its
+ *    place.  No size is rejected for want of scratch.
  *  - Every call shares the one array per device and it keeps the last call's
  *    contents; its status words are cleared on `stream` before each kernel.
  *    Calls that overlap on the GPU (different streams, no ordering) race on it.
@@ -387,6 +391,13 @@ SSM_API const char* ssm_status_string(ssm_status status);
 /* Detail of the last CUDA error (or rejected no-alloc request) seen by a call on
  * this host thread ("" if none). */
 SSM_API const char* ssm_last_cuda_error(void);
+
+/* Which kernels the last successful scan-forward call on this host thread launched
+ * (ssm_scan_fwd, _algo, _ex, _noalloc), with the split the library chose, e.g.
+ * "scan_channel_mixed_kernel: 2 one-lane CTAs per SM + 96 four-lane CTAs" ("" before
+ * the first call).  A diagnostic for benchmarks and profiles; the text is not a
+ * stable interface.  The pages have no counterpart. */
+SSM_API const char* ssm_last_plan(void);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 SSM_API int ssm_version(void);

@@ -51,7 +51,7 @@ EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "
             "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex", "ssm_selftest_wait",
             "ssm_scan_fwd_host_workspace_size", "ssm_scan_fwd_host",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
-            "ssm_status_string", "ssm_last_cuda_error", "ssm_version")
+            "ssm_status_string", "ssm_last_cuda_error", "ssm_last_plan", "ssm_version")
 
 
 class SsmError(RuntimeError):
@@ -137,6 +137,8 @@ def library(path: Optional[str] = None):
         lib.ssm_status_string.argtypes = [_int]
         lib.ssm_last_cuda_error.restype = ctypes.c_char_p
         lib.ssm_last_cuda_error.argtypes = []
+        lib.ssm_last_plan.restype = ctypes.c_char_p
+        lib.ssm_last_plan.argtypes = []
         lib.ssm_version.restype = _int
         lib.ssm_version.argtypes = []
         if path is None:
@@ -146,6 +148,11 @@ def library(path: Optional[str] = None):
 
 def status_string(status: int) -> str:
     return library().ssm_status_string(int(status)).decode()
+
+
+def last_plan() -> str:
+    """The kernels the last scan-forward call on this thread launched (ssm_last_plan)."""
+    return library().ssm_last_plan().decode()
 
 
 def _check(status: int, what: str):

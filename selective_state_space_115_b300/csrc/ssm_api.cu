@@ -2,7 +2,8 @@
 //
 // Host side: argument validation (nothing is enqueued when it fails), choice of
 // kernel family, TMA descriptor encoding, launches on the caller's stream.
-// The library allocates no device memory and keeps no per-call state.
+// The library allocates no device memory and keeps no per-call state (except the
+// statically reserved scratch of ssm_scan_fwd_noalloc, below).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,12 +55,50 @@ ssm_status dispatch_update(const UpdateParams& p, int64_t dstate, bool vec, bool
 // ---------------------------------------------------------------------------
 // Device scratch of fixed size that every GPU loading this library holds until
 // the process exits.  Host code must not pass the symbol itself to a kernel (on
-// the host it only names a stand-in object); the device address is looked up
-// once per device with cudaGetSymbolAddress.
+// the host it only names a stand-in object); the device address is looked up with
+// cudaGetSymbolAddress for the current device's context.  The address belongs to
+// that context: after cudaDeviceReset (or the primary context being released and
+// created again) the module loads anew and the array may move, so the cached
+// address is keyed by the context's unique id and looked up again when it changes.
 constexpr size_t kNoAllocScratchBytes = 4096;
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+struct NoAllocSlot {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
+NoAllocSlot g_noalloc[kNoAllocMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// unique id of the calling thread's current context (0 when it cannot be read: the
+// address is then looked up on every call)
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = []() -> CtxGetCurrentFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  static CtxGetIdFn get_id = []() -> CtxGetIdFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetIdFn>(f);
+  }();
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 }  // namespace
 
@@ -67,7 +106,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-// Device address of the static scratch on the current device (set-up on first use).
+// Device address of the static scratch in the current device's context: looked up
+// on the first call in a context (the runtime then makes the device's primary
+// context current and loads the module if it has not yet) and kept for later calls
+// in the same context.
 ssm_status noalloc_scratch(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -76,15 +118,46 @@ ssm_status noalloc_scratch(void** out) {
     g_last_cuda_error = "ssm_scan_fwd_noalloc: device ordinal beyond the supported range";
     return SSM_ERR_UNSUPPORTED;
   }
+  // nothing cached yet: look up first (that call also makes the primary context
+  // current), then record the context it belongs to
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocSlot& slot = g_noalloc[dev];
+  unsigned long long id = slot.ptr ? current_context_id() : 0;
+  if (!slot.ptr || id == 0 || id != slot.ctx_id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
-    g_noalloc_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = current_context_id();
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return SSM_OK;
+}
+
+// Text of the plan a scan-forward call launched (for ssm_last_plan).
+std::string describe_plan(const ScanCall& c, ssm_algo algo, const SegPlan& seg,
+                          const MixPlan& mix) {
+  const std::string io = c.bf16 ? "bf16" : "fp32";
+  const std::string n = std::to_string(c.dstate);
+  switch (algo) {
+    case SSM_ALGO_CHANNEL_MIXED:
+      return "scan_channel_mixed_kernel<" + io + ", N" + n + ">: " + std::to_string(mix.k) +
+             " one-lane-per-channel CTAs of 128 channels per SM (" +
+             std::to_string(mix.n_tiles) + ") + " + std::to_string(mix.n_quarters) +
+             " four-lane CTAs of 32 channels";
+    case SSM_ALGO_SEGMENTED:
+      return "scan_channel_kernel<" + io + ", N" + n + "> segmented: " +
+             std::to_string(seg.nseg) + " segments of " + std::to_string(seg.seg_len) +
+             " positions, pass 1 (segment end states) + pass 2 (outputs)";
+    case SSM_ALGO_CHANNEL:
+      return "scan_channel_kernel<" + io + ", N" + n + ">: " +
+             std::to_string(choose_lpc(c.batch, c.dim, c.dstate)) + " lane(s) per channel";
+    case SSM_ALGO_CHANNEL_L1: return "scan_channel_kernel<" + io + ", N" + n + ">: 1 lane per channel";
+    case SSM_ALGO_CHANNEL_L2: return "scan_channel_kernel<" + io + ", N" + n + ">: 2 lanes per channel";
+    case SSM_ALGO_CHANNEL_L4: return "scan_channel_kernel<" + io + ", N" + n + ">: 4 lanes per channel";
+    default:
+      return "scan_chunk_kernel<" + io + ", N" + n + ">: one warp per channel, lanes over positions";
+  }
 }
 
 }  // namespace
@@ -206,8 +279,10 @@ ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(ssm::DeviceStatus), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace status)");
-  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s, seg, mix)
-                : dispatch_scan<float>(c, algo, workspace, s, seg, mix);
+  const ssm_status rs = c.bf16 ? dispatch_scan<uint16_t>(c, algo, workspace, s, seg, mix)
+                               : dispatch_scan<float>(c, algo, workspace, s, seg, mix);
+  if (rs == SSM_OK) g_last_plan = describe_plan(c, algo, seg, mix);
+  return rs;
 }
 
 ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
@@ -236,15 +311,11 @@ ssm_status ssm_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int6
                                 const float* delta_bias, int delta_softplus, const float* A,
                                 const void* B, const void* C, const float* D, const void* z,
                                 const float* h0, float* h_last, void* y, ssm_stream_t stream) {
-  // every plan needs the status words; the segmented long-sequence plan needs more
-  // and is then skipped by AUTO (it picks the kernels whose scratch fits)
-  const size_t need = kWorkspaceBytes;
-  if (need > kNoAllocScratchBytes) {
-    g_last_cuda_error = "ssm_scan_fwd_noalloc: these sizes need " + std::to_string(need) +
-                        " bytes of scratch, more than the " +
-                        std::to_string(kNoAllocScratchBytes) + " bytes reserved statically";
-    return SSM_ERR_UNSUPPORTED;
-  }
+  // AUTO picks among the plans whose scratch fits the reserved bytes: the status
+  // words and the mixed split's counters always do; the segmented long-sequence plan
+  // when its segment states fit, else the lanes-over-positions kernel takes its place
+  static_assert(kStatusBytes + kMixCounterBytes <= kNoAllocScratchBytes,
+                "the channel kernels' scratch fits the reserved array");
   void* scratch = nullptr;
   const ssm_status st = noalloc_scratch(&scratch);
   if (st != SSM_OK) return st;
@@ -391,6 +462,7 @@ ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
   p.seg_E = reinterpret_cast<float*>(ws + w.off_E);
   p.seg_R = reinterpret_cast<float*>(ws + w.off_R);
   p.seg_sum = reinterpret_cast<float*>(ws + w.off_sum);
+  p.cta_fast = ws + w.off_flags;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool euler = disc == SSM_DISC_EULER;
   float* dD_out = D ? dD : nullptr;
@@ -484,6 +556,8 @@ const char* ssm_status_string(ssm_status status) {
 }
 
 const char* ssm_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+const char* ssm_last_plan(void) { return g_last_plan.c_str(); }
 
 int ssm_version(void) { return kVersion; }
 

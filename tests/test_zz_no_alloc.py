@@ -35,6 +35,9 @@ def _noalloc(lib, x, io, y, stream):
 @pytest.mark.parametrize("name,io,batch,dim,seqlen", [
     ("channel-kernel bf16", W.BF16, 2, 5120, 512),   # 10240 channels: TMA channel kernel
     ("chunk-kernel fp32", W.F32, 2, 96, 700),        # few channels, ragged L: chunk kernel
+    # one channel of 8192 positions: the segmented two-pass plan, whose segment states
+    # (2.5 KB) fit the static scratch
+    ("segmented bf16", W.BF16, 1, 1, 8192),
 ])
 def test_noalloc_matches_workspace_entry_point(name, io, batch, dim, seqlen):
     import torch
