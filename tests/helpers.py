@@ -8,6 +8,9 @@ from selective_state_space_115_b300 import workloads as W
 # Tolerances on the error metric below (max over elements):
 #   fp32 io: 1e-4;  bf16 io with fp32 state: 2e-2.
 TOL = {W.F32: 1e-4, W.BF16: 2e-2}
+# The final state h_last is fp32 and never rounded to bf16, so with bf16 io the tests
+# hold it to 1e-3 (stricter than the 2e-2 that covers y's bf16 rounding); fp32 io: 1e-4.
+H_TOL = {W.F32: 1e-4, W.BF16: 1e-3}
 
 
 def rel_err(y: np.ndarray, ref: np.ndarray) -> float:
@@ -48,15 +51,3 @@ def from_torch(t) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return W.bf16_bits_to_f32(t.view(torch.int16).numpy().view(np.uint16)).astype(np.float64)
     return t.numpy().astype(np.float64)
-
-
-def sample_rows(batch: int, dim: int, k: int, seed: int = 0) -> np.ndarray:
-    """k distinct row ids (b*dim + d), always including the first and last rows and
-    the last row of every batch tile boundary region."""
-    rng = np.random.default_rng(seed)
-    total = batch * dim
-    fixed = {0, total - 1, dim - 1, min(total - 1, dim)}
-    rest = rng.choice(total, size=min(total, k), replace=False)
-    rows = sorted(set(int(r) for r in rest) | fixed)
-    return np.array(rows[:max(k, len(fixed))] if len(rows) > k + len(fixed) else rows,
-                    dtype=np.int64)

@@ -232,14 +232,14 @@ def _bwd_bytes(batch, dim, n, seqlen, segments=0):
              + rnd(nseg * rows * n * 4) + rnd(nseg * rows * 2 * 4))
     if nseg > 1:
         total += 2 * rnd(nseg * rows * n * 4) + rnd(nseg * rows * 4)
-    return total
+    return total + rnd(nseg * batch * tiles)  # one fast/series flag byte per CTA
 
 
 def test_bwd_workspace_size():
     """Checkpoints every 8 positions, one dB/dC partial per 32-channel CTA, the
-    per-(segment, channel) dA / dD / bias sums, and with a split each segment's end
-    state, own adjoint and step-size sum (without a device the library assumes
-    148 SMs)."""
+    per-(segment, channel) dA / dD / bias sums, with a split each segment's end
+    state, own adjoint and step-size sum, and one flag byte per CTA (fast or series
+    coefficients); without a device the library assumes 148 SMs."""
     lib = binding.library()
     ws, wsx = lib.ssm_scan_bwd_workspace_size, lib.ssm_scan_bwd_ex_workspace_size
     for shape in ((8, 5120, 16, 2048), (1, 1536, 16, 131072), (2, 37, 8, 69), (1, 1, 4, 1),

@@ -50,3 +50,26 @@ def test_source_hash_covers_each_profiled_kernel():
     for k in bench.KERNEL_SOURCES:
         h = bench.source_sha(k)
         assert len(h) == 16 and int(h, 16) >= 0
+
+
+def test_roofline_binding_term_per_workload():
+    """The slowest of bytes / HBM, exps / ex2 peak and 2 FMA per update / fp32 peak:
+    the exps bind the 2.8B-like and long scans, the bytes the fp32 130M-like scan
+    (148 SMs, 2032 MHz, 6484.9 GB/s)."""
+    r = {n: bench.scan_roofline(W.SCAN_CONFIGS[n], 1.0, 148, 2032.0, 6484.9)
+         for n in ("2p8b", "long", "130m")}
+    assert r["2p8b"]["bound"] == "alu" and r["long"]["bound"] == "alu"
+    assert r["130m"]["bound"] == "hbm"
+    assert abs(r["2p8b"]["roof_us"]["ex2"] - 139.5) < 0.5
+    assert abs(r["130m"]["roof_us"]["hbm"] - 15.6) < 0.1
+    # at 1 ms per scan the 2.8B-like fraction is 139.5 us / 1 ms
+    assert abs(r["2p8b"]["frac"] - r["2p8b"]["roof_us"]["ex2"] / 1000.0) < 1e-9
+
+
+def test_link_floor():
+    """End-to-end floor: the larger of the copy-in and copy-out times at the measured
+    pinned-copy peaks."""
+    link = {"h2d_gbs": 50.0, "d2h_gbs": 40.0, "bytes": 1}
+    f = bench.link_fraction(link, h2d=500_000_000, d2h=100_000_000, e2e_s=0.02)
+    assert abs(f["floor_ms"] - 10.0) < 1e-9 and abs(f["frac"] - 0.5) < 1e-9
+    assert bench.link_fraction(None, 1, 1, 1.0) is None

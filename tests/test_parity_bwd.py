@@ -242,3 +242,72 @@ def test_bwd_2p8b_size():
     ref0 = oracle_bwd(row0, gr0, io)
     check({k: got[k][:1] for k in ("dB", "dC", "du")}, ref0, io, what="2p8b batch row 0",
           keys=("dB", "dC", "du"))
+
+
+@pytest.mark.parametrize("segments", [0, 4])
+@pytest.mark.parametrize("io", [W.F32, W.BF16])
+def test_bwd_large_and_tiny_dt(io, segments):
+    """softplus saturation (raw delta up to +60) and vanishing dt (raw down to -60), no D
+    skip, zero initial state; unsplit and in four segments."""
+    cfg = W.ScanConfig("t", 2, 40, 16, 256, io, gate=True, dt_bias=False, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=51)
+    x["D"] = None
+    rng = np.random.default_rng(8)
+    x["delta"] = W.encode(rng.uniform(-60, 60, size=x["delta"].shape).astype(np.float32), io)
+    gr = W.make_scan_grads(cfg, seed=51)
+    check(gpu_bwd(x, gr, io, segments=segments), oracle_bwd(x, gr, io), io,
+          what=f"large/tiny dt {io} seg {segments}")
+
+
+@pytest.mark.parametrize("segments", [0, 4])
+@pytest.mark.parametrize("io", [W.F32, W.BF16])
+def test_bwd_vanishing_dt(io, segments):
+    """Every step tiny (raw delta in [-60, -20]), no D skip, zero initial state: every
+    gradient is built from tiny steps only, so the scale-free error metric sees any
+    absolute error of the coefficients (bf16: these CTAs take the series coefficients)."""
+    cfg = W.ScanConfig("t", 2, 40, 16, 256, io, gate=True, dt_bias=False, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=52)
+    x["D"] = None
+    rng = np.random.default_rng(9)
+    x["delta"] = W.encode(rng.uniform(-60, -20, size=x["delta"].shape).astype(np.float32), io)
+    gr = W.make_scan_grads(cfg, seed=52)
+    check(gpu_bwd(x, gr, io, segments=segments), oracle_bwd(x, gr, io), io,
+          what=f"vanishing dt {io} seg {segments}")
+
+
+def test_bwd_mixed_fast_and_series_ctas():
+    """bf16: one 32-channel CTA of each batch row holds a channel of vanishing steps (it
+    takes the series coefficients, launched first) next to CTAs on the fast coefficients
+    (launched to overlap it); every gradient, including the dB / dC sums over both kinds
+    of CTA, against the oracle."""
+    io = W.BF16
+    cfg = W.ScanConfig("t", 2, 96, 16, 512, io, gate=True, dt_bias=True, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=53, with_h0=True)
+    dl = W.to_f64(x["delta"], io).astype(np.float32)
+    dl[:, 40, :] = -45.0  # channel 40 (second CTA): dt ~ 3e-20 after the bias
+    x["delta"] = W.encode(dl, io)
+    gr = W.make_scan_grads(cfg, seed=53)
+    check(gpu_bwd(x, gr, io), oracle_bwd(x, gr, io), io, what="mixed CTAs")
+
+
+def test_bwd_steps_near_fast_threshold():
+    """bf16: every step with |dt A| log2(e) from 0.5x to 4x of 2^-16, the lower limit of
+    the fast coefficients per CTA, no D skip, zero initial state: CTAs with a step
+    below it take the series, the others the fast coefficients."""
+    io = W.BF16
+    cfg = W.ScanConfig("t", 2, 64, 16, 512, io, gate=False, dt_bias=False, d_skip="normal",
+                       description="")
+    x = W.make_scan_inputs(cfg, seed=54)
+    x["D"] = None
+    rng = np.random.default_rng(10)
+    q = 2.0 ** -16 * np.exp(rng.uniform(np.log(0.5), np.log(4.0), size=x["delta"].shape))
+    # the first CTA's 32 channels stay above the limit throughout (fast coefficients at
+    # steps just above it); the second CTA's reach below it (series)
+    q[:, :32, :] = np.maximum(q[:, :32, :], 1.05 * 2.0 ** -16)
+    dt = q / np.log2(np.e)
+    x["delta"] = W.encode(np.log(np.expm1(dt)).astype(np.float32), io)
+    gr = W.make_scan_grads(cfg, seed=54)
+    check(gpu_bwd(x, gr, io), oracle_bwd(x, gr, io), io, what="near-threshold steps")

@@ -9,6 +9,7 @@ from selective_state_space_115_b300 import workloads as W
 from tests.helpers import TOL, from_torch, rel_err, torch_f32, torch_io
 
 pytestmark = pytest.mark.gpu
+NTHREADS = os.cpu_count() or 1
 
 
 def S():
@@ -23,14 +24,11 @@ def gpu_step(h, st, static, io):
                             delta_bias=torch_f32(static["delta_bias"]))
 
 
-def oracle_step(h, st, static, io, rows=None):
+def oracle_step(h, st, static, io):
     f = lambda a: None if a is None else W.to_f64(a, io)  # noqa: E731
     u, dl, z, B, C = (f(st.get(k)) for k in ("u", "delta", "z", "B", "C"))
-    if rows is not None:
-        u, dl, B, C = u[rows], dl[rows], B[rows], C[rows]
-        z = None if z is None else z[rows]
     return oracle.state_update(h, u, dl, static["A"], B, C, D=static["D"], z=z,
-                               delta_bias=static["delta_bias"])
+                               delta_bias=static["delta_bias"], nthreads=NTHREADS)
 
 
 def test_decode_all_rows_first_steps():
@@ -53,27 +51,28 @@ def test_decode_all_rows_first_steps():
 
 
 @pytest.mark.slow
-def test_decode_1024_steps_sampled_rows():
-    """The full 1024-step loop on the full batch; the oracle follows sampled batch
-    rows b in {0, 127, 255} (all channels) through every step."""
+def test_decode_1024_steps_all_rows():
+    """The full 1024-step loop on the full batch (B256 D5120 N16, h in place); the oracle
+    follows every channel through every step, and y and h are compared over all
+    channels every 64 steps and at the last step."""
     import torch
     cfg = W.DECODE_CONFIGS["decode"]
     static = W.make_decode_static(cfg, seed=0)
-    rows = np.array([0, 127, 255])
     h = torch_f32(static["h"])
-    href = static["h"][rows].astype(np.float64)
-    worst = 0.0
+    href = static["h"].astype(np.float64)
+    worst_y = worst_h = 0.0
     for t in range(cfg.steps):
         st = W.make_decode_step(cfg, t, seed=0)
         y = gpu_step(h, st, static, cfg.io)
-        yref, href = oracle_step(href, st, static, cfg.io, rows=rows)
+        yref, href = oracle_step(href, st, static, cfg.io)
         if t % 64 == 63 or t == cfg.steps - 1:
             torch.cuda.synchronize()
-            worst = max(worst, rel_err(from_torch(y)[rows], yref))
-            assert rel_err(from_torch(h)[rows], href) <= 1e-4, t
+            ey, eh = rel_err(from_torch(y), yref), rel_err(from_torch(h), href)
+            worst_y, worst_h = max(worst_y, ey), max(worst_h, eh)
+            assert ey <= TOL[cfg.io], (t, ey)
+            assert eh <= 1e-4, (t, eh)
     torch.cuda.synchronize()
-    print(f"decode 1024 steps: worst sampled y err {worst:.3e}")
-    assert worst <= TOL[cfg.io]
+    print(f"decode 1024 steps, all channels: worst y err {worst_y:.3e}, h err {worst_h:.3e}")
 
 
 @pytest.mark.parametrize("io", [W.F32, W.BF16])
