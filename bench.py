@@ -40,10 +40,13 @@ CFG = W.SCAN_CONFIGS["2p8b"]
 FLUSH_L2 = False
 DEC = W.DECODE_CONFIGS["decode"]
 DECODE_STEPS = DEC.steps
-SM_COUNT = 148
+SM_COUNT = 148              # B300; the GPU arm reads the device's own count
 SM_MAX_MHZ = 2032.0
-EX2_PER_CLK_SM = 32          # measured on this machine's B300 (ex2.approx.ftz.f32 throughput)
+EX2_PER_CLK_SM = 32          # measured on B300: ex2.approx.ftz.f32 per clock per SM
+FP32_LANES_PER_CLK_SM = 128  # fp32 FMA lanes per clock per SM
 FALLBACK_HBM_GBS = 6400.0
+SUB_CONFIGS = ("130m", "long", "tiny")  # scan workloads reported beside the headline one
+L2_BYTES = 126 * 2**20
 
 
 def measured_peaks():
@@ -72,10 +75,37 @@ def decode_bytes(cfg) -> int:
         2 * s * cfg.batch * cfg.dstate + 4 * (cfg.dim * cfg.dstate + 2 * cfg.dim)
 
 
+def scan_roofline(cfg, ms: float, sms: int, sm_mhz: float, hbm_gbs: float) -> dict:
+    """The method's roofline for one scan: the slowest of the algorithmic bytes at the
+    HBM peak, the B*D*L*N exps at the ex2 peak and the 2 FMA per state update at the
+    fp32 peak; the fraction is taken against the binding term."""
+    nbytes, units = scan_bytes(cfg), cfg.updates
+    ex2_rate = EX2_PER_CLK_SM * sms * sm_mhz * 1e6
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    t_ex2 = units / ex2_rate
+    t_fp32 = 2 * units / (FP32_LANES_PER_CLK_SM * sms * sm_mhz * 1e6)
+    t = ms * 1e-3
+    if t_hbm >= max(t_ex2, t_fp32):
+        ach = nbytes / t / 1e9
+        r = {"bound": "hbm", "achieved": ach, "peak": hbm_gbs, "unit": "GB/s",
+             "frac": ach / hbm_gbs}
+    else:
+        ach, peak = units / t / 1e12, ex2_rate / 1e12
+        r = {"bound": "alu", "achieved": ach, "peak": peak, "unit": "Texp/s",
+             "frac": ach / peak,
+             "peak_note": f"{sms} SMs x {EX2_PER_CLK_SM} ex2/clk/SM (measured "
+                          f"ex2.approx.f32 throughput) x {sm_mhz:.0f} MHz max SM clock"}
+    r["roof_us"] = {"hbm": t_hbm * 1e6, "ex2": t_ex2 * 1e6, "fp32_2fma": t_fp32 * 1e6}
+    r["units_per_launch"] = units
+    r["bytes_per_launch"] = nbytes
+    return r
+
+
 # device sources each profiled kernel is compiled from
 KERNEL_SOURCES = {
     "scan_channel_2p8b": ("scan_channel.cuh", "ssm_device.cuh"),
     "scan_channel_long": ("scan_channel.cuh", "ssm_device.cuh"),
+    "scan_chunk_130m": ("scan_chunk.cuh", "scan_channel.cuh", "ssm_device.cuh"),
     "state_update_decode": ("state_update.cuh", "ssm_device.cuh"),
     "scan_bwd_2p8b": ("scan_bwd.cuh", "ssm_device.cuh"),
     "conv1d_2p8b": ("conv1d.cuh", "ssm_device.cuh"),
@@ -208,33 +238,70 @@ def barrier(world: int):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
-def oracle_sample_rate(target_core_seconds: float, cores: int, steps: int = 1):
-    """Time the oracle on a row sample of the bench workload; returns
-    (elements/s, rows, seconds, sample description)."""
-    import oracle
-    rows_total = CFG.batch * CFG.dim
-    x = W.make_scan_inputs(CFG, seed=0, batch=1, dim=min(CFG.dim, 4096))
-    f = lambda a: W.to_f64(a, CFG.io)  # noqa: E731
-    u, dl, z, B, C = f(x["u"]), f(x["delta"]), f(x["z"]), f(x["B"]), f(x["C"])
-    # calibrate on 8 rows, one thread
-    t = time.perf_counter()
-    oracle.scan_fwd(u[:, :8], dl[:, :8], x["A"][:8], B, C, D=x["D"][:8], z=z[:, :8],
-                    delta_bias=x["delta_bias"][:8], nthreads=1)
-    per_row = (time.perf_counter() - t) / 8
-    rows = int(max(cores, min(u.shape[1], rows_total, target_core_seconds / per_row)))
-    rows = max(1, min(rows, u.shape[1]))
-    times = []
-    for _ in range(steps):
+class OracleSample:
+    """The oracle on the first `dim` channels of batch row 0 of a workload (inputs
+    widened to fp64 once); `run(rows, nthreads)` scans the first `rows` of them and
+    returns the seconds it took."""
+
+    def __init__(self, cfg, max_rows: int = 4096):
+        import oracle
+        self.oracle, self.cfg = oracle, cfg
+        self.max_rows = min(cfg.dim, max_rows)
+        x = W.make_scan_inputs(cfg, seed=0, batch=1, dim=self.max_rows)
+        f = lambda a: None if a is None else W.to_f64(a, cfg.io)  # noqa: E731
+        self.u, self.dl, self.z = f(x["u"]), f(x["delta"]), f(x.get("z"))
+        self.B, self.C = f(x["B"]), f(x["C"])
+        self.A, self.D, self.bias = x["A"], x.get("D"), x.get("delta_bias")
+
+    def run(self, rows: int, nthreads: int) -> float:
+        r = slice(0, rows)
+        opt = lambda a: None if a is None else a[r]  # noqa: E731
         t = time.perf_counter()
-        oracle.scan_fwd(u[:, :rows], dl[:, :rows], x["A"][:rows], B, C, D=x["D"][:rows],
-                        z=z[:, :rows], delta_bias=x["delta_bias"][:rows], nthreads=cores)
-        times.append(time.perf_counter() - t)
-    total = sum(times)
-    elems = rows * CFG.seqlen * steps
-    desc = (f"{rows} of {rows_total} (b,d) rows of the bench workload (batch row 0), full "
-            f"seqlen {CFG.seqlen}, dstate {CFG.dstate}, bf16 inputs widened to fp64, fp64 "
-            f"sequential loops, OpenMP over rows")
-    return elems / total, rows, total, desc
+        self.oracle.scan_fwd(self.u[:, r], self.dl[:, r], self.A[r], self.B, self.C,
+                             D=opt(self.D), z=None if self.z is None else self.z[:, r],
+                             delta_bias=opt(self.bias), nthreads=nthreads)
+        return time.perf_counter() - t
+
+    def per_row_seconds(self) -> float:
+        k = min(self.max_rows, 4)
+        self.run(k, 1)  # warm: library load, page-in
+        return self.run(k, 1) / k
+
+    def describe(self, rows: int, threads: int) -> str:
+        cfg = self.cfg
+        return (f"{rows} of {cfg.batch * cfg.dim} (b,d) rows of the workload (batch row 0), "
+                f"full seqlen {cfg.seqlen}, dstate {cfg.dstate}, inputs widened to fp64, fp64 "
+                f"sequential loops, {'OpenMP over rows, ' + str(threads) + ' threads' if threads > 1 else 'one thread'}")
+
+
+def cpu_baseline(cfg, cores: int, target_s: float) -> dict:
+    """The oracle as it stands, warmed up, timed on a bounded row sample of `cfg`: all
+    host cores (about 2/3 of `target_s`) and one core (the rest).  elements/s =
+    rows x seqlen / seconds."""
+    smp = OracleSample(cfg)
+    per_row = smp.per_row_seconds()
+    L = cfg.seqlen
+    rows1 = int(max(1, min(smp.max_rows, target_s / 3 / per_row)))
+    t1 = smp.run(rows1, 1)
+    rows = int(max(min(cores, smp.max_rows), min(smp.max_rows, target_s * 2 / 3 * cores / per_row)))
+    smp.run(min(rows, 2 * cores), cores)  # warm the thread pool
+    tn = smp.run(rows, cores)
+    return {"value": rows * L / tn, "unit": "elements/s", "cores": cores, "kind": "oracle",
+            "sample": smp.describe(rows, cores),
+            "single_core": {"value": rows1 * L / t1, "unit": "elements/s", "cores": 1,
+                            "sample": smp.describe(rows1, 1)}}
+
+
+def oracle_sample_rate(target_core_seconds: float, cores: int, steps: int = 1):
+    """The reference arm's steps: the oracle on a row sample of the bench workload sized
+    to `target_core_seconds` of one core's work, on all cores; returns (elements/s, rows,
+    seconds, sample description)."""
+    smp = OracleSample(CFG)
+    per_row = smp.per_row_seconds()
+    rows = int(max(min(cores, smp.max_rows), min(smp.max_rows, target_core_seconds / per_row)))
+    smp.run(min(rows, 2 * cores), cores)  # warm the thread pool
+    total = sum(smp.run(rows, cores) for _ in range(steps))
+    return rows * CFG.seqlen * steps / total, rows, total, smp.describe(rows, cores)
 
 
 def run_reference(args):
@@ -364,15 +431,20 @@ def run_gpu(args):
     assert S.read_device_status() == 0, "device-side wait timed out in the timed region"
     ms_step = max_over_ranks(dev_ms / args.steps, world, dev)
 
+    plan = S.last_plan()
     elems = CFG.elements
     value = world * elems / (ms_step * 1e-3)
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    sm_mhz = float(peaks.get("sm_max_mhz", SM_MAX_MHZ))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     bytes_step = scan_bytes(CFG)
-    ex2_peak = EX2_PER_CLK_SM * SM_COUNT * SM_MAX_MHZ * 1e6 / 1e12   # Texp/s
-    achieved_exp = CFG.updates / (dev_ms / args.steps * 1e-3) / 1e12
-    traffic = profiled_traffic({"2p8b": "scan_channel_2p8b", "long": "scan_channel_long"}.get(
-        CFG.name, ""))
+    ex2_peak = EX2_PER_CLK_SM * sms * sm_mhz * 1e6 / 1e12   # Texp/s
+    roof = scan_roofline(CFG, dev_ms / args.steps, sms, sm_mhz, hbm_peak)
+    roof["traffic"] = profiled_traffic({"2p8b": "scan_channel_2p8b",
+                                        "long": "scan_channel_long",
+                                        "130m": "scan_chunk_130m"}.get(CFG.name, ""))
+    roof["kernel"] = plan
 
     # ---- end to end through the C ABI's host-buffer call (ssm_scan_fwd_host): every
     # step copies its inputs in from pinned host memory and its output back; the
@@ -399,6 +471,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, dev)
     e2e_value = world * elems / e2e_s
+    link = link_peak(dev) if rank == 0 else None
 
     # ---- decode state update (rank 0's measurement)
     decode = run_decode(dev, S) if (rank == 0 and not args.no_decode) else None
@@ -423,13 +496,20 @@ def run_gpu(args):
                  "roofline_frac": CFG.updates / (ms_e * 1e-3) / 1e12 / ex2_peak}
     barrier(world)
 
+    # ---- the other scan workloads (rank 0)
+    subs = {}
+    if rank == 0 and not args.no_sub_configs:
+        for name in SUB_CONFIGS:
+            if name != CFG.name:
+                subs["scan_" + name] = run_scan_config(
+                    dev, S, W.SCAN_CONFIGS[name], sms, sm_mhz, hbm_peak,
+                    cpu=(world == 1 and not args.no_cpu_baseline))
+        torch.cuda.synchronize()
+
     # ---- CPU baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cores = os.cpu_count() or 1
-        rate, rows, secs, desc = oracle_sample_rate(20.0, cores)
-        cpu = {"value": rate, "unit": "elements/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
+        cpu = cpu_baseline(CFG, os.cpu_count() or 1, 24.0)
 
     if rank == 0:
         line = {
@@ -441,16 +521,10 @@ def run_gpu(args):
             "hbm": {"achieved_gbs": bytes_step / (ms_step * 1e-3) / 1e9, "peak_gbs": hbm_peak,
                     "frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm_peak,
                     "bytes_per_step": bytes_step, "peak_kind": peak_kind},
-            "roofline": {"bound": "alu", "achieved": achieved_exp, "peak": ex2_peak,
-                         "unit": "Texp/s", "frac": achieved_exp / ex2_peak, "traffic": traffic,
-                         "kernel": "scan_channel_mixed_kernel<bf16, N=16, gate> (the library's "
-                                   "choice at this size: two one-lane-per-channel CTAs per SM "
-                                   "plus the 24 leftover tiles as 96 four-lane CTAs)",
-                         "units_per_launch": CFG.updates,
-                         "peak_note": "148 SMs x 32 ex2/clk/SM (measured ex2.approx.f32 "
-                                      "throughput) x 2032 MHz max SM clock"},
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": "elements/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                    "link": link_fraction(link, h2d, d2h, e2e_s)},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "wall_s_timed": wall,
@@ -463,6 +537,7 @@ def run_gpu(args):
             line["scan_euler"] = euler
         if bwd:
             line["scan_bwd"] = bwd
+        line.update(subs)
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -470,6 +545,114 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def run_scan_config(dev, S, cfg, sms, sm_mhz, hbm_peak, cpu=True) -> dict:
+    """One more scan workload through the C ABI (inputs resident on the device): its
+    time per scan, elements/s, algorithmic GB/s, roofline against its binding term,
+    the plan the library chose, and (cpu) the oracle's rate on a sample of it.
+    Workloads that fit in L2 are timed one scan at a time after a 256 MB write (cold
+    L2), and also back to back (L2-warm)."""
+    import torch
+    x = W.make_scan_inputs(cfg, seed=0)
+    io = lambda a: None if a is None else to_dev_io_cfg(a, cfg, dev)  # noqa: E731
+    f32 = lambda a: None if a is None else torch.from_numpy(a).to(dev)  # noqa: E731
+    u, dl, z, B, C = io(x["u"]), io(x["delta"]), io(x.get("z")), io(x["B"]), io(x["C"])
+    A, Dv, bias = f32(x["A"]), f32(x.get("D")), f32(x.get("delta_bias"))
+    y = torch.empty_like(u)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        S.scan_fwd(u, dl, A, B, C, D=Dv, z=z, delta_bias=bias, out=y)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    assert S.read_device_status() == 0
+    plan = S.last_plan()
+    nbytes = scan_bytes(cfg)
+    steps = 20 if cfg.elements > 1e8 else 200
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_warm = e0.elapsed_time(e1) / steps
+    ms, l2 = ms_warm, f"inputs ({nbytes / 1e6:.0f} MB) larger than L2; back to back"
+    if nbytes < L2_BYTES:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        l2 = (f"inputs ({nbytes / 1e6:.1f} MB) fit in L2: each scan timed alone after a "
+              f"256 MB write (cold L2); ms_per_step_l2_warm back to back")
+    assert S.read_device_status() == 0
+    roof = scan_roofline(cfg, ms, sms, sm_mhz, hbm_peak)
+    roof["traffic"] = profiled_traffic({"long": "scan_channel_long",
+                                        "130m": "scan_chunk_130m"}.get(cfg.name, ""))
+    roof["kernel"] = plan
+    rec = {"workload": cfg.description, "batch": cfg.batch, "dim": cfg.dim,
+           "dstate": cfg.dstate, "seqlen": cfg.seqlen,
+           "io": "bf16" if cfg.io == W.BF16 else "fp32",
+           "ms_per_step": ms, "ms_per_step_l2_warm": ms_warm,
+           "value": cfg.elements / (ms * 1e-3), "unit": "elements/s",
+           "hbm": {"achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "bytes_per_step": nbytes,
+                   "frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak},
+           "roofline": roof, "l2": l2, "steps": steps,
+           "gpu_launches": steps * (2 if "segmented" in plan else 1)}
+    del u, dl, z, B, C, y
+    if cpu:
+        rec["cpu_baseline"] = cpu_baseline(cfg, os.cpu_count() or 1, 4.0)
+    return rec
+
+
+def to_dev_io_cfg(a, cfg, dev):
+    import torch
+    if cfg.io == W.BF16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def link_peak(dev, nbytes: int = 512 << 20) -> dict:
+    """Pinned host <-> device copy bandwidth: one cudaMemcpyAsync of 512 MB each way,
+    best of 5, timed with CUDA events."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out[name + "_gbs"] = nbytes / (best * 1e-3) / 1e9
+    out["bytes"] = nbytes
+    return out
+
+
+def link_fraction(link, h2d: int, d2h: int, e2e_s: float):
+    """The host link's floor for one end-to-end step (copy-in and copy-out of its bytes
+    at the measured peaks, the two directions overlapped) and the fraction of the step
+    that floor is."""
+    if not link:
+        return None
+    floor = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9))
+    return dict(link, floor_ms=floor * 1e3, frac=floor / e2e_s,
+                note="floor = the larger of the step's host-to-device and device-to-host "
+                     "bytes at the measured pinned-copy peaks (directions overlapped)")
 
 
 def run_conv(dev, S, iters=50):
@@ -553,16 +736,20 @@ def run_bwd(dev, S, iters=20):
     ms = e0.elapsed_time(e1) / iters
     peaks, kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    ex2_peak = EX2_PER_CLK_SM * SM_COUNT * SM_MAX_MHZ * 1e6 / 1e12
+    peaks_mhz = float(peaks.get("sm_max_mhz", SM_MAX_MHZ))
+    ex2_peak = (EX2_PER_CLK_SM * torch.cuda.get_device_properties(dev).multi_processor_count
+                * peaks_mhz * 1e6 / 1e12)
     texp = CFG.updates / (ms * 1e-3) / 1e12
     nbytes = bwd_bytes(CFG)
     return {"workload": f"gradient of the {CFG.name} scan (du, ddelta, dz, dA, dB, dC, dD, "
                         "ddelta_bias, dh0)",
             "ms_per_call": ms, "value": CFG.elements / (ms * 1e-3), "unit": "elements/s",
-            # the gradient kernel (bf16 io: one launch for the CTAs on the fast ZOH
-            # arithmetic, one for the rest), the segments' first pass when the
-            # sequence is split (as many again), and the two fixed-order reductions
-            "gpu_launches": ((2 if CFG.io == W.BF16 else 1) * (2 if bwd_split(CFG) else 1)
+            # bf16 ZOH: the classify kernel, then the gradient kernel as two launches
+            # (the CTAs on the series coefficients, then those on the fast ones); the
+            # segments' first pass when the sequence is split (as many again); the two
+            # fixed-order reductions
+            "gpu_launches": ((1 if CFG.io == W.BF16 else 0)
+                             + (2 if CFG.io == W.BF16 else 1) * (2 if bwd_split(CFG) else 1)
                              + 2) * iters,
             "roofline": {"bound": "alu", "achieved": texp, "peak": ex2_peak, "unit": "Texp/s",
                          "frac": texp / ex2_peak,
@@ -654,6 +841,8 @@ def main():
     ap.add_argument("--impl", default="libssm", choices=["libssm", "reference"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-configs", action="store_true",
+                    help="skip the 130M-like, long and tiny scan sub-records")
     ap.add_argument("--algo", default="auto",
                     choices=["auto", "channel", "chunk", "channel_l1", "channel_l2", "channel_l4"],
                     help="scan kernel family (default: the library's own choice)")
