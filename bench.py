@@ -277,19 +277,39 @@ class OracleSample:
 def cpu_baseline(cfg, cores: int, target_s: float) -> dict:
     """The oracle as it stands, warmed up, timed on a bounded row sample of `cfg`: all
     host cores (about 2/3 of `target_s`) and one core (the rest).  elements/s =
-    rows x seqlen / seconds."""
+    rows x seqlen / seconds.  Timed in a fresh process (as the reference arm is), so
+    the GPU arm's torch threads and CUDA context do not share the cores."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", cfg.name,
+           "--cpu-target-s", str(target_s), "--cpu-cores", str(cores)]
+    if cfg.batch != W.SCAN_CONFIGS[cfg.name].batch:
+        cmd += ["--batch", str(cfg.batch)]
+    r = subprocess.run(cmd, capture_output=True, text=True, check=True)
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_local(cfg, cores: int, target_s: float) -> dict:
+    """cpu_baseline's measurement, in this process."""
     smp = OracleSample(cfg)
     per_row = smp.per_row_seconds()
     L = cfg.seqlen
+
+    def timed(rows, threads, budget):
+        # repeat the sample until the budget is spent (at least once)
+        reps, total = 0, 0.0
+        while reps == 0 or total < budget:
+            total += smp.run(rows, threads)
+            reps += 1
+        return reps, total
+
     rows1 = int(max(1, min(smp.max_rows, target_s / 3 / per_row)))
-    t1 = smp.run(rows1, 1)
+    reps1, t1 = timed(rows1, 1, target_s / 3)
     rows = int(max(min(cores, smp.max_rows), min(smp.max_rows, target_s * 2 / 3 * cores / per_row)))
-    smp.run(min(rows, 2 * cores), cores)  # warm the thread pool
-    tn = smp.run(rows, cores)
-    return {"value": rows * L / tn, "unit": "elements/s", "cores": cores, "kind": "oracle",
-            "sample": smp.describe(rows, cores),
-            "single_core": {"value": rows1 * L / t1, "unit": "elements/s", "cores": 1,
-                            "sample": smp.describe(rows1, 1)}}
+    smp.run(rows, cores)  # warm: the thread pool and the output pages
+    reps, tn = timed(rows, cores, target_s * 2 / 3)
+    return {"value": reps * rows * L / tn, "unit": "elements/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x " + smp.describe(rows, cores),
+            "single_core": {"value": reps1 * rows1 * L / t1, "unit": "elements/s", "cores": 1,
+                            "sample": f"{reps1} x " + smp.describe(rows1, 1)}}
 
 
 def oracle_sample_rate(target_core_seconds: float, cores: int, steps: int = 1):
@@ -843,6 +863,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-configs", action="store_true",
                     help="skip the 130M-like, long and tiny scan sub-records")
+    ap.add_argument("--cpu-baseline-only", default=None, choices=sorted(W.SCAN_CONFIGS),
+                    help="time the oracle on a sample of this workload and print its JSON "
+                         "(the bench runs this in a fresh process)")
+    ap.add_argument("--cpu-target-s", type=float, default=20.0)
+    ap.add_argument("--cpu-cores", type=int, default=0)
     ap.add_argument("--algo", default="auto",
                     choices=["auto", "channel", "chunk", "channel_l1", "channel_l2", "channel_l4"],
                     help="scan kernel family (default: the library's own choice)")
@@ -872,6 +897,13 @@ def main():
         DECODE_STEPS = args.decode_steps
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.cpu_baseline_only:
+        cfg = W.SCAN_CONFIGS[args.cpu_baseline_only]
+        if args.batch:
+            cfg = dataclasses.replace(cfg, batch=args.batch)
+        print(json.dumps(cpu_baseline_local(cfg, args.cpu_cores or (os.cpu_count() or 1),
+                                            args.cpu_target_s)), flush=True)
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     if args.decode_only:

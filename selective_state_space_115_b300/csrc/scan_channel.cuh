@@ -362,15 +362,16 @@ __device__ __forceinline__ void chan_positions(const float* bcfB, const float* b
 // one chunk of positions for one lane (its channel's row `row` of the tiles,
 // its states part*NS .. part*NS + NS - 1).  ACC: accurate arithmetic for the
 // whole chunk (fp32 io, or a channel group with small |A|); otherwise each block
-// whose step sizes reach below `s_min` (a state update with |dt A log2 e| under
-// kFastPathMinQ) takes the accurate update, the rest the fast one.
+// whose raw step argument x2 = (delta + bias) log2 e reaches below `x2_min` (the
+// argument whose step gives a state update with |dt A log2 e| = kFastPathMinQ)
+// takes the accurate update, the rest the fast one.
 // ---------------------------------------------------------------------------
 template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG>
 __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile, const float* bcfB,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
                                            const float* nIA, float Dd, float bias2, int softplus,
-                                           float s_min, float* h, float& ssum) {
+                                           float x2_min, float* h, float& ssum) {
   constexpr bool OUT = MODE != kModeStates;  // this pass writes y
   constexpr int LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB, RB = Cfg::RB;
   const uint8_t* tu = stage;
@@ -383,18 +384,29 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
     const uint32_t off = swz<RB>(row, blk);
     float uj[TB], sj[TB];
     lds_vals<IO, TB>(tu + off, uj);
-    // step sizes of this lane's positions, then shared with the channel's lanes
+    // step sizes of this lane's positions, then shared with the channel's lanes; the
+    // smallest raw argument x2 of the block (softplus is monotone) for the choice of
+    // update below, formed beside the softplus chain rather than after it
+    float x2min;
     {
       float dm[PB], sm[PB];
       lds_vals<IO, PB>(td + off + pofs, dm);
+      float x2s[PB];
+#pragma unroll
+      for (int k = 0; k < PB; ++k) x2s[k] = fmaf(dm[k], kLog2e, bias2);
+      x2min = x2s[0];
+#pragma unroll
+      for (int k = 1; k < PB; ++k) x2min = fminf(x2min, x2s[k]);
 #pragma unroll
       for (int k = 0; k < PB; ++k) {
-        const float x2 = fmaf(dm[k], kLog2e, bias2);
+        const float x2 = x2s[k];
         float s = softplus ? (ACC ? softplus_log2_accurate(x2) : softplus_log2_fast(x2)) : x2;
         if constexpr (TAIL) s = (l0 + blk * TB + part * PB + k < seqlen) ? s : 0.0f;  // Abar = 1
         sm[k] = s;
       }
       allgather<LPC, PB>(sm, sj, xch, lane);
+      if constexpr (LPC >= 2) x2min = fminf(x2min, __shfl_xor_sync(0xffffffffu, x2min, 1));
+      if constexpr (LPC >= 4) x2min = fminf(x2min, __shfl_xor_sync(0xffffffffu, x2min, 2));
     }
     if constexpr (!OUT) {
 #pragma unroll
@@ -409,11 +421,10 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
     } else {
       // a step too small for Abar (h + w) - w (its error relative to the update grows
       // like 2^-22 / |q|): this block takes the accurate update.  The decision depends
-      // only on the channel's own step sizes and A row, so every lane split takes it alike.
-      float smallest = sj[0];
-#pragma unroll
-      for (int j = 1; j < TB; ++j) smallest = fminf(smallest, sj[j]);
-      if (!(smallest >= s_min))
+      // only on the channel's own raw steps and A row, so every lane split takes it
+      // alike.  (Past the end of the sequence u is zero-filled, so the fast form
+      // leaves h exactly unchanged there whatever is decided.)
+      if (!(x2min >= x2_min))
         chan_positions<Cfg, OUT, AR_ACC>(bcfB, bcfC, blk, part, uj, sj, Areg, nIA, h, acc);
       else
         chan_positions<Cfg, OUT, kArFast>(bcfB, bcfC, blk, part, uj, sj, Areg, nIA, h, acc);
@@ -518,14 +529,16 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
     if constexpr (sizeof(IO) == 2) accurate = __any_sync(0xffffffffu, small_a);
     neg = !__any_sync(0xffffffffu, nonneg);
   }
-  // smallest step size (log2 units) the fast update takes for this channel: every
-  // state's |q| = s |A| must reach kFastPathMinQ
-  float s_min = 0.0f;
+  // smallest raw step argument x2 = (delta + bias) log2 e the fast update takes for
+  // this channel: every state's |q| = s |A| must reach kFastPathMinQ, with the step
+  // s = log2(1 + 2^x2) (softplus) or s = x2; inverted, x2 = log2(2^s - 1)
+  float x2_min = -3.0e38f;
   if (sizeof(IO) == 2 && !accurate && valid) {
     float amin = fabsf(__ldg(p.A + static_cast<int64_t>(d) * N));
 #pragma unroll
     for (int i = 1; i < N; ++i) amin = fminf(amin, fabsf(__ldg(p.A + static_cast<int64_t>(d) * N + i)));
-    s_min = kFastPathMinQ / amin;
+    const float s_min = kFastPathMinQ / amin;
+    x2_min = p.softplus ? log2f(expm1f(s_min * kLn2)) : s_min;
   }
 
   if (tid == 0) {
@@ -605,7 +618,7 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
     // (the group flags are warp-uniform: every lane of a warp takes the same branch)
 #define SSM_CHAN_CHUNK(ACC, TAIL, NEG)                                                        \
   chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,   \
-                                            p.seqlen, Areg, nIA, Dd, bias2, p.softplus, s_min, \
+                                            p.seqlen, Areg, nIA, Dd, bias2, p.softplus, x2_min, \
                                             h, ssum)
     bool fast_chunk = false;
     if constexpr (sizeof(IO) == 2) fast_chunk = !accurate;

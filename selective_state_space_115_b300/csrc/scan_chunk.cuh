@@ -13,7 +13,7 @@
 // and the state after the last lane is carried (in shared memory) to the next chunk.
 // The 4-D (position, state) tensor exists only as T pairs per lane per state.
 //
-// A CTA holds WARPS channels of one batch row, which share B and C: each chunk's B
+// A CTA holds WARPS (8) channels of one batch row, which share B and C: each chunk's B
 // and C tiles ([N][32*T] each) are staged once per CTA in shared memory (cp.async,
 // one chunk ahead, when rows are 16-byte aligned; element loads otherwise), so the
 // per-state loop reads them from shared memory instead of waiting on global loads.
@@ -32,7 +32,10 @@ struct ChunkCfg {
   static constexpr bool GATE = GATE_;
   static constexpr bool EULER = EULER_;     // input term dt * B instead of the ZOH form
   static constexpr bool VEC = VEC_;
-  static constexpr int WARPS = 4;
+  // 8 channels per CTA: the CTAs of a 3072-channel layer (the 130M-like one) then
+  // fit the SMs in one wave (3 per SM by the 64 KB of B, C staging); at 4 channels
+  // they took 1.73 waves (measured on B300: 148 -> 124 us)
+  static constexpr int WARPS = 8;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int ESZ = Io<IO>::kBytes;
   static constexpr int T = 32 / ESZ;        // positions per lane: 16 bf16 / 8 fp32 (32 bytes)
