@@ -172,6 +172,34 @@ __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const 
     lds_run<IO, T>(tile + n * LCH + lane * T, Bv);
     lds_run<IO, T>(tile + (N + n) * LCH + lane * T, Cv);
     float P = 1.0f, H = 0.0f;
+    if constexpr (!Cfg::EULER && (AR == kArFast || AR == kArNeg)) {
+      // pairs of positions in packed f32x2 arithmetic (the two ex2 issue in the shadow
+      // of the packed FMAs); the fold of H and P stays sequential over the positions
+      const f2 An2 = mk2(An, An), nIA2 = mk2(-IAn, -IAn), one = mk2(1.0f, 1.0f);
+#pragma unroll
+      for (int i = 0; i < T; i += 2) {
+        const f2 X = mul2(mk2(Bv[i], Bv[i + 1]), mk2(u[i], u[i + 1]));
+        f2 a2, bb2;
+        if constexpr (AR == kArFast) {
+          const f2 q = mul2(mk2(s[i], s[i + 1]), An2);
+          a2 = mk2(ex2(q.x), ex2(q.y));
+          bb2 = mul2(mul2(X, nIA2), sub2(one, a2));        // (Abar - 1) B u / A
+        } else {
+          const f2 nq = mul2(mk2(-s[i], -s[i + 1]), An2);  // -q >= 0
+          const f2 ome = one_minus_exp2_neg2(nq, mk2(ex2(-nq.x), ex2(-nq.y)));  // 1 - Abar
+          a2 = sub2(one, ome);
+          bb2 = mul2(mul2(ome, nIA2), X);                  // (Abar - 1) / A B u
+        }
+        a[i] = a2.x;
+        a[i + 1] = a2.y;
+        bb[i] = bb2.x;
+        bb[i + 1] = bb2.y;
+        H = fmaf(a[i], H, bb[i]);
+        P *= a[i];
+        H = fmaf(a[i + 1], H, bb[i + 1]);
+        P *= a[i + 1];
+      }
+    } else {
 #pragma unroll
     for (int i = 0; i < T; ++i) {
       const float q = s[i] * An;
@@ -197,6 +225,7 @@ __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const 
       }
       H = fmaf(a[i], H, bb[i]);
       P *= a[i];
+    }
     }
     // inclusive warp scan of (P, H) over lanes (lane order = position order)
 #pragma unroll
