@@ -305,6 +305,51 @@ SSM_API ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, i
                                    ssm_discretization disc, int segments, ssm_stream_t stream);
 
 /*
+ * Training step: the forward writes the state checkpoints the gradient needs, so the
+ * gradient runs no forward pass of its own.  The pages' recomputation (lengnian,
+ * Part3: intermediate states recomputed in the backward pass instead of stored) keeps
+ * one fp32 state per channel every 8 positions (4 bytes per state every 8 positions:
+ * the (B, L, D, N) tensor is never stored).
+ *
+ * ssm_scan_ckpt_bytes: bytes of the checkpoints, ceil(seqlen / 8) * batch * dim *
+ * dstate * 4 (0 for invalid sizes).
+ *
+ * ssm_scan_fwd_train: ssm_scan_fwd_ex (same arguments, same y and h_last, bit for
+ * bit) that also writes ckpt[j][b * dim + d][n] = the state entering position 8 j
+ * (j = 0 .. ceil(seqlen / 8) - 1; j = 0 holds h0, or 0), float32, device memory owned
+ * by the caller, 16-byte aligned, ckpt_bytes >= ssm_scan_ckpt_bytes().
+ * SSM_ERR_INVALID_ARG for a NULL, misaligned or short buffer.
+ *
+ * ssm_scan_bwd_ckpt: ssm_scan_bwd_ex from those checkpoints (`ckpt`, as the training
+ * forward wrote them for the same inputs and h0; float32, 4-byte aligned); workspace
+ * of ssm_scan_bwd_ckpt_workspace_size() bytes (no room for checkpoints of its own).
+ * The gradient equals ssm_scan_bwd_ex's up to the rounding of the states the two
+ * forwards compute.
+ */
+SSM_API size_t ssm_scan_ckpt_bytes(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+SSM_API ssm_status ssm_scan_fwd_train(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                      ssm_dtype io, const void* u, const void* delta,
+                                      const float* delta_bias, int delta_softplus,
+                                      const float* A, const void* B, const void* C,
+                                      const float* D, const void* z, const float* h0,
+                                      float* h_last, void* y, float* ckpt, size_t ckpt_bytes,
+                                      void* workspace, size_t workspace_bytes,
+                                      ssm_discretization disc, ssm_algo algo,
+                                      ssm_stream_t stream);
+SSM_API size_t ssm_scan_bwd_ckpt_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                                int64_t seqlen, int segments);
+SSM_API ssm_status ssm_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                     ssm_dtype io, const void* u, const void* delta,
+                                     const float* delta_bias, int delta_softplus, const float* A,
+                                     const void* B, const void* C, const float* D, const void* z,
+                                     const float* h0, const float* ckpt, const void* dy,
+                                     const float* dh_last, void* du, void* ddelta, float* dA,
+                                     void* dB, void* dC, float* dD, void* dz,
+                                     float* ddelta_bias, float* dh0, void* workspace,
+                                     size_t workspace_bytes, ssm_discretization disc,
+                                     int segments, ssm_stream_t stream);
+
+/*
  * Causal depthwise convolution over time, the step before the scan in the
  * MambaBlock of Mamba_Model_Report.md (section 3: nn.Conv1d with groups = channels,
  * kernel_size = width, padding = width - 1, the first L outputs, then silu):

@@ -51,7 +51,9 @@ EXPORTED = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd_algo_workspace_size", "
             "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex", "ssm_selftest_wait",
             "ssm_scan_fwd_host_workspace_size", "ssm_scan_fwd_host",
             "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_read_device_status",
-            "ssm_status_string", "ssm_last_cuda_error", "ssm_last_plan", "ssm_version")
+            "ssm_status_string", "ssm_last_cuda_error", "ssm_last_plan", "ssm_version",
+            "ssm_scan_ckpt_bytes", "ssm_scan_fwd_train", "ssm_scan_bwd_ckpt_workspace_size",
+            "ssm_scan_bwd_ckpt")
 
 
 class SsmError(RuntimeError):
@@ -101,6 +103,11 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_fwd_noalloc.argtypes = scan_args[:17] + [_vp]
         lib.ssm_scan_fwd_ex.restype = _int
         lib.ssm_scan_fwd_ex.argtypes = scan_args + [_int, _int, _vp]
+        lib.ssm_scan_ckpt_bytes.restype = ctypes.c_size_t
+        lib.ssm_scan_ckpt_bytes.argtypes = [_i64, _i64, _i64, _i64]
+        lib.ssm_scan_fwd_train.restype = _int
+        lib.ssm_scan_fwd_train.argtypes = (scan_args[:17] + [_vp, ctypes.c_size_t]
+                                           + scan_args[17:] + [_int, _int, _vp])
         lib.ssm_state_update.restype = _int
         lib.ssm_state_update.argtypes = [_i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _int, _vp,
                                          _vp, _vp, _vp, _vp, _vp, _vp]
@@ -123,6 +130,11 @@ def library(path: Optional[str] = None):
         lib.ssm_scan_bwd_ex.restype = _int
         lib.ssm_scan_bwd_ex.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
                                         + [_vp] * 18 + [ctypes.c_size_t, _int, _int, _vp])
+        lib.ssm_scan_bwd_ckpt_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_bwd_ckpt_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _int]
+        lib.ssm_scan_bwd_ckpt.restype = _int
+        lib.ssm_scan_bwd_ckpt.argtypes = ([_i64, _i64, _i64, _i64, _int, _vp, _vp, _vp, _int]
+                                          + [_vp] * 19 + [ctypes.c_size_t, _int, _int, _vp])
         lib.ssm_scan_fwd_host_workspace_size.restype = ctypes.c_size_t
         lib.ssm_scan_fwd_host_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _int, _int,
                                                          _int, _int, _int]
@@ -213,13 +225,16 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True, h0=None,
              return_last_state=False, algo="auto", out=None, workspace=None,
-             discretization="zoh"):
+             discretization="zoh", ckpt=None):
     """Selective-scan forward on torch CUDA tensors.
 
     u, delta, z, out: [batch, dim, seqlen] (float32 or bfloat16); B, C: [batch, dstate, seqlen]
     (same dtype); A: [dim, dstate] float32; D, delta_bias: [dim] float32; h0: [batch, dim,
     dstate] float32.  Returns y (and h_last [batch, dim, dstate] float32 when asked).
-    discretization: "zoh" (default) or "euler" (input term dt * B)."""
+    discretization: "zoh" (default) or "euler" (input term dt * B).
+    ckpt (training forward, ssm_scan_fwd_train): a float32 tensor [ceil(seqlen / 8), batch,
+    dim, dstate] that receives the state entering every block of 8 positions, for
+    scan_bwd(..., ckpt=...)."""
     if not isinstance(u, torch.Tensor) or not u.is_cuda:
         raise SsmError(SSM_ERR_INVALID_ARG, "u must be a CUDA tensor")
     if u.dim() != 3:
@@ -245,6 +260,18 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     nbytes = int(lib.ssm_scan_fwd_algo_workspace_size(batch, dim, dstate, seqlen, _ALGOS[algo]))
     ws = _workspace(dev, nbytes) if workspace is None else workspace
     stream = torch.cuda.current_stream(dev).cuda_stream
+    if ckpt is not None:
+        _need(ckpt, "ckpt", ((seqlen + 7) // 8, batch, dim, dstate), torch.float32, dev)
+        with torch.cuda.device(dev):
+            st = lib.ssm_scan_fwd_train(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                        _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
+                                        _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(h0),
+                                        _ptr(h_last), _ptr(y), _ptr(ckpt),
+                                        ckpt.numel() * 4, _ptr(ws), ws.numel(),
+                                        _DISC[discretization], _ALGOS[algo],
+                                        ctypes.c_void_p(stream))
+        _check(st, "ssm_scan_fwd_train")
+        return (y, h_last) if return_last_state else y
     with torch.cuda.device(dev):
         st = lib.ssm_scan_fwd_ex(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
                                  _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
@@ -253,6 +280,11 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                                  ctypes.c_void_p(stream))
     _check(st, "ssm_scan_fwd")
     return (y, h_last) if return_last_state else y
+
+
+def ckpt_shape(batch: int, dim: int, dstate: int, seqlen: int):
+    """Shape of the training forward's checkpoint tensor (float32)."""
+    return ((seqlen + 7) // 8, batch, dim, dstate)
 
 
 _bwd_ws_cache = {}
@@ -264,14 +296,16 @@ def scan_bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> i
 
 def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True,
              h0=None, dh_last=None, want_dh0=True, discretization="zoh", workspace=None,
-             segments=0):
+             segments=0, ckpt=None):
     """Gradient of scan_fwd for the upstream gradient dy [batch, dim, seqlen] (and
     dh_last [batch, dim, dstate] float32 for the final state).  Takes the forward's
     inputs as passed to scan_fwd.  Returns a dict: du, ddelta, dz (io dtype,
     [batch, dim, seqlen]); dB, dC (io dtype, [batch, dstate, seqlen]); dA [dim, dstate],
     dD [dim] (when D), ddelta_bias [dim] (when delta_bias), dh0 [batch, dim, dstate]
     (when want_dh0), all float32.  segments: split of the sequence (0: the
-    library's choice)."""
+    library's choice).  ckpt: the training forward's checkpoints (scan_fwd(...,
+    ckpt=...)) for the same inputs; the gradient then runs no forward pass of its own
+    (ssm_scan_bwd_ckpt)."""
     if not isinstance(u, torch.Tensor) or not u.is_cuda:
         raise SsmError(SSM_ERR_INVALID_ARG, "u must be a CUDA tensor")
     if u.dim() != 3:
@@ -298,9 +332,12 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
          "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
          "dh0": torch.empty((batch, dim, dstate), **f32) if want_dh0 else None}
     lib = library()
+    if ckpt is not None:
+        _need(ckpt, "ckpt", ((seqlen + 7) // 8, batch, dim, dstate), torch.float32, dev)
     with torch.cuda.device(dev):
-        nbytes = int(lib.ssm_scan_bwd_ex_workspace_size(batch, dim, dstate, seqlen,
-                                                        int(segments)))
+        size_fn = (lib.ssm_scan_bwd_ckpt_workspace_size if ckpt is not None
+                   else lib.ssm_scan_bwd_ex_workspace_size)
+        nbytes = int(size_fn(batch, dim, dstate, seqlen, int(segments)))
     if workspace is None:
         ws = _bwd_ws_cache.get(dev.index)
         if ws is None or ws.numel() < nbytes:
@@ -309,15 +346,24 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
     else:
         ws = workspace
     stream = torch.cuda.current_stream(dev).cuda_stream
+    grads = (_ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+             _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]))
     with torch.cuda.device(dev):
-        st = lib.ssm_scan_bwd_ex(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
-                                 _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A), _ptr(B),
-                                 _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(dy), _ptr(dh_last),
-                                 _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
-                                 _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]),
-                                 _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), _ptr(ws), ws.numel(),
-                                 _DISC[discretization], int(segments), ctypes.c_void_p(stream))
-    _check(st, "ssm_scan_bwd")
+        if ckpt is not None:
+            st = lib.ssm_scan_bwd_ckpt(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                       _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
+                                       _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(h0),
+                                       _ptr(ckpt), _ptr(dy), _ptr(dh_last), *grads, _ptr(ws),
+                                       ws.numel(), _DISC[discretization], int(segments),
+                                       ctypes.c_void_p(stream))
+        else:
+            st = lib.ssm_scan_bwd_ex(batch, dim, dstate, seqlen, io, _ptr(u), _ptr(delta),
+                                     _ptr(delta_bias), int(bool(delta_softplus)), _ptr(A),
+                                     _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(h0), _ptr(dy),
+                                     _ptr(dh_last), *grads, _ptr(ws), ws.numel(),
+                                     _DISC[discretization], int(segments),
+                                     ctypes.c_void_p(stream))
+    _check(st, "ssm_scan_bwd_ckpt" if ckpt is not None else "ssm_scan_bwd")
     return g
 
 

@@ -77,6 +77,10 @@ struct BwdParams {
   float* seg_sum;  // [nseg][batch * dim]: sum of the segment's step sizes (log2 units)
   // [nseg * batch * tiles] (bf16 ZOH): 1 where the CTA takes the fast coefficients
   const unsigned char* cta_fast;
+  // the training forward's checkpoints, [nblk][batch * dim][N] in state order (the
+  // state entering every block): when given, the gradient runs no forward pass of its
+  // own (phase 1 and the segments' forward half are skipped)
+  const float* ckpt_in;
 };
 
 template <typename IO, int N_, bool GATE_, bool EULER_, bool VEC_, int THREADS_ = 128>
@@ -508,8 +512,9 @@ __device__ __forceinline__ void bwd_segment_pass(
   IO rb[Cfg::BC_EPT], rc[Cfg::BC_EPT];
   float ssum = 0.0f;
 
-  // forward from a zero state (every segment but the last)
-  if (seg < p.nseg - 1) {
+  // forward from a zero state (every segment but the last; not needed when the
+  // training forward's checkpoints give every block's entering state)
+  if (seg < p.nseg - 1 && !p.ckpt_in) {
     float h[NS];
 #pragma unroll
     for (int k = 0; k < NS; ++k) h[k] = 0.0f;
@@ -572,7 +577,7 @@ __device__ __forceinline__ void bwd_segment_pass(
       for (int pp = kBwdPos - 1; pp >= 0; --pp) {
         if (l0 + pp < p.seqlen) {
           const float s = S[chl * Cfg::SCS + pp];
-          if (seg == p.nseg - 1) ssum += s;
+          if (seg == p.nseg - 1 || p.ckpt_in) ssum += s;
           float dy0 = ld_io<IO>(stage(buf) + 3 * Cfg::CHB, chl * Cfg::ROWB, pp);
           if constexpr (Cfg::GATE) {
             const float zf = ld_io<IO>(stage(buf) + 2 * Cfg::CHB, chl * Cfg::ROWB, pp);
@@ -674,13 +679,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
     bwd_segment_pass<Cfg, FAST>(p, smem, seg, b, d0, chl, part, n0, perm, chv, row, rowbase,
                                 rows, l_begin, j_begin, j_end, bias, a, ra);
   } else {
+    // checkpoints of the state entering every block, in state order: the training
+    // forward's, or those phase 1 writes below
+    const float* ckr = p.ckpt_in ? p.ckpt_in : p.ckpt;
     // state entering the segment: h0, then each earlier segment i folded in as
     // h <- 2^(A sum_i) h + E_i (the recurrence is linear in h; 2^(A sum_i) is the
     // product of segment i's Abar factors)
     float h[NS];
 #pragma unroll
     for (int k = 0; k < NS; ++k) h[k] = (chv && p.h0) ? p.h0[row * N + n0 + (k ^ perm)] : 0.0f;
-    if (chv) {
+    if (chv && !p.ckpt_in) {
 #pragma unroll 1
       for (int i = 0; i < seg; ++i) {
         const float sum = p.seg_sum[i * rows + row];
@@ -692,13 +700,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
 
     const int nblk = j_end - j_begin;  // blocks of this segment
     // ---------------- phase 1: forward, checkpoint entering each block
-    if (nblk > 0) {
+    if (nblk > 0 && !p.ckpt_in) {
       bwd_stage<Cfg>(p, stage(0), rowbase, d0, l_begin, false);
       cp_async_commit();
       bwd_bc_fetch<Cfg>(p, b, l_begin, false, rb, rc);
       bwd_bc_park<Cfg>(bcbuf(0), rb, rc);
     }
-    for (int jj = 0; jj < nblk; ++jj) {
+    for (int jj = 0; jj < (p.ckpt_in ? 0 : nblk); ++jj) {
       const int j = j_begin + jj, l0 = j * kBwdPos, buf = jj & 1;
       cp_async_wait_all();
       __syncthreads();  // stage j and B of block j visible; block j-1 fully consumed
@@ -712,7 +720,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
       if (chv) {
 #pragma unroll
         for (int k = 0; k < NS; ++k)
-          p.ckpt[(static_cast<int64_t>(j) * rows + row) * N + n0 + k] = h[k];
+          p.ckpt[(static_cast<int64_t>(j) * rows + row) * N + n0 + (k ^ perm)] = h[k];
       }
       __syncwarp();
       bwd_advance<Cfg, FAST>(p, stage(buf), bt(buf), S, chl, n0, l0, a, ra, h);
@@ -751,7 +759,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
       if (chv) {
 #pragma unroll
         for (int k = 0; k < NS; ++k)
-          hn[k] = p.ckpt[(static_cast<int64_t>(j_end - 1) * rows + row) * N + n0 + k];
+          hn[k] = ckr[(static_cast<int64_t>(j_end - 1) * rows + row) * N + n0 + (k ^ perm)];
       }
     }
     for (int it = 0; it < nblk; ++it) {
@@ -768,7 +776,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
         if (chv) {
 #pragma unroll
           for (int k = 0; k < NS; ++k)
-            hn[k] = p.ckpt[(static_cast<int64_t>(j - 1) * rows + row) * N + n0 + k];
+            hn[k] = ckr[(static_cast<int64_t>(j - 1) * rows + row) * N + n0 + (k ^ perm)];
         }
       }
       bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, p.softplus != 0);

@@ -61,7 +61,13 @@ struct ScanParams {
   int seg_len;              // positions per segment (a multiple of the chunk)
   float* seg_state;         // [nseg][batch * dim][N]: end state of each segment from h = 0
   float* seg_sum;           // [nseg][batch * dim]: sum of dt * log2(e) over each segment
+  // training forward: the state entering every block of kCkptPos positions,
+  // [ceil(seqlen / kCkptPos)][batch * dim][N] fp32 (null: not written)
+  float* ckpt;
 };
+
+// positions per state checkpoint of the training forward (the gradient's block)
+constexpr int kCkptPos = 8;
 
 // Kernel modes of the channel kernel:
 //   kModeFull    one pass over the whole sequence (nseg = 1)
@@ -371,7 +377,8 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
                                            const float* nIA, float Dd, float bias2, int softplus,
-                                           float x2_min, float* h, float& ssum) {
+                                           float x2_min, float* h, float& ssum, float* ck,
+                                           int64_t ck_stride) {
   constexpr bool OUT = MODE != kModeStates;  // this pass writes y
   constexpr int LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB, RB = Cfg::RB;
   const uint8_t* tu = stage;
@@ -382,6 +389,16 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 #pragma unroll 1
   for (int blk = 0; blk < Cfg::NBLK; ++blk) {
     const uint32_t off = swz<RB>(row, blk);
+    // training forward: the state entering this block, when it starts a checkpoint block
+    if (ck) {
+      const int l = l0 + blk * TB;
+      if (l % kCkptPos == 0 && l < seqlen) {
+        float* dst = ck + static_cast<int64_t>(l / kCkptPos) * ck_stride;
+#pragma unroll
+        for (int i = 0; i < Cfg::NS; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(h[i], h[i + 1], h[i + 2], h[i + 3]);
+      }
+    }
     float uj[TB], sj[TB];
     lds_vals<IO, TB>(tu + off, uj);
     // step sizes of this lane's positions, then shared with the channel's lanes; the
@@ -484,6 +501,10 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
   // per-lane parameters and state: states part*NS .. part*NS + NS - 1
   float Areg[NS], nIA[NS], h[NS];
   const int64_t state0 = (static_cast<int64_t>(b) * p.dim + d) * N + part * NS;
+  // this lane's checkpoint slot (pass 1 of the segmented scan runs from a zero state:
+  // it writes none)
+  float* const ck = (MODE != kModeStates && valid && p.ckpt) ? p.ckpt + state0 : nullptr;
+  const int64_t ck_stride = static_cast<int64_t>(p.batch) * p.dim * N;
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
     const float a = valid ? __ldg(p.A + static_cast<int64_t>(d) * N + part * NS + i) : -1.0f;
@@ -619,7 +640,7 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
 #define SSM_CHAN_CHUNK(ACC, TAIL, NEG)                                                        \
   chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,   \
                                             p.seqlen, Areg, nIA, Dd, bias2, p.softplus, x2_min, \
-                                            h, ssum)
+                                            h, ssum, ck, ck_stride)
     bool fast_chunk = false;
     if constexpr (sizeof(IO) == 2) fast_chunk = !accurate;
     if (fast_chunk) {

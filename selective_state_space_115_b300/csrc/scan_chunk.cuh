@@ -159,7 +159,8 @@ __device__ __forceinline__ void chunk_stage_bc(const ScanParams& p, int b, int k
 template <typename IO, typename Cfg, int AR>
 __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const IO* tile,
                                              const float* s, const float* u, float* y,
-                                             float* carry) {
+                                             float* carry, float* ck, int64_t ck_stride,
+                                             int64_t l, int seqlen) {
   constexpr bool UACC = AR != kArFast;
   constexpr int N = Cfg::N, T = Cfg::T, LCH = Cfg::LCH;
   const unsigned FULL = 0xffffffffu;
@@ -245,10 +246,18 @@ __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const 
     float hs = (lane == 0) ? cin : fmaf(Pe, cin, He);
     __syncwarp();
     if (lane == 0) carry[n] = fmaf(P31, cin, H31);
+    // training forward: the states entering this lane's checkpoint blocks (its first
+    // position, and position 8 of 16); a lane's row of a checkpoint is written state by
+    // state and merges in L2
+    if (ck && l < seqlen) ck[(l / kCkptPos) * ck_stride + n] = hs;
 #pragma unroll
     for (int i = 0; i < T; ++i) {
       hs = fmaf(a[i], hs, bb[i]);
       y[i] = fmaf(Cv[i], hs, y[i]);
+      if constexpr (T > kCkptPos) {
+        if (i % kCkptPos == kCkptPos - 1 && i + 1 < T && ck && l + i + 1 < seqlen)
+          ck[((l + i + 1) / kCkptPos) * ck_stride + n] = hs;
+      }
     }
   }
 }
@@ -286,16 +295,22 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
     slow |= in && !(sv >= s_min);
     y[i] = 0.0f;
   }
+  float* const ck = p.ckpt ? p.ckpt + row * Cfg::N : nullptr;
+  const int64_t ck_stride = static_cast<int64_t>(p.batch) * p.dim * Cfg::N;
   if constexpr (Cfg::EULER) {
     // (the Euler input term dt B u has no cancellation at small steps)
-    chunk_states<IO, Cfg, ACC ? kArGen : kArFast>(Arow, lane, tile, s, u, y, carry);
+    chunk_states<IO, Cfg, ACC ? kArGen : kArFast>(Arow, lane, tile, s, u, y, carry, ck,
+                                                  ck_stride, l, p.seqlen);
   } else {
     if (!ACC && !__any_sync(0xffffffffu, slow))
-      chunk_states<IO, Cfg, kArFast>(Arow, lane, tile, s, u, y, carry);
+      chunk_states<IO, Cfg, kArFast>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
+                                     p.seqlen);
     else if (neg)
-      chunk_states<IO, Cfg, kArNeg>(Arow, lane, tile, s, u, y, carry);
+      chunk_states<IO, Cfg, kArNeg>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
+                                    p.seqlen);
     else
-      chunk_states<IO, Cfg, kArGen>(Arow, lane, tile, s, u, y, carry);
+      chunk_states<IO, Cfg, kArGen>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
+                                    p.seqlen);
   }
   float z[T];
   if constexpr (Cfg::GATE) load_run<IO, Cfg>(zrow, l, p.seqlen, z);

@@ -190,12 +190,17 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, i
   return ssm_scan_fwd_algo_workspace_size(batch, dim, dstate, seqlen, SSM_ALGO_AUTO);
 }
 
-ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                           ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
-                           int delta_softplus, const float* A, const void* B, const void* C,
-                           const float* D, const void* z, const float* h0, float* h_last,
-                           void* y, void* workspace, size_t workspace_bytes,
-                           ssm_discretization disc, ssm_algo algo, ssm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The scan forward; `ckpt` (training forward) receives the state checkpoints, else null.
+ssm_status scan_fwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                         ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
+                         int delta_softplus, const float* A, const void* B, const void* C,
+                         const float* D, const void* z, const float* h0, float* h_last, void* y,
+                         float* ckpt, void* workspace, size_t workspace_bytes,
+                         ssm_discretization disc, ssm_algo algo, ssm_stream_t stream) {
   if (disc != SSM_DISC_ZOH && disc != SSM_DISC_EULER) return SSM_ERR_UNSUPPORTED;
   if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_CHANNEL && algo != SSM_ALGO_CHUNK &&
       algo != SSM_ALGO_CHANNEL_L1 && algo != SSM_ALGO_CHANNEL_L2 && algo != SSM_ALGO_CHANNEL_L4 &&
@@ -222,6 +227,7 @@ ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
   c.y = y;
   c.softplus = delta_softplus ? 1 : 0;
   c.euler = (disc == SSM_DISC_EULER);
+  c.ckpt = ckpt;
   if (io != SSM_DTYPE_F32 && io != SSM_DTYPE_BF16) return SSM_ERR_UNSUPPORTED;
   ssm_status st = validate_scan(c, workspace, workspace_bytes);
   if (st != SSM_OK) return st;
@@ -283,6 +289,46 @@ ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                                : dispatch_scan<float>(c, algo, workspace, s, seg, mix);
   if (rs == SSM_OK) g_last_plan = describe_plan(c, algo, seg, mix);
   return rs;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                           ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
+                           int delta_softplus, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* h0, float* h_last,
+                           void* y, void* workspace, size_t workspace_bytes,
+                           ssm_discretization disc, ssm_algo algo, ssm_stream_t stream) {
+  return scan_fwd_impl(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A, B,
+                       C, D, z, h0, h_last, y, nullptr, workspace, workspace_bytes, disc, algo,
+                       stream);
+}
+
+size_t ssm_scan_ckpt_bytes(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1) return 0;
+  if (batch > (int64_t(1) << 62) / dim / seqlen / dstate) return 0;
+  return ckpt_bytes(batch, dim, dstate, seqlen);
+}
+
+ssm_status ssm_scan_fwd_train(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                              ssm_dtype io, const void* u, const void* delta,
+                              const float* delta_bias, int delta_softplus, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              const float* h0, float* h_last, void* y, float* ckpt,
+                              size_t ckpt_bytes_given, void* workspace, size_t workspace_bytes,
+                              ssm_discretization disc, ssm_algo algo, ssm_stream_t stream) {
+  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1) return SSM_ERR_INVALID_ARG;
+  if (batch > (int64_t(1) << 62) / dim / seqlen / dstate) return SSM_ERR_INVALID_ARG;
+  if (!ckpt || !aligned(ckpt, 16)) return SSM_ERR_INVALID_ARG;
+  if (ckpt_bytes_given < ckpt_bytes(batch, dim, dstate, seqlen)) {
+    g_last_cuda_error = "checkpoint buffer smaller than ssm_scan_ckpt_bytes()";
+    return SSM_ERR_INVALID_ARG;
+  }
+  return scan_fwd_impl(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A, B,
+                       C, D, z, h0, h_last, y, ckpt, workspace, workspace_bytes, disc, algo,
+                       stream);
 }
 
 ssm_status ssm_scan_fwd_algo(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
@@ -395,14 +441,20 @@ ssm_status ssm_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seql
                          dh0, workspace, workspace_bytes, disc, 0, stream);
 }
 
-ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                           ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
-                           int delta_softplus, const float* A, const void* B, const void* C,
-                           const float* D, const void* z, const float* h0, const void* dy,
-                           const float* dh_last, void* du, void* ddelta, float* dA, void* dB,
-                           void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
-                           void* workspace, size_t workspace_bytes, ssm_discretization disc,
-                           int segments, ssm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The scan gradient; `ckpt_in` (from the training forward) gives every block's entering
+// state, else null (the gradient recomputes them).
+ssm_status scan_bwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                         ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
+                         int delta_softplus, const float* A, const void* B, const void* C,
+                         const float* D, const void* z, const float* h0, const float* ckpt_in,
+                         const void* dy, const float* dh_last, void* du, void* ddelta, float* dA,
+                         void* dB, void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                         void* workspace, size_t workspace_bytes, ssm_discretization disc,
+                         int segments, ssm_stream_t stream) {
   if (segments < 0) return SSM_ERR_INVALID_ARG;
   ssm_status st = validate_common(batch, dim, dstate, io);
   if (st != SSM_OK) return st;
@@ -414,8 +466,9 @@ ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
   if ((z != nullptr) != (dz != nullptr)) return SSM_ERR_INVALID_ARG;
   if (D && !dD) return SSM_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256)) return SSM_ERR_INVALID_ARG;
-  const BwdLayout w = bwd_layout(batch, dim, dstate, seqlen, segments);
+  const BwdLayout w = bwd_layout(batch, dim, dstate, seqlen, segments, ckpt_in == nullptr);
   if (workspace_bytes < w.total) return SSM_ERR_INVALID_ARG;
+  if (ckpt_in && !aligned(ckpt_in, 4)) return SSM_ERR_INVALID_ARG;
   const size_t esz = (io == SSM_DTYPE_BF16) ? 2 : 4;
   const void* io_ptrs[12] = {u, delta, B, C, z, dy, du, ddelta, dB, dC, dz, nullptr};
   for (const void* q : io_ptrs)
@@ -463,6 +516,7 @@ ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
   p.seg_R = reinterpret_cast<float*>(ws + w.off_R);
   p.seg_sum = reinterpret_cast<float*>(ws + w.off_sum);
   p.cta_fast = ws + w.off_flags;
+  p.ckpt_in = ckpt_in;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool euler = disc == SSM_DISC_EULER;
   float* dD_out = D ? dD : nullptr;
@@ -471,6 +525,44 @@ ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                                      dC, dA, dD_out, ddelta_bias, s);
   return launch_scan_bwd<float>(p, static_cast<int>(dstate), z != nullptr, euler, vec, dB, dC, dA,
                                 dD_out, ddelta_bias, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_bwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                           ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
+                           int delta_softplus, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* h0, const void* dy,
+                           const float* dh_last, void* du, void* ddelta, float* dA, void* dB,
+                           void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                           void* workspace, size_t workspace_bytes, ssm_discretization disc,
+                           int segments, ssm_stream_t stream) {
+  return scan_bwd_impl(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A, B,
+                       C, D, z, h0, nullptr, dy, dh_last, du, ddelta, dA, dB, dC, dD, dz,
+                       ddelta_bias, dh0, workspace, workspace_bytes, disc, segments, stream);
+}
+
+size_t ssm_scan_bwd_ckpt_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                        int64_t seqlen, int segments) {
+  if (batch < 1 || dim < 1 || dstate < 1 || seqlen < 1 || segments < 0) return kStatusBytes;
+  return bwd_layout(batch, dim, dstate, seqlen, segments, false).total;
+}
+
+ssm_status ssm_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                             ssm_dtype io, const void* u, const void* delta,
+                             const float* delta_bias, int delta_softplus, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* h0, const float* ckpt, const void* dy,
+                             const float* dh_last, void* du, void* ddelta, float* dA, void* dB,
+                             void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                             void* workspace, size_t workspace_bytes, ssm_discretization disc,
+                             int segments, ssm_stream_t stream) {
+  if (!ckpt) return SSM_ERR_INVALID_ARG;
+  return scan_bwd_impl(batch, dim, dstate, seqlen, io, u, delta, delta_bias, delta_softplus, A, B,
+                       C, D, z, h0, ckpt, dy, dh_last, du, ddelta, dA, dB, dC, dD, dz,
+                       ddelta_bias, dh0, workspace, workspace_bytes, disc, segments, stream);
 }
 
 ssm_status ssm_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,

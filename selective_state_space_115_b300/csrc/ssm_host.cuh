@@ -103,6 +103,7 @@ struct ScanCall {
   const float *bias, *A, *D, *h0;
   float* h_last;
   void* y;
+  float* ckpt = nullptr;  // training forward: state checkpoints (else null)
   int softplus;
   bool euler;  // input term dt * B instead of the ZOH form
 };
@@ -192,6 +193,7 @@ inline ScanParams make_params(const ScanCall& c, void* workspace) {
   p.seg_len = static_cast<int>(c.seqlen);
   p.seg_state = nullptr;
   p.seg_sum = nullptr;
+  p.ckpt = c.ckpt;
   return p;
 }
 
@@ -238,6 +240,13 @@ inline size_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, co
          round_up(static_cast<size_t>(pl.nseg) * chans * 4, 256);
 }
 
+// bytes of the training forward's state checkpoints: the state entering every block of
+// ssm::kCkptPos positions, [ceil(seqlen / kCkptPos)][batch * dim][dstate] fp32
+inline size_t ckpt_bytes(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+  return static_cast<size_t>((seqlen + ssm::kCkptPos - 1) / ssm::kCkptPos) *
+         static_cast<size_t>(batch) * static_cast<size_t>(dim) * static_cast<size_t>(dstate) * 4;
+}
+
 // ---------------------------------------------------------------------------
 // scan gradient workspace: [0, 256) status words; the block checkpoints
 // [nblk][batch * dim][N]; the per-CTA dB / dC partials [tiles][batch][2][N][L];
@@ -247,6 +256,8 @@ inline size_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, co
 // CTA [nseg][batch][tiles] saying whether it takes the fast coefficients
 // ---------------------------------------------------------------------------
 constexpr int kBwdThreads = 128;
+static_assert(ssm::kBwdPos == ssm::kCkptPos,
+              "the gradient's blocks are the training forward's checkpoint blocks");
 constexpr int kBwdChannels = kBwdThreads / ssm::kBwdLpc;
 // split sequences until about this many (segment, tile) CTAs per SM: four waves of
 // the four resident CTAs (measured on the long-sequence gradient, B1 D1536 L131072:
@@ -265,8 +276,10 @@ struct BwdLayout {
 // the SMs (fewer than two per SM), split the sequence into about
 // kBwdSegCtasPerSm CTAs per SM, each segment at least kBwdMinSegLen positions, a
 // multiple of the 8-position block.  `segments` > 0 asks for that many (tests).
+// `own_ckpt`: the workspace holds the checkpoints (false when the training forward's
+// are given)
 inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                            int64_t segments = 0) {
+                            int64_t segments = 0, bool own_ckpt = true) {
   BwdLayout w;
   w.nblk = (seqlen + ssm::kBwdPos - 1) / ssm::kBwdPos;
   w.tiles = (dim + kBwdChannels - 1) / kBwdChannels;
@@ -287,7 +300,8 @@ inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t 
   const size_t rows = static_cast<size_t>(batch) * static_cast<size_t>(dim);
   const size_t ns = static_cast<size_t>(w.nseg);
   w.off_ckpt = kStatusBytes;
-  w.off_bc = w.off_ckpt + round_up(static_cast<size_t>(w.nblk) * rows * dstate * 4, 256);
+  w.off_bc = w.off_ckpt +
+             (own_ckpt ? round_up(static_cast<size_t>(w.nblk) * rows * dstate * 4, 256) : 0);
   w.off_a = w.off_bc + round_up(static_cast<size_t>(w.tiles) * batch * 2 * dstate *
                                     static_cast<size_t>(seqlen) * 4, 256);
   w.off_dd = w.off_a + round_up(ns * rows * dstate * 4, 256);

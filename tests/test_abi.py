@@ -330,3 +330,48 @@ def test_host_scan_workspace_size_and_validation():
     bad = list(args)
     bad[5] = None  # no u
     assert lib.ssm_scan_fwd_host(*bad, v(WS), 1 << 30, 0, 0) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_ckpt_sizes():
+    """Training-step checkpoints: one fp32 state per channel every 8 positions; the
+    checkpointed gradient's workspace is the plain one without its own checkpoints."""
+    lib = binding.library()
+    for b, d, n, L in ((8, 5120, 16, 2048), (2, 37, 8, 69), (1, 1, 4, 1), (1, 1536, 16, 131072)):
+        assert lib.ssm_scan_ckpt_bytes(b, d, n, L) == ((L + 7) // 8) * b * d * n * 4
+        rnd = ((L + 7) // 8 * b * d * n * 4 + 255) // 256 * 256
+        assert (lib.ssm_scan_bwd_ckpt_workspace_size(b, d, n, L, 0)
+                == lib.ssm_scan_bwd_ex_workspace_size(b, d, n, L, 0) - rnd), (b, d, n, L)
+    assert lib.ssm_scan_ckpt_bytes(0, 8, 16, 64) == 0
+
+
+def _train_call(lib, ckpt=P + (1 << 24), ckpt_bytes=1 << 20, **kw):
+    a = dict(batch=2, dim=8, dstate=16, seqlen=64, io=1, u=P, delta=P, y=P + 8192, ws=WS,
+             wsb=4096)
+    a.update(kw)
+    v = lambda q: None if q is None else ctypes.c_void_p(q)  # noqa: E731
+    return lib.ssm_scan_fwd_train(a["batch"], a["dim"], a["dstate"], a["seqlen"], a["io"],
+                                  v(a["u"]), v(a["delta"]), None, 1, v(P), v(P), v(P), None,
+                                  None, None, None, v(a["y"]), v(ckpt), ckpt_bytes, v(a["ws"]),
+                                  a["wsb"], 0, 0, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ckpt=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(ckpt=P + (1 << 24) + 4), binding.SSM_ERR_INVALID_ARG),   # not 16-byte aligned
+    (dict(ckpt_bytes=8 * 2 * 8 * 16 * 4 - 4), binding.SSM_ERR_INVALID_ARG),  # one float short
+    (dict(batch=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(u=None), binding.SSM_ERR_INVALID_ARG),
+    (dict(dstate=12), binding.SSM_ERR_UNSUPPORTED),
+])
+def test_train_forward_validation(kw, expect):
+    assert _train_call(binding.library(), **kw) == expect
+
+
+def test_ckpt_gradient_rejects_null_checkpoints():
+    lib = binding.library()
+    v = lambda q: None if q is None else ctypes.c_void_p(q)  # noqa: E731
+    st = lib.ssm_scan_bwd_ckpt(2, 8, 16, 64, 1, v(P), v(P), None, 1, v(P), v(P), v(P), None, None,
+                               None, None, v(P), None, v(P + 4096), v(P + 8192), v(P + 12288),
+                               v(P + 16384), v(P + 20480), None, None, None, None, v(WS),
+                               1 << 30, 0, 0, None)
+    assert st == binding.SSM_ERR_INVALID_ARG
