@@ -497,6 +497,7 @@ def run_gpu(args):
     decode = run_decode(dev, S) if (rank == 0 and not args.no_decode) else None
     conv = run_conv(dev, S) if (rank == 0 and not args.no_decode) else None
     bwd = run_bwd(dev, S) if (rank == 0 and not args.no_decode) else None
+    train = run_train_step(dev, S) if (rank == 0 and not args.no_decode) else None
     euler = None
     if rank == 0 and not args.no_decode:
         # the same scan with the Euler input term (Bbar = dt B)
@@ -557,6 +558,8 @@ def run_gpu(args):
             line["scan_euler"] = euler
         if bwd:
             line["scan_bwd"] = bwd
+        if train:
+            line["train_step"] = train
         line.update(subs)
         if cpu:
             line["cpu_baseline"] = cpu
@@ -726,6 +729,53 @@ def bwd_split(cfg) -> bool:
     """Whether the library splits this gradient's sequence into segments (fewer
     than two 32-channel CTAs per SM, and room for two segments of 256 positions)."""
     return (cfg.batch * ((cfg.dim + 31) // 32) < 2 * SM_COUNT) and cfg.seqlen >= 512
+
+
+def run_train_step(dev, S, iters=10):
+    """A training step of the bench workload through the C ABI: the forward that writes
+    the state checkpoints (ssm_scan_fwd_train) and the gradient that reads them
+    (ssm_scan_bwd_ckpt), each timed with CUDA events, and their sum."""
+    import torch
+    x = W.make_scan_inputs(CFG, seed=0)
+    gr = W.make_scan_grads(CFG, seed=0)
+    u, dl, z = to_dev_io(x["u"], dev), to_dev_io(x["delta"], dev), to_dev_io(x["z"], dev)
+    B, C = to_dev_io(x["B"], dev), to_dev_io(x["C"], dev)
+    dy = to_dev_io(gr["dy"], dev)
+    A = torch.from_numpy(x["A"]).to(dev)
+    Dv = torch.from_numpy(x["D"]).to(dev)
+    bias = torch.from_numpy(x["delta_bias"]).to(dev)
+    ck = torch.empty(S.ckpt_shape(CFG.batch, CFG.dim, CFG.dstate, CFG.seqlen),
+                     dtype=torch.float32, device=dev)
+    y = torch.empty_like(u)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        S.scan_fwd(u, dl, A, B, C, D=Dv, z=z, delta_bias=bias, out=y, ckpt=ck)
+
+    def bwd():
+        return S.scan_bwd(u, dl, A, B, C, dy, D=Dv, z=z, delta_bias=bias, ckpt=ck)
+
+    out = {}
+    for name, fn in (("forward_ms", fwd), ("gradient_ms", bwd)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / iters
+    ms = out["forward_ms"] + out["gradient_ms"]
+    ck_mb = ck.numel() * 4 / 1e6
+    return {"workload": f"training step of the {CFG.name} scan: forward writing the state "
+                        f"entering every 8 positions ({ck_mb:.0f} MB), gradient from them",
+            **out, "ms_per_step": ms, "value": CFG.elements / (ms * 1e-3),
+            "unit": "elements/s",
+            "gpu_launches": iters * (1 + ((1 if CFG.io == W.BF16 else 0)
+                                          + (2 if CFG.io == W.BF16 else 1)
+                                          * (2 if bwd_split(CFG) else 1) + 2))}
 
 
 def run_bwd(dev, S, iters=20):
