@@ -123,11 +123,17 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
       const float q = s * a0;
       const float ahw = ex2(q);
       const float em1 = exp2m1_accurate(q, ahw);
-      const float abar = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
-      // (Abar - 1) / A, or dt at A == 0; 1/A from the hardware reciprocal (a few
-      // ulp, far below the series' truncation)
-      const float coef = (Cfg::EULER || a0 == 0.0f) ? s * kLn2 : em1 * rcp(a0);
-      const float hn = fmaf(abar, hv[4 * k + i], coef * (Bv[i] * uv));
+      float hn;
+      if constexpr (Cfg::EULER) {
+        const float abar = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
+        hn = fmaf(abar, hv[4 * k + i], (s * kLn2) * (Bv[i] * uv));
+      } else {
+        // h + coef (A h + B u) = Abar h + coef B u with coef = (Abar - 1) / A (dt at
+        // A == 0, where the bracket is B u); 1/A from the hardware reciprocal
+        const float coef = (a0 == 0.0f) ? s * kLn2 : em1 * rcp(a0);
+        const float hh = hv[4 * k + i];
+        hn = fmaf(coef, fmaf(a0, hh, Bv[i] * uv), hh);
+      }
       hv[4 * k + i] = hn;
       if (i & 1)
         acc1 = fmaf(Cv[i], hn, acc1);
