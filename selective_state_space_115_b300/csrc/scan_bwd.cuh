@@ -128,14 +128,24 @@ __device__ __forceinline__ float ex2_fresh(float x) {
 // log2(e): the difference (dt Abar - coef) / A cancels for small |q|, where the
 // Taylor series dt^2 (1/2 + x/3 + x^2/8 + x^3/30 + x^4/144) (x = dt A) is used
 // instead (truncation below 2e-8 relative for |q| < 1/8); at A = 0 it gives the
-// limit dt^2 / 2.
+// limit dt^2 / 2.  SHORT (the fast coefficients of bf16 io) keeps three terms,
+// written in q: truncation below (x^3 / 30) / (1/2) < 4.4e-5 relative for |q| < 1/8,
+// under the direct form's own error there (its coefficient carries the hardware
+// ex2's ~2^-22, which the cancellation raises to ~2^-21 / x^2 = 6e-5).
+template <bool SHORT>
 __device__ __forceinline__ float dcoef_dA(float dt, float q, float ra, float abar, float coef) {
-  const float x = q * kLn2;
-  float ps = fmaf(x, 1.0f / 144.0f, 1.0f / 30.0f);
-  ps = fmaf(ps, x, 0.125f);
-  ps = fmaf(ps, x, 1.0f / 3.0f);
-  ps = fmaf(ps, x, 0.5f);
-  const float series = dt * dt * ps;
+  float ps;
+  if constexpr (SHORT) {
+    // 1/2 + (ln2 / 3) q + (ln2^2 / 8) q^2
+    ps = fmaf(fmaf(q, 0.06005662673977513f, 0.23104906018664842f), q, 0.5f);
+  } else {
+    const float x = q * kLn2;
+    ps = fmaf(x, 1.0f / 144.0f, 1.0f / 30.0f);
+    ps = fmaf(ps, x, 0.125f);
+    ps = fmaf(ps, x, 1.0f / 3.0f);
+    ps = fmaf(ps, x, 0.5f);
+  }
+  const float series = (dt * dt) * ps;
   const float direct = fmaf(dt, abar, -coef) * ra;
   return (fabsf(q) < kExpm1SeriesMaxQ) ? series : direct;
 }
@@ -465,7 +475,7 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
           // (dt Abar - coef) / A cancels like dt^2 while its rounding and the
           // hardware ex2's error stay ~2^-24 |B u / A|, so at small |dt A| it would be
           // lost (its relative error grows like 2^-23 / (dt A)^2)
-          dA2[k] = fmaf(gk * dcoef_dA(dt, q, ra[k], ab, coef), bu, dA2[k]);
+          dA2[k] = fmaf(gk * dcoef_dA<FAST>(dt, q, ra[k], ab, coef), bu, dA2[k]);
         }
         g[k] = gk;
         an[k] = ab;
