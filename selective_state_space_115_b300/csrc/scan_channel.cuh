@@ -372,7 +372,7 @@ __device__ __forceinline__ void chan_positions(const float* bcfB, const float* b
 // argument whose step gives a state update with |dt A log2 e| = kFastPathMinQ)
 // takes the accurate update, the rest the fast one.
 // ---------------------------------------------------------------------------
-template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG>
+template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG, bool CKPT>
 __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile, const float* bcfB,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
@@ -390,7 +390,7 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
   for (int blk = 0; blk < Cfg::NBLK; ++blk) {
     const uint32_t off = swz<RB>(row, blk);
     // training forward: the state entering this block, when it starts a checkpoint block
-    if (ck) {
+    if (CKPT && ck) {
       const int l = l0 + blk * TB;
       if (l % kCkptPos == 0 && l < seqlen) {
         float* dst = ck + static_cast<int64_t>(l / kCkptPos) * ck_stride;
@@ -475,7 +475,9 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 // One CTA's work: channels d0 .. d0 + DT - 1 of batch row b over segment `seg`
 // (the whole sequence when nseg == 1).  `maps` must live in kernel parameter
 // space (a __grid_constant__ argument): TMA reads the descriptors from there.
-template <typename IO, typename Cfg, int MODE>
+// CKPT: the training forward, writing the state entering every kCkptPos positions to
+// p.ckpt (compiled apart, so that the plain forward carries none of it)
+template <typename IO, typename Cfg, int MODE, bool CKPT>
 __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanParams& p, int b,
                                              int d0, int seg, uint8_t* smem_raw) {
   constexpr int N = Cfg::N, NS = Cfg::NS, S = Cfg::S, LC = Cfg::LC;
@@ -503,7 +505,8 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
   const int64_t state0 = (static_cast<int64_t>(b) * p.dim + d) * N + part * NS;
   // this lane's checkpoint slot (pass 1 of the segmented scan runs from a zero state:
   // it writes none)
-  float* const ck = (MODE != kModeStates && valid && p.ckpt) ? p.ckpt + state0 : nullptr;
+  static_assert(!(CKPT && MODE == kModeStates), "the states pass writes no checkpoints");
+  float* const ck = (CKPT && valid) ? p.ckpt + state0 : nullptr;
   const int64_t ck_stride = static_cast<int64_t>(p.batch) * p.dim * N;
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
@@ -638,9 +641,9 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
     const bool tail = l0 + LC > p.seqlen;
     // (the group flags are warp-uniform: every lane of a warp takes the same branch)
 #define SSM_CHAN_CHUNK(ACC, TAIL, NEG)                                                        \
-  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG>(st, ytile, bcfB, bcfC, xch, row, part, lane, l0,   \
-                                            p.seqlen, Areg, nIA, Dd, bias2, p.softplus, x2_min, \
-                                            h, ssum, ck, ck_stride)
+  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG, CKPT>(st, ytile, bcfB, bcfC, xch, row, part, lane,  \
+                                                  l0, p.seqlen, Areg, nIA, Dd, bias2,           \
+                                                  p.softplus, x2_min, h, ssum, ck, ck_stride)
     bool fast_chunk = false;
     if constexpr (sizeof(IO) == 2) fast_chunk = !accurate;
     if (fast_chunk) {
@@ -686,13 +689,13 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
   }
 }
 
-template <typename IO, typename Cfg, int MODE>
+template <typename IO, typename Cfg, int MODE, bool CKPT = false>
 __global__ void __launch_bounds__(Cfg::THREADS)
     scan_channel_kernel(const __grid_constant__ ChanMaps maps, const ScanParams p) {
   extern __shared__ uint8_t smem_raw[];
   // block index = (segment * batch + b) * dtiles + channel tile
   const int rest = blockIdx.x / p.dtiles;
-  channel_body<IO, Cfg, MODE>(maps, p, rest % p.batch, (blockIdx.x % p.dtiles) * Cfg::DT,
+  channel_body<IO, Cfg, MODE, CKPT>(maps, p, rest % p.batch, (blockIdx.x % p.dtiles) * Cfg::DT,
                               rest / p.batch, smem_raw);
 }
 
@@ -719,7 +722,7 @@ struct MixSched {
   unsigned max_sm_slots;  // SM ids with an arrival counter
 };
 
-template <typename IO, typename CfgA, typename CfgB>
+template <typename IO, typename CfgA, typename CfgB, bool CKPT = false>
 __global__ void __launch_bounds__(CfgA::THREADS)
     scan_channel_mixed_kernel(const __grid_constant__ ChanMaps mapsA,
                               const __grid_constant__ ChanMaps mapsB, const ScanParams p,
@@ -752,12 +755,13 @@ __global__ void __launch_bounds__(CfgA::THREADS)
   __syncthreads();
   const int role = role_unit[0], unit = role_unit[1];
   if (role == 0) {
-    channel_body<IO, CfgA, kModeFull>(mapsA, p, unit / m.dtiles128, (unit % m.dtiles128) * 128,
-                                      0, smem_raw);
+    channel_body<IO, CfgA, kModeFull, CKPT>(mapsA, p, unit / m.dtiles128,
+                                            (unit % m.dtiles128) * 128, 0, smem_raw);
   } else if (role == 1) {
     const int tile = m.n_tiles + unit / 4;
     const int d0 = (tile % m.dtiles128) * 128 + (unit % 4) * 32;
-    if (d0 < p.dim) channel_body<IO, CfgB, kModeFull>(mapsB, p, tile / m.dtiles128, d0, 0, smem_raw);
+    if (d0 < p.dim)
+      channel_body<IO, CfgB, kModeFull, CKPT>(mapsB, p, tile / m.dtiles128, d0, 0, smem_raw);
   }
 }
 

@@ -156,7 +156,7 @@ __device__ __forceinline__ void chunk_stage_bc(const ScanParams& p, int b, int k
 // The per-state loop of one chunk for the warp that owns the channel: pairs, warp
 // scan, carry and replay with y += C h.  AR: kArFast (1 - Abar) B u / -A, kArNeg the
 // accurate coefficient for negative A, kArGen the accurate one for any A.
-template <typename IO, typename Cfg, int AR>
+template <typename IO, typename Cfg, int AR, bool CKPT>
 __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const IO* tile,
                                              const float* s, const float* u, float* y,
                                              float* carry, float* ck, int64_t ck_stride,
@@ -249,13 +249,13 @@ __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const 
     // training forward: the states entering this lane's checkpoint blocks (its first
     // position, and position 8 of 16); a lane's row of a checkpoint is written state by
     // state and merges in L2
-    if (ck && l < seqlen) ck[(l / kCkptPos) * ck_stride + n] = hs;
+    if (CKPT && l < seqlen) ck[(l / kCkptPos) * ck_stride + n] = hs;
 #pragma unroll
     for (int i = 0; i < T; ++i) {
       hs = fmaf(a[i], hs, bb[i]);
       y[i] = fmaf(Cv[i], hs, y[i]);
       if constexpr (T > kCkptPos) {
-        if (i % kCkptPos == kCkptPos - 1 && i + 1 < T && ck && l + i + 1 < seqlen)
+        if (CKPT && i % kCkptPos == kCkptPos - 1 && i + 1 < T && l + i + 1 < seqlen)
           ck[((l + i + 1) / kCkptPos) * ck_stride + n] = hs;
       }
     }
@@ -267,7 +267,7 @@ __device__ __forceinline__ void chunk_states(const float* Arow, int lane, const 
 // it; `tile` holds the chunk's B and C.  ACC: accurate arithmetic throughout (fp32
 // io, or small |A|); otherwise a chunk holding a step with |q| = s |A| below
 // kFastPathMinQ (s_min = kFastPathMinQ / min |A|) takes the accurate update.
-template <typename IO, typename Cfg, bool ACC>
+template <typename IO, typename Cfg, bool ACC, bool CKPT>
 __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d, int lane, int k,
                                               const IO* tile, float* carry, float s_min,
                                               bool neg) {
@@ -295,21 +295,21 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
     slow |= in && !(sv >= s_min);
     y[i] = 0.0f;
   }
-  float* const ck = p.ckpt ? p.ckpt + row * Cfg::N : nullptr;
+  float* const ck = CKPT ? p.ckpt + row * Cfg::N : nullptr;
   const int64_t ck_stride = static_cast<int64_t>(p.batch) * p.dim * Cfg::N;
   if constexpr (Cfg::EULER) {
     // (the Euler input term dt B u has no cancellation at small steps)
-    chunk_states<IO, Cfg, ACC ? kArGen : kArFast>(Arow, lane, tile, s, u, y, carry, ck,
+    chunk_states<IO, Cfg, ACC ? kArGen : kArFast, CKPT>(Arow, lane, tile, s, u, y, carry, ck,
                                                   ck_stride, l, p.seqlen);
   } else {
     if (!ACC && !__any_sync(0xffffffffu, slow))
-      chunk_states<IO, Cfg, kArFast>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
+      chunk_states<IO, Cfg, kArFast, CKPT>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
                                      p.seqlen);
     else if (neg)
-      chunk_states<IO, Cfg, kArNeg>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
+      chunk_states<IO, Cfg, kArNeg, CKPT>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
                                     p.seqlen);
     else
-      chunk_states<IO, Cfg, kArGen>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
+      chunk_states<IO, Cfg, kArGen, CKPT>(Arow, lane, tile, s, u, y, carry, ck, ck_stride, l,
                                     p.seqlen);
   }
   float z[T];
@@ -326,7 +326,8 @@ __device__ __forceinline__ void chunk_channel(const ScanParams& p, int b, int d,
 
 // Grid: x = batch row * ceil(dim / WARPS) + channel group; warp w of a CTA owns
 // channel group * WARPS + w of that batch row (warps past dim only stage).
-template <typename IO, typename Cfg>
+// CKPT: the training forward (state checkpoints to p.ckpt), compiled apart
+template <typename IO, typename Cfg, bool CKPT = false>
 __global__ void __launch_bounds__(Cfg::THREADS) scan_chunk_kernel(const ScanParams p) {
   extern __shared__ __align__(16) unsigned char chunk_smem[];
   __shared__ float carry_smem[Cfg::WARPS][Cfg::N];
@@ -377,9 +378,9 @@ __global__ void __launch_bounds__(Cfg::THREADS) scan_chunk_kernel(const ScanPara
     }
     if (active) {
       if (acc)
-        chunk_channel<IO, Cfg, true>(p, b, d, lane, k, cur, carry, s_min, neg);
+        chunk_channel<IO, Cfg, true, CKPT>(p, b, d, lane, k, cur, carry, s_min, neg);
       else
-        chunk_channel<IO, Cfg, false>(p, b, d, lane, k, cur, carry, s_min, neg);
+        chunk_channel<IO, Cfg, false, CKPT>(p, b, d, lane, k, cur, carry, s_min, neg);
     }
   }
   if (active && p.h_last && lane < N) p.h_last[row * N + lane] = carry[lane];

@@ -43,7 +43,8 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
       p.seg_sum = reinterpret_cast<float*>(
           base + kStatusBytes + round_up(static_cast<size_t>(seg.nseg) * chans * N * 4, 256));
       auto k1 = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeStates>;
-      auto k2 = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeCarry>;
+      auto k2 = p.ckpt ? ssm::scan_channel_kernel<IO, Cfg, ssm::kModeCarry, true>
+                       : ssm::scan_channel_kernel<IO, Cfg, ssm::kModeCarry, false>;
       cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            Cfg::SMEM_ALLOC);
       if (e == cudaSuccess)
@@ -60,7 +61,8 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
       return SSM_OK;
     }
   }
-  auto kern = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeFull>;
+  auto kern = p.ckpt ? ssm::scan_channel_kernel<IO, Cfg, ssm::kModeFull, true>
+                     : ssm::scan_channel_kernel<IO, Cfg, ssm::kModeFull, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel)");
@@ -107,7 +109,8 @@ ssm_status launch_mixed(const ScanCall& c, void* workspace, cudaStream_t stream,
   cudaError_t e = cudaMemsetAsync(sched.counters, 0, kMixCounterBytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scheduler counters)");
   constexpr int smem = CfgA::SMEM_ALLOC > CfgB::SMEM_ALLOC ? CfgA::SMEM_ALLOC : CfgB::SMEM_ALLOC;
-  auto kern = ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB>;
+  auto kern = p.ckpt ? ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, true>
+                     : ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel_mixed)");
   const unsigned grid = static_cast<unsigned>(m.n_tiles + m.n_quarters);
@@ -124,7 +127,8 @@ ssm_status launch_chunk(const ScanCall& c, void* workspace, cudaStream_t stream)
   // one CTA per (batch row, group of WARPS channels)
   const int64_t grid64 = c.batch * ((c.dim + Cfg::WARPS - 1) / Cfg::WARPS);
   if (grid64 > INT32_MAX) return SSM_ERR_INVALID_ARG;
-  auto kern = ssm::scan_chunk_kernel<IO, Cfg>;
+  auto kern =
+      p.ckpt ? ssm::scan_chunk_kernel<IO, Cfg, true> : ssm::scan_chunk_kernel<IO, Cfg, false>;
   // per call: the attribute belongs to the current device's context
   const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
