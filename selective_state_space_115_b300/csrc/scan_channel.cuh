@@ -23,7 +23,9 @@
 //     are bounded in time and record a status bit on timeout;
 //   * once per chunk the CTA re-lays B, C out as fp32 [position][state], so a
 //     lane reads four states of one position with one 16-byte broadcast load;
-//   * y goes through a swizzled output tile that one thread stores by TMA.
+//   * each lane stores its finished positions of y straight to global memory (16
+//     bytes per block of positions at one lane per channel): no output tile, so
+//     the CTA's shared memory holds the input ring alone.
 //
 // Discretisation (velog review, section 2 "Discretization"; "mamba 学习",
 // section "MAMBA"): Abar = 2^(s A) with s = dt log2(e) (softplus evaluated in
@@ -110,9 +112,8 @@ struct ChanCfg {
   static constexpr int BCT = pad(N * RB);          // one [N x LC] swizzled tile
   static constexpr int STAGE = NARR * TILE + 2 * BCT;
   static constexpr int OFF_STAGES = 0;
-  static constexpr int OFF_Y = OFF_STAGES + S * STAGE;          // 2 output tiles
   static constexpr int BCF = LC * N * 4;                        // fp32 [LC][N]
-  static constexpr int OFF_BCF = OFF_Y + 2 * TILE;              // [2 buf][B, C]
+  static constexpr int OFF_BCF = OFF_STAGES + S * STAGE;        // [2 buf][B, C]
   // per-warp exchange buffers (LPC > 1): step sizes [32 lanes][PB] and partial
   // contractions [LPC parts][32 lanes][PB]
   static constexpr int XCH_S = 32 * PB;                         // floats
@@ -126,7 +127,7 @@ struct ChanCfg {
 };
 
 struct ChanMaps {
-  CUtensorMap u, delta, z, y, B, C;
+  CUtensorMap u, delta, z, B, C;
 };
 
 // Byte offset of 16-byte granule c of row r in a tile of RB-byte rows written by
@@ -172,9 +173,9 @@ __device__ __forceinline__ void lds_vals(const uint8_t* p, float* out) {
   }
 }
 
-// round K values to io and store them (K * size bytes) to shared memory
+// round K values to io and store them (K * size bytes, naturally aligned)
 template <typename IO, int K>
-__device__ __forceinline__ void sts_vals(uint8_t* p, const float* v) {
+__device__ __forceinline__ void st_vals(void* p, const float* v) {
   constexpr int BYTES = K * sizeof(IO);
   uint32_t w[(BYTES + 3) / 4];
   if constexpr (sizeof(IO) == 2) {
@@ -372,8 +373,9 @@ __device__ __forceinline__ void chan_positions(const float* bcfB, const float* b
 // argument whose step gives a state update with |dt A log2 e| = kFastPathMinQ)
 // takes the accurate update, the rest the fast one.
 // ---------------------------------------------------------------------------
+// `yrow`: this lane's channel's row of y (null: no output, or a channel past dim).
 template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG, bool CKPT>
-__device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile, const float* bcfB,
+__device__ __forceinline__ void chan_chunk(const uint8_t* stage, IO* yrow, const float* bcfB,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
                                            const float* nIA, float Dd, float bias2, int softplus,
@@ -465,7 +467,10 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, uint8_t* ytile,
 #pragma unroll
       for (int k = 0; k < PB; ++k) ym[k] *= (ACC ? silu_accurate(zm[k]) : silu_fast(zm[k]));
     }
-    sts_vals<IO, PB>(ytile + off + pofs, ym);
+    // (the row length is a multiple of the block, as the TMA row pitch requires, so a
+    // block lies wholly inside the sequence or wholly past it)
+    const int lb = l0 + blk * TB;
+    if (yrow != nullptr && (!TAIL || lb < seqlen)) st_vals<IO, PB>(yrow + lb + part * PB, ym);
   }
 }
 
@@ -507,6 +512,9 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
   // it writes none)
   static_assert(!(CKPT && MODE == kModeStates), "the states pass writes no checkpoints");
   float* const ck = (CKPT && valid) ? p.ckpt + state0 : nullptr;
+  IO* const yrow = (OUT && valid)
+                       ? static_cast<IO*>(p.y) + (static_cast<int64_t>(b) * p.dim + d) * p.seqlen
+                       : nullptr;
   const int64_t ck_stride = static_cast<int64_t>(p.batch) * p.dim * N;
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
@@ -572,7 +580,6 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
     prefetch_tmap(&maps.delta);
     prefetch_tmap(&maps.B);
     prefetch_tmap(&maps.C);
-    prefetch_tmap(&maps.y);
     if (Cfg::GATE) prefetch_tmap(&maps.z);
   }
   __syncthreads();
@@ -616,32 +623,23 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
         for (int e = 0; e < Cfg::TB; ++e) dst[e * N] = v[e];
       }
     }
-    if (OUT && tid == 0 && k >= 2) tma_store_wait_read<0>();  // chunk k-2's store read its tile
     if (__syncthreads_or(!arrived)) {
       ok = false;
       break;
     }
-    if (tid == 0 && k >= 1) {
-      if (OUT) {
-        tma_store_3d(&maps.y, smem + Cfg::OFF_Y + ((k - 1) & 1) * Cfg::TILE,
-                     l_begin + (k - 1) * LC, d0, b);
-        tma_store_commit();
-      }
-      if (k - 1 + S < nchunks) {
-        fence_proxy_async_smem();
-        issue_loads(k - 1 + S);  // stage of chunk k-1 is free: every thread passed the barrier
-        ++issued;
-      }
+    if (tid == 0 && k >= 1 && k - 1 + S < nchunks) {
+      fence_proxy_async_smem();
+      issue_loads(k - 1 + S);  // stage of chunk k-1 is free: every thread passed the barrier
+      ++issued;
     }
     const float* bcfB =
         reinterpret_cast<const float*>(smem + Cfg::OFF_BCF + (k & 1) * 2 * Cfg::BCF);
     const float* bcfC = bcfB + Cfg::BCF / 4;
-    uint8_t* ytile = smem + Cfg::OFF_Y + (k & 1) * Cfg::TILE;
     const int l0 = l_begin + k * LC;
     const bool tail = l0 + LC > p.seqlen;
     // (the group flags are warp-uniform: every lane of a warp takes the same branch)
 #define SSM_CHAN_CHUNK(ACC, TAIL, NEG)                                                        \
-  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG, CKPT>(st, ytile, bcfB, bcfC, xch, row, part, lane,  \
+  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG, CKPT>(st, yrow, bcfB, bcfC, xch, row, part, lane,   \
                                                   l0, p.seqlen, Areg, nIA, Dd, bias2,           \
                                                   p.softplus, x2_min, h, ssum, ck, ck_stride)
     bool fast_chunk = false;
@@ -658,16 +656,9 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
       if (neg) SSM_CHAN_CHUNK(true, true, true); else SSM_CHAN_CHUNK(true, true, false);
     }
 #undef SSM_CHAN_CHUNK
-    fence_proxy_async_smem();  // y tile writes -> visible to the TMA store
   }
   __syncthreads();
   if (tid == 0) {
-    if (OUT && ok && nchunks > 0) {
-      tma_store_3d(&maps.y, smem + Cfg::OFF_Y + ((nchunks - 1) & 1) * Cfg::TILE,
-                   l_begin + (nchunks - 1) * LC, d0, b);
-      tma_store_commit();
-    }
-    tma_store_wait_all<0>();
     if (!ok) {
       // a wait gave up at chunk k: before the CTA exits, wait (bounded) for every
       // load that may still be in flight into the ring (chunks k .. issued-1)

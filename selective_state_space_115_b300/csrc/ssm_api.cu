@@ -232,7 +232,7 @@ ssm_status scan_fwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seq
   ssm_status st = validate_scan(c, workspace, workspace_bytes);
   if (st != SSM_OK) return st;
 
-  const int lc = c.bf16 ? 16 : 8;  // channel kernel chunk (32-byte rows)
+  const int lc = ChanShape<1>::RB / (c.bf16 ? 2 : 4);  // channel kernel chunk (positions)
   SegPlan seg;
   if (algo == SSM_ALGO_SEGMENTED) {
     seg = seg_plan(c.batch, c.dim, c.seqlen, lc, true);

@@ -322,13 +322,16 @@ inline BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t dstate, int64_t 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-// Channel-kernel shapes: 32-byte chunk rows (16 bf16 / 8 fp32 positions) and a
-// 4-stage ring.  Per 4-warp CTA (bf16, dstate 16, gate): ~66 KB of shared memory
-// and ~107 registers a thread at 1 lane per channel (3 CTAs per SM), ~37 KB and
-// ~80 at 2 (6 per SM), ~22 KB and ~56 at 4 (9 per SM).
+// Channel-kernel shapes: 64-byte chunk rows (32 bf16 / 16 fp32 positions) in a
+// 2-stage ring.  A CTA meets its warps at a barrier once per chunk: 64-byte rows
+// halve those meetings against 32-byte ones (measured on B300, one-lane CTAs of
+// the 2.8B-like layer's arithmetic at 2 warps per SM sub-partition: 481 -> 446 us),
+// and two stages of them keep as many positions in flight as four of 32 bytes.
+// Per 4-warp CTA (bf16, dstate 16, gate): ~61 KB of shared memory at 1 lane per
+// channel (3 CTAs per SM), less at 2 and 4.
 template <int LPC>
 struct ChanShape {
-  static constexpr int S = 4, RB = 32;
+  static constexpr int S = 2, RB = 64;
 };
 
 // Lanes per channel for the channel kernel.  Every SM sub-partition runs one warp

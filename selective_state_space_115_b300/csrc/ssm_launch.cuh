@@ -20,7 +20,6 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
   const uint64_t L = c.seqlen, Dm = c.dim, Bt = c.batch, Nn = N;
   if (!make_map(&maps.u, c.u, bf, L, Dm, Bt, Cfg::LC, Cfg::DT) ||
       !make_map(&maps.delta, c.delta, bf, L, Dm, Bt, Cfg::LC, Cfg::DT) ||
-      !make_map(&maps.y, c.y, bf, L, Dm, Bt, Cfg::LC, Cfg::DT) ||
       !make_map(&maps.B, c.B, bf, L, Nn, Bt, Cfg::LC, N) ||
       !make_map(&maps.C, c.C, bf, L, Nn, Bt, Cfg::LC, N) ||
       (GATE && !make_map(&maps.z, c.z, bf, L, Dm, Bt, Cfg::LC, Cfg::DT))) {
@@ -89,7 +88,6 @@ ssm_status launch_mixed(const ScanCall& c, void* workspace, cudaStream_t stream,
     const uint32_t rows = r ? CfgB::DT : CfgA::DT;
     ok = make_map(&mp.u, c.u, bf, L, Dm, Bt, CfgA::LC, rows) &&
          make_map(&mp.delta, c.delta, bf, L, Dm, Bt, CfgA::LC, rows) &&
-         make_map(&mp.y, c.y, bf, L, Dm, Bt, CfgA::LC, rows) &&
          make_map(&mp.B, c.B, bf, L, Nn, Bt, CfgA::LC, 16) &&
          make_map(&mp.C, c.C, bf, L, Nn, Bt, CfgA::LC, 16) &&
          (!GATE || make_map(&mp.z, c.z, bf, L, Dm, Bt, CfgA::LC, rows));
