@@ -270,6 +270,14 @@ SSM_API ssm_status ssm_state_update_ex(int64_t batch, int64_t dim, int64_t dstat
  * a fixed order: results are bit-reproducible for a given shape.  Arithmetic is
  * fp32; bf16 outputs are rounded to nearest even.  Validated on the host first
  * (nothing is enqueued when a check fails); enqueued on `stream`.
+ *
+ * The state checkpoints (every 8 positions, in the workspace) come from the
+ * forward's own kernels in a checkpoint-only pass (no output, neither C nor z read)
+ * when AUTO would run the forward on its channel kernel, mixed split or segmented
+ * plan (with `segments` 0), else from a forward pass of the gradient kernel; the
+ * gradient is then bit for bit the one ssm_scan_bwd_ckpt returns from the
+ * checkpoints of a training forward that ran AUTO's plan.  That pass records its wait
+ * timeouts in the workspace's first 16 bytes, which ssm_read_device_status reads.
  */
 SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
                                            int64_t seqlen);
@@ -388,8 +396,9 @@ SSM_API ssm_status ssm_conv1d_update(int64_t batch, int64_t dim, int64_t width, 
 
 /*
  * Synchronises `stream`, then reads the status words of `workspace` (as filled
- * by the last ssm_scan_fwd that used it).  Returns SSM_OK, SSM_ERR_DEVICE_TIMEOUT,
- * or SSM_ERR_CUDA if the synchronisation or the copy failed.
+ * by the last ssm_scan_fwd, or ssm_scan_bwd's checkpoint pass, that used it).
+ * Returns SSM_OK, SSM_ERR_DEVICE_TIMEOUT, or SSM_ERR_CUDA if the synchronisation or
+ * the copy failed.
  */
 SSM_API ssm_status ssm_read_device_status(const void* workspace, ssm_stream_t stream);
 

@@ -374,14 +374,14 @@ __device__ __forceinline__ void chan_positions(const float* bcfB, const float* b
 // takes the accurate update, the rest the fast one.
 // ---------------------------------------------------------------------------
 // `yrow`: this lane's channel's row of y (null: no output, or a channel past dim).
-template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG, bool CKPT>
+template <typename Cfg, typename IO, int MODE, bool ACC, bool TAIL, bool NEG, bool CKPT, bool Y>
 __device__ __forceinline__ void chan_chunk(const uint8_t* stage, IO* yrow, const float* bcfB,
                                            const float* bcfC, float* xch, int row, int part,
                                            int lane, int l0, int seqlen, const float* Areg,
                                            const float* nIA, float Dd, float bias2, int softplus,
                                            float x2_min, float* h, float& ssum, float* ck,
                                            int64_t ck_stride) {
-  constexpr bool OUT = MODE != kModeStates;  // this pass writes y
+  constexpr bool OUT = MODE != kModeStates && Y;  // this pass writes y
   constexpr int LPC = Cfg::LPC, TB = Cfg::TB, PB = Cfg::PB, RB = Cfg::RB;
   const uint8_t* tu = stage;
   const uint8_t* td = stage + Cfg::TILE;
@@ -427,7 +427,7 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, IO* yrow, const
       if constexpr (LPC >= 2) x2min = fminf(x2min, __shfl_xor_sync(0xffffffffu, x2min, 1));
       if constexpr (LPC >= 4) x2min = fminf(x2min, __shfl_xor_sync(0xffffffffu, x2min, 2));
     }
-    if constexpr (!OUT) {
+    if constexpr (MODE == kModeStates) {
 #pragma unroll
       for (int j = 0; j < TB; ++j) ssum += sj[j];
     }
@@ -481,13 +481,15 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, IO* yrow, const
 // (the whole sequence when nseg == 1).  `maps` must live in kernel parameter
 // space (a __grid_constant__ argument): TMA reads the descriptors from there.
 // CKPT: the training forward, writing the state entering every kCkptPos positions to
-// p.ckpt (compiled apart, so that the plain forward carries none of it)
-template <typename IO, typename Cfg, int MODE, bool CKPT>
+// p.ckpt (compiled apart, so that the plain forward carries none of it); Y: the pass
+// writes y (a checkpoint-only pass reads neither C nor z and writes no output)
+template <typename IO, typename Cfg, int MODE, bool CKPT, bool Y>
 __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanParams& p, int b,
                                              int d0, int seg, uint8_t* smem_raw) {
   constexpr int N = Cfg::N, NS = Cfg::NS, S = Cfg::S, LC = Cfg::LC;
-  constexpr bool OUT = MODE != kModeStates;
-  // bytes one chunk brings in: pass 1 needs u, delta and B only
+  constexpr bool OUT = MODE != kModeStates && Y;
+  static_assert(Y || CKPT, "a pass writes y, checkpoints or both");
+  // bytes one chunk brings in: a pass without output needs u, delta and B only
   constexpr uint32_t TX = OUT ? Cfg::TX_BYTES : 2 * Cfg::DT * Cfg::RB + N * Cfg::RB;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + Cfg::ALIGN - 1) &
@@ -639,9 +641,9 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
     const bool tail = l0 + LC > p.seqlen;
     // (the group flags are warp-uniform: every lane of a warp takes the same branch)
 #define SSM_CHAN_CHUNK(ACC, TAIL, NEG)                                                        \
-  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG, CKPT>(st, yrow, bcfB, bcfC, xch, row, part, lane,   \
-                                                  l0, p.seqlen, Areg, nIA, Dd, bias2,           \
-                                                  p.softplus, x2_min, h, ssum, ck, ck_stride)
+  chan_chunk<Cfg, IO, MODE, ACC, TAIL, NEG, CKPT, Y>(st, yrow, bcfB, bcfC, xch, row, part, lane, \
+                                                     l0, p.seqlen, Areg, nIA, Dd, bias2,        \
+                                                     p.softplus, x2_min, h, ssum, ck, ck_stride)
     bool fast_chunk = false;
     if constexpr (sizeof(IO) == 2) fast_chunk = !accurate;
     if (fast_chunk) {
@@ -680,13 +682,13 @@ __device__ __forceinline__ void channel_body(const ChanMaps& maps, const ScanPar
   }
 }
 
-template <typename IO, typename Cfg, int MODE, bool CKPT = false>
+template <typename IO, typename Cfg, int MODE, bool CKPT = false, bool Y = true>
 __global__ void __launch_bounds__(Cfg::THREADS)
     scan_channel_kernel(const __grid_constant__ ChanMaps maps, const ScanParams p) {
   extern __shared__ uint8_t smem_raw[];
   // block index = (segment * batch + b) * dtiles + channel tile
   const int rest = blockIdx.x / p.dtiles;
-  channel_body<IO, Cfg, MODE, CKPT>(maps, p, rest % p.batch, (blockIdx.x % p.dtiles) * Cfg::DT,
+  channel_body<IO, Cfg, MODE, CKPT, Y>(maps, p, rest % p.batch, (blockIdx.x % p.dtiles) * Cfg::DT,
                               rest / p.batch, smem_raw);
 }
 
@@ -713,7 +715,7 @@ struct MixSched {
   unsigned max_sm_slots;  // SM ids with an arrival counter
 };
 
-template <typename IO, typename CfgA, typename CfgB, bool CKPT = false>
+template <typename IO, typename CfgA, typename CfgB, bool CKPT = false, bool Y = true>
 __global__ void __launch_bounds__(CfgA::THREADS)
     scan_channel_mixed_kernel(const __grid_constant__ ChanMaps mapsA,
                               const __grid_constant__ ChanMaps mapsB, const ScanParams p,
@@ -746,13 +748,13 @@ __global__ void __launch_bounds__(CfgA::THREADS)
   __syncthreads();
   const int role = role_unit[0], unit = role_unit[1];
   if (role == 0) {
-    channel_body<IO, CfgA, kModeFull, CKPT>(mapsA, p, unit / m.dtiles128,
-                                            (unit % m.dtiles128) * 128, 0, smem_raw);
+    channel_body<IO, CfgA, kModeFull, CKPT, Y>(mapsA, p, unit / m.dtiles128,
+                                               (unit % m.dtiles128) * 128, 0, smem_raw);
   } else if (role == 1) {
     const int tile = m.n_tiles + unit / 4;
     const int d0 = (tile % m.dtiles128) * 128 + (unit % 4) * 32;
     if (d0 < p.dim)
-      channel_body<IO, CfgB, kModeFull, CKPT>(mapsB, p, tile / m.dtiles128, d0, 0, smem_raw);
+      channel_body<IO, CfgB, kModeFull, CKPT, Y>(mapsB, p, tile / m.dtiles128, d0, 0, smem_raw);
   }
 }
 

@@ -194,6 +194,34 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, i
 
 namespace {
 
+// AUTO's plan for a call: the channel kernel for many channels; for few, a long
+// sequence split across CTAs when `workspace_bytes` holds the segments' states, else
+// lanes over positions (measured on B300: the 130M-like layer, 3072 channels x 2048
+// fp32, runs 179 us over positions and 306 us in 8 segments; a 1536-channel x 131072
+// bf16 scan 3.7 ms over positions and 1.7 ms in 37 segments).
+ssm_algo auto_plan(const ScanCall& c, size_t workspace_bytes, int lc, SegPlan* seg) {
+  if (c.batch * c.dim >= kChannelKernelMinChannels) return SSM_ALGO_CHANNEL;
+  if (c.seqlen >= kSegMinSeqlen) *seg = seg_plan(c.batch, c.dim, c.seqlen, lc, false);
+  return (seg->nseg > 1 && workspace_bytes >= seg_workspace_bytes(c.batch, c.dim, c.dstate, *seg))
+             ? SSM_ALGO_SEGMENTED
+             : SSM_ALGO_CHUNK;
+}
+
+// The channel kernel with the split chosen per size becomes the mixed launch (dstate
+// 16) when its model cost is lower and the workspace holds its scheduler counters.
+ssm_algo mixed_upgrade(const ScanCall& c, size_t workspace_bytes, MixPlan* mix) {
+  if (c.dstate != 16 || workspace_bytes < kStatusBytes + kMixCounterBytes)
+    return SSM_ALGO_CHANNEL;
+  double split_cost = 0.0;
+  choose_lpc(c.batch, c.dim, c.dstate, &split_cost);
+  const MixPlan m = mix_plan(c.batch, c.dim);
+  if (m.use && m.k >= 1 && m.n_quarters > 0 && mix_cost(m) < split_cost) {
+    *mix = m;
+    return SSM_ALGO_CHANNEL_MIXED;
+  }
+  return SSM_ALGO_CHANNEL;
+}
+
 // The scan forward; `ckpt` (training forward) receives the state checkpoints, else null.
 ssm_status scan_fwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                          ssm_dtype io, const void* u, const void* delta, const float* delta_bias,
@@ -243,20 +271,7 @@ ssm_status scan_fwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seq
       return SSM_ERR_INVALID_ARG;
     }
   } else if (algo == SSM_ALGO_AUTO) {
-    if (c.batch * c.dim >= kChannelKernelMinChannels) {
-      algo = SSM_ALGO_CHANNEL;
-    } else {
-      // few channels: split a long sequence across CTAs when the caller's workspace
-      // holds the segments' states; else lanes over positions (measured on B300: the
-      // 130M-like layer, 3072 channels x 2048 fp32, runs 179 us over positions and
-      // 306 us in 8 segments; a 1536-channel x 131072 bf16 scan 3.7 ms over positions
-      // and 1.7 ms in 37 segments)
-      if (c.seqlen >= kSegMinSeqlen) seg = seg_plan(c.batch, c.dim, c.seqlen, lc, false);
-      algo = (seg.nseg > 1 &&
-              workspace_bytes >= seg_workspace_bytes(c.batch, c.dim, c.dstate, seg))
-                 ? SSM_ALGO_SEGMENTED
-                 : SSM_ALGO_CHUNK;
-    }
+    algo = auto_plan(c, workspace_bytes, lc, &seg);
   }
   if (algo != SSM_ALGO_CHUNK && !tma_eligible(c)) algo = SSM_ALGO_CHUNK;  // TMA kernels only
   // the channel kernel with the split chosen per size: one split for every CTA, or
@@ -271,15 +286,8 @@ ssm_status scan_fwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seq
       g_last_cuda_error = "workspace smaller than ssm_scan_fwd_algo_workspace_size()";
       return SSM_ERR_INVALID_ARG;
     }
-  } else if (algo == SSM_ALGO_CHANNEL && c.dstate == 16 &&
-             workspace_bytes >= kStatusBytes + kMixCounterBytes) {
-    double split_cost = 0.0;
-    choose_lpc(c.batch, c.dim, c.dstate, &split_cost);
-    const MixPlan m = mix_plan(c.batch, c.dim);
-    if (m.use && m.k >= 1 && m.n_quarters > 0 && mix_cost(m) < split_cost) {
-      mix = m;
-      algo = SSM_ALGO_CHANNEL_MIXED;
-    }
+  } else if (algo == SSM_ALGO_CHANNEL) {
+    algo = mixed_upgrade(c, workspace_bytes, &mix);
   }
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -289,6 +297,51 @@ ssm_status scan_fwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seq
                                : dispatch_scan<float>(c, algo, workspace, s, seg, mix);
   if (rs == SSM_OK) g_last_plan = describe_plan(c, algo, seg, mix);
   return rs;
+}
+
+// The gradient's own forward pass on the forward's kernels: the state entering every
+// kCkptPos positions into `ckpt`, no output (neither C nor z read).  It takes AUTO's
+// plan when that is the channel kernel (one split, the mixed launch or segments) and
+// returns SSM_ERR_UNSUPPORTED otherwise, where the gradient then forms its checkpoints
+// itself.  `scratch` holds the plan's scheduler counters or segment states; wait
+// timeouts go to `status`.
+ssm_status ckpt_forward(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, bool bf16,
+                        const void* u, const void* delta, const float* delta_bias, int softplus,
+                        const float* A, const void* B, const void* C, const float* h0, bool euler,
+                        float* ckpt, void* scratch, size_t scratch_bytes,
+                        ssm::DeviceStatus* status, cudaStream_t s) {
+  ScanCall c;
+  c.batch = batch;
+  c.dim = dim;
+  c.dstate = dstate;
+  c.seqlen = seqlen;
+  c.bf16 = bf16;
+  c.u = u;
+  c.delta = delta;
+  c.B = B;
+  c.C = C;
+  c.z = nullptr;
+  c.bias = delta_bias;
+  c.A = A;
+  c.D = nullptr;
+  c.h0 = h0;
+  c.h_last = nullptr;
+  c.y = nullptr;
+  c.ckpt = ckpt;
+  c.status = status;
+  c.softplus = softplus ? 1 : 0;
+  c.euler = euler;
+  if (!tma_eligible(c) || (c.batch * c.dim + 3) / 4 > INT32_MAX) return SSM_ERR_UNSUPPORTED;
+  const int lc = ChanShape<1>::RB / (c.bf16 ? 2 : 4);
+  SegPlan seg;
+  MixPlan mix;
+  ssm_algo algo = auto_plan(c, scratch_bytes, lc, &seg);
+  if (algo == SSM_ALGO_CHUNK) return SSM_ERR_UNSUPPORTED;
+  if (algo == SSM_ALGO_CHANNEL) algo = mixed_upgrade(c, scratch_bytes, &mix);
+  const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(ssm::DeviceStatus), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  return c.bf16 ? dispatch_scan<uint16_t>(c, algo, scratch, s, seg, mix)
+                : dispatch_scan<float>(c, algo, scratch, s, seg, mix);
 }
 
 }  // namespace
@@ -518,6 +571,21 @@ ssm_status scan_bwd_impl(int64_t batch, int64_t dim, int64_t dstate, int64_t seq
   p.cta_fast = ws + w.off_flags;
   p.ckpt_in = ckpt_in;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!ckpt_in && segments == 0) {
+    // the checkpoints from the forward's channel kernels (cheaper per update than the
+    // gradient kernel's own forward pass), in the workspace's checkpoint region; the
+    // dB/dC partials' region, unused until the gradient kernel, is their scratch, and
+    // the workspace's first bytes their status words
+    const ssm_status fs = ckpt_forward(
+        batch, dim, dstate, seqlen, io == SSM_DTYPE_BF16, u, delta, delta_bias, delta_softplus,
+        A, B, C, h0, disc == SSM_DISC_EULER, p.ckpt, ws + w.off_bc, w.off_a - w.off_bc,
+        reinterpret_cast<ssm::DeviceStatus*>(ws), s);
+    if (fs == SSM_OK) {
+      p.ckpt_in = p.ckpt;
+    } else if (fs != SSM_ERR_UNSUPPORTED) {
+      return fs;
+    }
+  }
   const bool euler = disc == SSM_DISC_EULER;
   float* dD_out = D ? dD : nullptr;
   if (io == SSM_DTYPE_BF16)

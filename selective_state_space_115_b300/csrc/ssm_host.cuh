@@ -104,6 +104,8 @@ struct ScanCall {
   float* h_last;
   void* y;
   float* ckpt = nullptr;  // training forward: state checkpoints (else null)
+  // where the kernels record wait timeouts (null: the first bytes of the workspace)
+  ssm::DeviceStatus* status = nullptr;
   int softplus;
   bool euler;  // input term dt * B instead of the ZOH form
 };
@@ -182,7 +184,7 @@ inline ScanParams make_params(const ScanCall& c, void* workspace) {
   p.bias = c.bias;
   p.h0 = c.h0;
   p.h_last = c.h_last;
-  p.status = static_cast<ssm::DeviceStatus*>(workspace);
+  p.status = c.status ? c.status : static_cast<ssm::DeviceStatus*>(workspace);
   p.u = c.u;
   p.delta = c.delta;
   p.z = c.z;

@@ -9,6 +9,18 @@
 
 namespace ssm_host {
 
+// The channel-kernel instantiation a pass runs: y only (the plain forward), y and the
+// state checkpoints (the training forward), or the checkpoints alone (the gradient's
+// own forward: a call without y, and without the gate, whose z it would not read).
+template <typename IO, typename Cfg, int MODE>
+static auto chan_kernel(const ScanCall& c, const ScanParams& p) {
+  if constexpr (!Cfg::GATE) {
+    if (!c.y) return ssm::scan_channel_kernel<IO, Cfg, MODE, true, false>;
+  }
+  return p.ckpt ? ssm::scan_channel_kernel<IO, Cfg, MODE, true, true>
+                : ssm::scan_channel_kernel<IO, Cfg, MODE, false, true>;
+}
+
 template <typename IO, int N, bool GATE, int LPC, bool EULER>
 ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t stream,
                           const SegPlan& seg = SegPlan()) {
@@ -27,6 +39,7 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
     return SSM_ERR_CUDA;
   }
   ScanParams p = make_params(c, workspace);
+  if (!c.y && (GATE || !p.ckpt)) return SSM_ERR_INVALID_ARG;  // a pass writes y or checkpoints
   p.dtiles = static_cast<int>((c.dim + Cfg::DT - 1) / Cfg::DT);
   const int64_t tiles = c.batch * p.dtiles;
   if (tiles * (seg.nseg > 1 ? seg.nseg : 1) > INT32_MAX) return SSM_ERR_INVALID_ARG;
@@ -42,8 +55,7 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
       p.seg_sum = reinterpret_cast<float*>(
           base + kStatusBytes + round_up(static_cast<size_t>(seg.nseg) * chans * N * 4, 256));
       auto k1 = ssm::scan_channel_kernel<IO, Cfg, ssm::kModeStates>;
-      auto k2 = p.ckpt ? ssm::scan_channel_kernel<IO, Cfg, ssm::kModeCarry, true>
-                       : ssm::scan_channel_kernel<IO, Cfg, ssm::kModeCarry, false>;
+      auto k2 = chan_kernel<IO, Cfg, ssm::kModeCarry>(c, p);
       cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            Cfg::SMEM_ALLOC);
       if (e == cudaSuccess)
@@ -60,8 +72,7 @@ ssm_status launch_channel(const ScanCall& c, void* workspace, cudaStream_t strea
       return SSM_OK;
     }
   }
-  auto kern = p.ckpt ? ssm::scan_channel_kernel<IO, Cfg, ssm::kModeFull, true>
-                     : ssm::scan_channel_kernel<IO, Cfg, ssm::kModeFull, false>;
+  auto kern = chan_kernel<IO, Cfg, ssm::kModeFull>(c, p);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::SMEM_ALLOC);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel)");
@@ -107,8 +118,12 @@ ssm_status launch_mixed(const ScanCall& c, void* workspace, cudaStream_t stream,
   cudaError_t e = cudaMemsetAsync(sched.counters, 0, kMixCounterBytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scheduler counters)");
   constexpr int smem = CfgA::SMEM_ALLOC > CfgB::SMEM_ALLOC ? CfgA::SMEM_ALLOC : CfgB::SMEM_ALLOC;
-  auto kern = p.ckpt ? ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, true>
-                     : ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, false>;
+  if (!c.y && (GATE || !p.ckpt)) return SSM_ERR_INVALID_ARG;  // a pass writes y or checkpoints
+  auto kern = p.ckpt ? ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, true, true>
+                     : ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, false, true>;
+  if constexpr (!GATE) {
+    if (!c.y) kern = ssm::scan_channel_mixed_kernel<IO, CfgA, CfgB, true, false>;
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(scan_channel_mixed)");
   const unsigned grid = static_cast<unsigned>(m.n_tiles + m.n_quarters);

@@ -157,3 +157,52 @@ def test_gradient_from_checkpoints_vanishing_steps():
                           dh_last=gr["dh_last"], nthreads=NTHREADS)
     for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dh0"):
         assert rel_err(from_torch(g[k]), ref[k]) <= TOL[io], k
+
+
+# Shapes whose AUTO forward plan is the channel kernel (batch * dim >= 8192: four, two
+# and one lanes per channel, both discretisations) or the segmented scan (few channels,
+# L >= 8192): the gradient called without checkpoints forms them on those kernels, in
+# their checkpoint-only mode, instead of in its own forward pass.
+CKPT_FORWARD_CASES = [
+    # io, batch, dim, dstate, seqlen, gate, disc
+    (W.BF16, 2, 4096, 16, 256, True, "zoh"),
+    (W.F32, 1, 8192, 8, 128, False, "zoh"),
+    (W.BF16, 4, 2048, 4, 64, True, "euler"),
+    (W.BF16, 1, 64, 16, 8192, True, "zoh"),
+]
+
+
+@pytest.mark.parametrize("io,batch,dim,dstate,seqlen,gate,disc", CKPT_FORWARD_CASES)
+def test_gradient_checkpoints_from_forward_kernels(io, batch, dim, dstate, seqlen, gate, disc):
+    """ssm_scan_bwd without checkpoints where the forward's kernels form them: against
+    the oracle's gradient, and bit for bit against the gradient from the training
+    forward's checkpoints (the same kernels, the same plan, the same states)."""
+    import torch
+    cfg = W.ScanConfig("t", batch, dim, dstate, seqlen, io, gate=gate, dt_bias=True,
+                       d_skip="normal", description="")
+    x = W.make_scan_inputs(cfg, seed=seqlen + dim, with_h0=True)
+    gr = W.make_scan_grads(cfg, seed=seqlen + dim)
+    t = dev_inputs(x, io)
+    ck = torch.full(S().ckpt_shape(batch, dim, dstate, seqlen), float("nan"),
+                    dtype=torch.float32, device="cuda")
+    S().scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                 delta_bias=t["delta_bias"], h0=t["h0"], discretization=disc, ckpt=ck)
+    dy, dhl = torch_io(gr["dy"], io), torch_f32(gr["dh_last"])
+    kw = dict(D=t["D"], z=t["z"], delta_bias=t["delta_bias"], h0=t["h0"], dh_last=dhl,
+              discretization=disc)
+    g = S().scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], dy, **kw)
+    gt = S().scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], dy, ckpt=ck, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(f64(x["u"], io), f64(x["delta"], io), x["A"], f64(x["B"], io),
+                          f64(x["C"], io), f64(gr["dy"], io), D=x["D"], z=f64(x.get("z"), io),
+                          delta_bias=x["delta_bias"], h0=x["h0"], dh_last=gr["dh_last"],
+                          nthreads=NTHREADS, discretization=disc)
+    for k in GRAD_KEYS:
+        if ref.get(k) is None:
+            continue
+        got = from_torch(g[k])
+        assert np.isfinite(got).all(), k
+        e = rel_err(got, ref[k])
+        print(f"{io} b{batch} d{dim} n{dstate} L{seqlen} {disc} {k}: max rel err {e:.3e}")
+        assert e <= TOL[io], (k, e)
+        assert np.array_equal(got, from_torch(gt[k])), k
