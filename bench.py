@@ -731,6 +731,15 @@ def bwd_split(cfg) -> bool:
     return (cfg.batch * ((cfg.dim + 31) // 32) < 2 * SM_COUNT) and cfg.seqlen >= 512
 
 
+def bwd_ckpt_pass_launches(cfg) -> int:
+    """Kernels of the gradient's checkpoint pass on the forward's kernels: one for the
+    channel kernel (batch * dim >= 8192), two for the segmented plan (a long sequence
+    over few channels); none where the gradient kernel forms its checkpoints itself."""
+    if cfg.batch * cfg.dim >= 8192:
+        return 1
+    return 2 if cfg.seqlen >= 8192 else 0
+
+
 def run_train_step(dev, S, iters=10):
     """A training step of the bench workload through the C ABI: the forward that writes
     the state checkpoints (ssm_scan_fwd_train) and the gradient that reads them
@@ -814,19 +823,23 @@ def run_bwd(dev, S, iters=20):
     return {"workload": f"gradient of the {CFG.name} scan (du, ddelta, dz, dA, dB, dC, dD, "
                         "ddelta_bias, dh0)",
             "ms_per_call": ms, "value": CFG.elements / (ms * 1e-3), "unit": "elements/s",
-            # bf16 ZOH: the classify kernel, then the gradient kernel as two launches
-            # (the CTAs on the series coefficients, then those on the fast ones); the
-            # segments' first pass when the sequence is split (as many again); the two
-            # fixed-order reductions
-            "gpu_launches": ((1 if CFG.io == W.BF16 else 0)
+            "checkpoints": ("the forward's kernels in a checkpoint-only pass"
+                            if bwd_ckpt_pass_launches(CFG) else "the gradient kernel's own "
+                            "forward pass"),
+            # the checkpoint pass; bf16 ZOH: the classify kernel, then the gradient kernel
+            # as two launches (the CTAs on the series coefficients, then those on the fast
+            # ones); the segments' first pass when the sequence is split (as many again);
+            # the two fixed-order reductions
+            "gpu_launches": (bwd_ckpt_pass_launches(CFG) + (1 if CFG.io == W.BF16 else 0)
                              + (2 if CFG.io == W.BF16 else 1) * (2 if bwd_split(CFG) else 1)
                              + 2) * iters,
             "roofline": {"bound": "alu", "achieved": texp, "peak": ex2_peak, "unit": "Texp/s",
                          "frac": texp / ex2_peak,
                          "traffic": profiled_traffic("scan_bwd_2p8b") if CFG.name == "2p8b"
                          else None,
-                         "note": "one ex2 per state update, as the forward; the kernel also "
-                                 "recomputes the forward states (two more passes of ex2)"},
+                         "note": "one ex2 per state update, as the forward; the "
+                                 "checkpoint pass and the gradient kernel's recompute of each "
+                                 "block's states add two more passes of ex2"},
             "hbm": {"bytes_per_call": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
                     "frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": kind}}
 
