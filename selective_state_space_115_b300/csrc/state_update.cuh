@@ -122,17 +122,23 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
       const float a0 = Av[4 * k + i];
       const float q = s * a0;
       const float ahw = ex2(q);
-      const float em1 = exp2m1_accurate(q, ahw);
       float hn;
       if constexpr (Cfg::EULER) {
+        const float em1 = exp2m1_accurate(q, ahw);
         const float abar = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
         hn = fmaf(abar, hv[4 * k + i], (s * kLn2) * (Bv[i] * uv));
       } else {
-        // h + coef (A h + B u) = Abar h + coef B u with coef = (Abar - 1) / A (dt at
-        // A == 0, where the bracket is B u); 1/A from the hardware reciprocal
-        const float coef = (a0 == 0.0f) ? s * kLn2 : em1 * rcp(a0);
+        // h + coef (A h + B u) = Abar h + coef B u with coef = (Abar - 1) / A = s f(q),
+        // f(q) = (2^q - 1) / q: near zero the Taylor series of 2^q - 1 (coefficients
+        // ln2^k / k!) without its last factor q, so that f(0) = ln 2 gives coef = dt at
+        // A == 0 (where the bracket is B u); beyond, (Abar - 1) / q with the hardware
+        // reciprocal
+        const float fser = fmaf(fmaf(fmaf(0.00961812910762848f, q, 0.05550410866482158f), q,
+                                     0.24022650695910071f),
+                                q, 0.69314718055994531f);
+        const float f = (fabsf(q) < kExpm1SeriesMaxQ) ? fser : (ahw - 1.0f) * rcp(q);
         const float hh = hv[4 * k + i];
-        hn = fmaf(coef, fmaf(a0, hh, Bv[i] * uv), hh);
+        hn = fmaf(s * f, fmaf(a0, hh, Bv[i] * uv), hh);
       }
       hv[4 * k + i] = hn;
       if (i & 1)
