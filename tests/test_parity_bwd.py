@@ -100,10 +100,13 @@ def test_bwd_euler(io):
           what=f"euler {io}")
 
 
+# (2, 40, 256): the gradient kernel forms its checkpoints; (2, 4096, 64): 8192 channels,
+# the forward's channel kernel forms them in its checkpoint-only pass
+@pytest.mark.parametrize("dim,seqlen", [(40, 256), (4096, 64)])
 @pytest.mark.parametrize("io", [W.F32, W.BF16])
-def test_bwd_optional_arguments_absent(io):
+def test_bwd_optional_arguments_absent(io, dim, seqlen):
     """No D, bias, gate, h0 or dh_last; delta used as dt directly (no softplus)."""
-    cfg = W.ScanConfig("t", 2, 40, 16, 256, io, gate=False, dt_bias=False, d_skip="normal",
+    cfg = W.ScanConfig("t", 2, dim, 16, seqlen, io, gate=False, dt_bias=False, d_skip="normal",
                        description="")
     x = W.make_scan_inputs(cfg, seed=5)
     x["D"] = None
@@ -113,7 +116,7 @@ def test_bwd_optional_arguments_absent(io):
     gr = W.make_scan_grads(cfg, seed=5)
     got = gpu_bwd(x, gr, io, softplus=False, with_dh_last=False)
     ref = oracle_bwd(x, gr, io, softplus=False, with_dh_last=False)
-    check(got, ref, io, what=f"no options {io}")
+    check(got, ref, io, what=f"no options {io} d{dim} L{seqlen}")
 
 
 @pytest.mark.parametrize("io", [W.F32, W.BF16])
