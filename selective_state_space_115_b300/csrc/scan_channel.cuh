@@ -464,8 +464,27 @@ __device__ __forceinline__ void chan_chunk(const uint8_t* stage, IO* yrow, const
     if constexpr (Cfg::GATE) {
       float zm[PB];
       lds_vals<IO, PB>(tz + off + pofs, zm);
+      if constexpr (ACC) {
 #pragma unroll
-      for (int k = 0; k < PB; ++k) ym[k] *= (ACC ? silu_accurate(zm[k]) : silu_fast(zm[k]));
+        for (int k = 0; k < PB; ++k) ym[k] *= silu_accurate(zm[k]);
+      } else if constexpr (PB % 2 == 0) {
+        // y silu(z) = g + g tanh(h) with h = z / 2, g = y h (the hardware tanh), in
+        // packed pairs: the same operations as the scalar form below
+#pragma unroll
+        for (int k = 0; k < PB; k += 2) {
+          const f2 h = mul2(mk2(zm[k], zm[k + 1]), mk2(0.5f, 0.5f));
+          const f2 g = mul2(mk2(ym[k], ym[k + 1]), h);
+          const f2 r = fma2(g, mk2(tanh_hw(h.x), tanh_hw(h.y)), g);
+          ym[k] = r.x;
+          ym[k + 1] = r.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < PB; ++k) {
+          const float h = zm[k] * 0.5f, g = ym[k] * h;
+          ym[k] = fmaf(g, tanh_hw(h), g);
+        }
+      }
     }
     // (the row length is a multiple of the block, as the TMA row pitch requires, so a
     // block lies wholly inside the sequence or wholly past it)
