@@ -150,6 +150,18 @@ __device__ __forceinline__ float dcoef_dA(float dt, float q, float ra, float aba
   return (fabsf(q) < kExpm1SeriesMaxQ) ? series : direct;
 }
 
+// dcoef_dA<true> for a pair of states in packed f32x2 (the same operations, so the
+// same bits); `ncoef` is -coef, exactly
+__device__ __forceinline__ f2 dcoef_dA_short2(f2 dtsq, f2 dt, f2 q, f2 ra, f2 abar, f2 ncoef) {
+  const f2 ps = fma2(fma2(q, mk2(0.06005662673977513f, 0.06005662673977513f),
+                          mk2(0.23104906018664842f, 0.23104906018664842f)),
+                     q, mk2(0.5f, 0.5f));
+  const f2 series = mul2(dtsq, ps);
+  const f2 direct = mul2(fma2(dt, abar, ncoef), ra);
+  return mk2((fabsf(q.x) < kExpm1SeriesMaxQ) ? series.x : direct.x,
+             (fabsf(q.y) < kExpm1SeriesMaxQ) ? series.y : direct.y);
+}
+
 // the ZOH (or Euler) input coefficient for one state: FAST takes Abar - 1
 // directly (bf16 io with |A| >= 1/8, as the forward's fast path), otherwise the
 // expm1 series near zero and the dt limit at A = 0
@@ -371,6 +383,7 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
                                           float* WB, unsigned char* OUT, int chl, int part,
                                           int lane, int warp, int n0, int l0, float Dd,
                                           const float (&a)[Cfg::NS], const float (&ra)[Cfg::NS],
+                                          const float (&nra)[Cfg::NS],
                                           const float (&he)[Cfg::NS], float (&g)[Cfg::NS],
                                           float (&an)[Cfg::NS], float (&dA)[Cfg::NS],
                                           float& dD_acc) {
@@ -394,14 +407,42 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
         ld_states<NS>(Bt + pp * Cfg::BCS + n0, Bv);
         ld_states<NS>(Ct + pp * Cfg::BCS + n0, Cv);
         float y = 0.0f;
+        if constexpr (NS % 2 == 0) {
+          // state pairs in packed f32x2: the per-state operations of the scalar form
+          // below, the contraction summed per pair then across
+          const f2 s2 = mk2(s, s), u2 = mk2(uf, uf);
+          f2 y2 = mk2(0.0f, 0.0f);
 #pragma unroll
-        for (int k = 0; k < NS; ++k) {
-          const float q = s * a[k];
-          const float ab = ex2(q);
-          const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
-          h[k] = fmaf(ab, h[k], coef * (Bv[k] * uf));
-          traj[pp][k] = h[k];
-          y = fmaf(Cv[k], h[k], y);
+          for (int k = 0; k < NS; k += 2) {
+            const f2 a2 = mk2(a[k], a[k + 1]);
+            const f2 q = mul2(s2, a2);
+            const f2 ab = mk2(ex2(q.x), ex2(q.y));
+            f2 coef;
+            if constexpr (FAST && !Cfg::EULER) {
+              coef = fma2(ab, mk2(ra[k], ra[k + 1]), mk2(nra[k], nra[k + 1]));
+            } else {
+              coef = mk2(bwd_coef<Cfg::EULER, FAST>(q.x, dt, a[k], ra[k], ab.x),
+                         bwd_coef<Cfg::EULER, FAST>(q.y, dt, a[k + 1], ra[k + 1], ab.y));
+            }
+            const f2 hn = fma2(ab, mk2(h[k], h[k + 1]),
+                               mul2(coef, mul2(mk2(Bv[k], Bv[k + 1]), u2)));
+            h[k] = hn.x;
+            h[k + 1] = hn.y;
+            traj[pp][k] = hn.x;
+            traj[pp][k + 1] = hn.y;
+            y2 = fma2(mk2(Cv[k], Cv[k + 1]), hn, y2);
+          }
+          y = y2.x + y2.y;
+        } else {
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            const float q = s * a[k];
+            const float ab = ex2(q);
+            const float coef = bwd_coef<Cfg::EULER, FAST>(q, dt, a[k], ra[k], ab);
+            h[k] = fmaf(ab, h[k], coef * (Bv[k] * uf));
+            traj[pp][k] = h[k];
+            y = fmaf(Cv[k], h[k], y);
+          }
         }
         RED[chl * Cfg::REDS + pp * 8 + part] = y;
       }
@@ -452,6 +493,67 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
       float dBv[NS], dCv[NS], Bs[NS], Cs[NS];
       ld_states<NS>(Bt + pp * Cfg::BCS + n0, Bs);
       ld_states<NS>(Ct + pp * Cfg::BCS + n0, Cs);
+      if constexpr (NS % 2 == 0) {
+        // state pairs in packed f32x2: the per-state operations of the scalar form
+        // below; du and ddt summed per pair then across
+        const f2 s2 = mk2(s, s), dt2 = mk2(dt, dt), u2 = mk2(uf, uf), dy2 = mk2(dy0, dy0);
+        const f2 dtsq = mk2(dt * dt, dt * dt);
+        f2 du2 = mk2(0.0f, 0.0f), ddt2 = mk2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < NS; k += 2) {
+          const f2 hp = (pp > 0) ? mk2(traj[pp > 0 ? pp - 1 : 0][k], traj[pp > 0 ? pp - 1 : 0][k + 1])
+                                 : mk2(he[k], he[k + 1]);
+          const f2 a2 = mk2(a[k], a[k + 1]), ra2 = mk2(ra[k], ra[k + 1]);
+          const f2 q = mul2(s2, a2);
+          const f2 ab = mk2(ex2_fresh(q.x), ex2_fresh(q.y));
+          f2 coef;
+          if constexpr (FAST && !Cfg::EULER) {
+            coef = fma2(ab, ra2, mk2(nra[k], nra[k + 1]));
+          } else {
+            coef = mk2(bwd_coef<Cfg::EULER, FAST>(q.x, dt, a[k], ra[k], ab.x),
+                       bwd_coef<Cfg::EULER, FAST>(q.y, dt, a[k + 1], ra[k + 1], ab.y));
+          }
+          const f2 B2 = mk2(Bs[k], Bs[k + 1]);
+          const f2 gk = fma2(mk2(g[k], g[k + 1]), mk2(an[k], an[k + 1]),
+                             mul2(mk2(Cs[k], Cs[k + 1]), dy2));  // dLoss/dh at this position
+          const f2 dC = mul2(dy2, mk2(traj[pp][k], traj[pp][k + 1]));
+          const f2 gc = mul2(gk, coef);
+          const f2 dB = mul2(gc, u2);
+          du2 = fma2(gc, B2, du2);
+          const f2 bu = mul2(B2, u2);
+          const f2 ga = mul2(gk, ab);
+          const f2 gdt = mul2(ga, dt2);
+          const f2 d1 = fma2(gdt, hp, mk2(dA1[k], dA1[k + 1]));
+          dA1[k] = d1.x;
+          dA1[k + 1] = d1.y;
+          if constexpr (Cfg::EULER) {
+            ddt2 = fma2(mul2(ga, a2), hp, fma2(gk, bu, ddt2));
+          } else {
+            ddt2 = fma2(ga, fma2(a2, hp, bu), ddt2);
+            f2 dc;
+            if constexpr (FAST) {
+              dc = dcoef_dA_short2(dtsq, dt2, q, ra2, ab,
+                                   fma2(ab, mk2(nra[k], nra[k + 1]), ra2));  // -coef
+            } else {
+              dc = mk2(dcoef_dA<false>(dt, q.x, ra[k], ab.x, coef.x),
+                       dcoef_dA<false>(dt, q.y, ra[k + 1], ab.y, coef.y));
+            }
+            const f2 d2 = fma2(mul2(gk, dc), bu, mk2(dA2[k], dA2[k + 1]));
+            dA2[k] = d2.x;
+            dA2[k + 1] = d2.y;
+          }
+          dCv[k] = dC.x;
+          dCv[k + 1] = dC.y;
+          dBv[k] = dB.x;
+          dBv[k + 1] = dB.y;
+          g[k] = gk.x;
+          g[k + 1] = gk.y;
+          an[k] = ab.x;
+          an[k + 1] = ab.y;
+        }
+        du_p = du2.x + du2.y;
+        ddt_p = ddt2.x + ddt2.y;
+      } else {
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         const float hp = (pp > 0) ? traj[pp > 0 ? pp - 1 : 0][k] : he[k];
@@ -479,6 +581,7 @@ __device__ __forceinline__ void bwd_block(const BwdParams& p, const unsigned cha
         }
         g[k] = gk;
         an[k] = ab;
+      }
       }
       RED[chl * Cfg::REDS + pp * 8 + part] = du_p;
       RED[chl * Cfg::REDS + pp * 8 + 4 + part] = ddt_p;
@@ -681,6 +784,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
     a[k] = __ldg(p.A + static_cast<int64_t>(dc) * N + n0 + (k ^ perm));
     ra[k] = (a[k] != 0.0f) ? 1.0f / a[k] : 0.0f;
   }
+  float nra[NS];  // -1/A: the packed coefficient (Abar - 1) / A = fma(Abar, 1/A, -1/A)
+#pragma unroll
+  for (int k = 0; k < NS; ++k) nra[k] = -ra[k];
   const float bias = p.bias ? __ldg(p.bias + dc) : 0.0f;
   const float Dd = p.D ? __ldg(p.D + dc) : 0.0f;
 
@@ -792,7 +898,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 4) scan_bwd_kernel(const BwdPara
       bwd_prologue<Cfg>(p, stage(buf), chl, part, bias, S, SG, p.softplus != 0);
       __syncwarp();
       bwd_block<Cfg, FAST>(p, stage(buf), bt(buf), ct(buf), S, DY0, RED, WB, OUT, chl, part,
-                           lane, warp, n0, l0, Dd, a, ra, he, g, an, dA, dD_acc);
+                           lane, warp, n0, l0, Dd, a, ra, nra, he, g, an, dA, dD_acc);
       __syncwarp();
       // per-position totals over the channel's four lanes: du (with the D skip) and
       // ddelta (through the softplus) for this lane's positions part*kBwdPpl ..
