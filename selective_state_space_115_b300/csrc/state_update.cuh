@@ -117,34 +117,50 @@ __device__ __forceinline__ void update_channel(const UpdateParams& p, int64_t b,
     float Bv[4], Cv[4];
     load4<IO, Cfg::VEC>(Bp + g, Bv);
     load4<IO, Cfg::VEC>(Cp + g, Cv);
+    if constexpr (Cfg::EULER) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a0 = Av[4 * k + i];
-      const float q = s * a0;
-      const float ahw = ex2(q);
-      float hn;
-      if constexpr (Cfg::EULER) {
+      for (int i = 0; i < 4; ++i) {
+        const float a0 = Av[4 * k + i];
+        const float q = s * a0;
+        const float ahw = ex2(q);
         const float em1 = exp2m1_accurate(q, ahw);
         const float abar = (fabsf(q) < kExpm1SeriesMaxQ) ? 1.0f + em1 : ahw;
-        hn = fmaf(abar, hv[4 * k + i], (s * kLn2) * (Bv[i] * uv));
-      } else {
-        // h + coef (A h + B u) = Abar h + coef B u with coef = (Abar - 1) / A = s f(q),
-        // f(q) = (2^q - 1) / q: near zero the Taylor series of 2^q - 1 (coefficients
-        // ln2^k / k!) without its last factor q, so that f(0) = ln 2 gives coef = dt at
-        // A == 0 (where the bracket is B u); beyond, (Abar - 1) / q with the hardware
-        // reciprocal
-        const float fser = fmaf(fmaf(fmaf(0.00961812910762848f, q, 0.05550410866482158f), q,
-                                     0.24022650695910071f),
-                                q, 0.69314718055994531f);
-        const float f = (fabsf(q) < kExpm1SeriesMaxQ) ? fser : (ahw - 1.0f) * rcp(q);
-        const float hh = hv[4 * k + i];
-        hn = fmaf(s * f, fmaf(a0, hh, Bv[i] * uv), hh);
+        const float hn = fmaf(abar, hv[4 * k + i], (s * kLn2) * (Bv[i] * uv));
+        hv[4 * k + i] = hn;
+        if (i & 1)
+          acc1 = fmaf(Cv[i], hn, acc1);
+        else
+          acc0 = fmaf(Cv[i], hn, acc0);
       }
-      hv[4 * k + i] = hn;
-      if (i & 1)
-        acc1 = fmaf(Cv[i], hn, acc1);
-      else
-        acc0 = fmaf(Cv[i], hn, acc0);
+    } else {
+      // h + coef (A h + B u) = Abar h + coef B u with coef = (Abar - 1) / A = s f(q),
+      // f(q) = (2^q - 1) / q: near zero the Taylor series of 2^q - 1 (coefficients
+      // ln2^k / k!) without its last factor q, so that f(0) = ln 2 gives coef = dt at
+      // A == 0 (where the bracket is B u); beyond, (Abar - 1) / q with the hardware
+      // reciprocal.  States in packed f32x2 pairs (even, odd), which are also the two
+      // partial sums of the contraction.
+      const f2 s2 = mk2(s, s), u2 = mk2(uv, uv);
+      f2 acc2 = mk2(acc0, acc1);
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const f2 a2 = mk2(Av[4 * k + i], Av[4 * k + i + 1]);
+        const f2 q = mul2(s2, a2);
+        const f2 ahw = mk2(ex2(q.x), ex2(q.y));
+        const f2 fser = fma2(fma2(fma2(mk2(0.00961812910762848f, 0.00961812910762848f), q,
+                                       mk2(0.05550410866482158f, 0.05550410866482158f)),
+                                  q, mk2(0.24022650695910071f, 0.24022650695910071f)),
+                             q, mk2(0.69314718055994531f, 0.69314718055994531f));
+        const f2 fbig = mul2(sub2(ahw, mk2(1.0f, 1.0f)), mk2(rcp(q.x), rcp(q.y)));
+        const f2 f = mk2((fabsf(q.x) < kExpm1SeriesMaxQ) ? fser.x : fbig.x,
+                         (fabsf(q.y) < kExpm1SeriesMaxQ) ? fser.y : fbig.y);
+        const f2 hh = mk2(hv[4 * k + i], hv[4 * k + i + 1]);
+        const f2 hn = fma2(mul2(s2, f), fma2(a2, hh, mul2(mk2(Bv[i], Bv[i + 1]), u2)), hh);
+        hv[4 * k + i] = hn.x;
+        hv[4 * k + i + 1] = hn.y;
+        acc2 = fma2(mk2(Cv[i], Cv[i + 1]), hn, acc2);
+      }
+      acc0 = acc2.x;
+      acc1 = acc2.y;
     }
   }
 #pragma unroll
