@@ -169,6 +169,7 @@ CKPT_FORWARD_CASES = [
     (W.F32, 1, 8192, 8, 128, False, "zoh"),
     (W.BF16, 4, 2048, 4, 64, True, "euler"),
     (W.BF16, 1, 64, 16, 8192, True, "zoh"),
+    (W.F32, 8, 5120, 16, 64, True, "zoh"),   # the mixed split (2 one-lane CTAs per SM + quarters)
 ]
 
 
