@@ -73,3 +73,12 @@ def test_link_floor():
     f = bench.link_fraction(link, h2d=500_000_000, d2h=100_000_000, e2e_s=0.02)
     assert abs(f["floor_ms"] - 10.0) < 1e-9 and abs(f["frac"] - 0.5) < 1e-9
     assert bench.link_fraction(None, 1, 1, 1.0) is None
+
+
+def test_gradient_checkpoint_pass_launches():
+    # the forward's kernels form the gradient's checkpoints where AUTO runs the forward
+    # on the channel kernel (one launch, or the mixed split) or the segmented plan (its
+    # two passes); elsewhere the gradient kernel forms them itself (no launch)
+    assert bench.bwd_ckpt_pass_launches(W.SCAN_CONFIGS["2p8b"]) == 1
+    assert bench.bwd_ckpt_pass_launches(W.SCAN_CONFIGS["long"]) == 2
+    assert bench.bwd_ckpt_pass_launches(W.SCAN_CONFIGS["130m"]) == 0
